@@ -1,0 +1,225 @@
+"""ctypes binding of libeagle_draft.so (include/eagle_draft.h).
+
+Argument marshalling only: every step of the draft tree runs in the library's CUDA
+kernels.  torch is used for device memory and streams; tensors are passed as raw
+pointers.  ``load()`` raises if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from .configs import DraftConfig
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libeagle_draft.so")
+
+EAGLE_OK, EAGLE_ERR_INVALID_ARG, EAGLE_ERR_UNSUPPORTED, EAGLE_ERR_OOM, EAGLE_ERR_CUDA, EAGLE_ERR_DEVICE = range(6)
+DTYPE_F32, DTYPE_BF16 = 0, 1
+TREE_STATIC, TREE_DYNAMIC = 1, 2
+FEAT_F, FEAT_FUSED = 1, 3
+FLAG_NO_GRAPH, FLAG_NO_PDL = 1, 2
+MAX_DEPTH = 16
+DEVERR_TIMEOUT, DEVERR_PREFIX = 1, 2
+
+
+class Config(C.Structure):
+    _fields_ = [("d", C.c_int32), ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("d_ff", C.c_int32), ("vocab", C.c_int32),
+                ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("dtype", C.c_int32),
+                ("tree_kind", C.c_int32), ("feat_kind", C.c_int32), ("depth", C.c_int32),
+                ("k", C.c_int32), ("m", C.c_int32), ("branching", C.c_int32 * MAX_DEPTH),
+                ("max_batch", C.c_int32), ("max_prefix", C.c_int32), ("flags", C.c_int32)]
+
+
+class Weights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("embed", "w_fc", "w_fc3", "attn_norm", "w_qkv", "w_o",
+                                         "mlp_norm", "w_gate", "w_up", "w_down", "w_lm")]
+
+
+class Inputs(C.Structure):
+    _fields_ = [("B", C.c_int32), ("root_feat", C.c_void_p), ("root_tok", C.c_void_p),
+                ("k_cache", C.c_void_p), ("v_cache", C.c_void_p), ("cu_seqlens", C.c_void_p)]
+
+
+class Outputs(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("tokens", "parents", "positions", "logv", "mask")]
+
+
+TRACE_FIELDS = ("h", "q", "attn", "y", "a", "lse", "children", "child_logp", "frontier",
+                "final_nodes", "tree_k", "tree_v")
+
+
+class Trace(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in TRACE_FIELDS]
+
+
+class Info(C.Structure):
+    _fields_ = [("slots", C.c_int32), ("generated", C.c_int32), ("rows", C.c_int32),
+                ("n_max", C.c_int32), ("k_max", C.c_int32), ("f_max", C.c_int32),
+                ("launches_per_tree", C.c_int32), ("tensor_core_gemm", C.c_int32),
+                ("workspace_bytes", C.c_int64)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (python -m "
+                           "eagle_speculative_decoding_03_gb300.build)")
+    lib = C.CDLL(path)
+    P = C.c_void_p
+    lib.eagle_draft_create.argtypes = [C.POINTER(Config), C.POINTER(Weights), C.POINTER(P)]
+    lib.eagle_draft_create.restype = C.c_int
+    lib.eagle_draft_tree.argtypes = [P, C.POINTER(Inputs), C.POINTER(Outputs), C.POINTER(Trace), P]
+    lib.eagle_draft_tree.restype = C.c_int
+    lib.eagle_draft_lm_head_topk.argtypes = [P, P, C.c_int32, C.c_int32, P, P, P, P]
+    lib.eagle_draft_lm_head_topk.restype = C.c_int
+    lib.eagle_draft_query.argtypes = [P, C.POINTER(Info)]
+    lib.eagle_draft_query.restype = C.c_int
+    lib.eagle_draft_check.argtypes = [P, C.POINTER(C.c_uint32)]
+    lib.eagle_draft_check.restype = C.c_int
+    lib.eagle_draft_destroy.argtypes = [P]
+    lib.eagle_draft_destroy.restype = None
+    lib.eagle_draft_last_error.argtypes = []
+    lib.eagle_draft_last_error.restype = C.c_char_p
+    _lib = lib
+    return lib
+
+
+class EagleError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"eagle status {status}: {msg}")
+        self.status = status
+
+
+def _check(status: int):
+    if status != EAGLE_OK:
+        raise EagleError(status, load().eagle_draft_last_error().decode())
+
+
+def make_config(cfg: DraftConfig, max_batch: int | None = None, max_prefix: int | None = None,
+                flags: int = 0) -> Config:
+    c = Config()
+    c.d, c.n_heads, c.n_kv_heads, c.head_dim = cfg.d, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+    c.d_ff, c.vocab, c.rms_eps, c.rope_theta = cfg.d_ff, cfg.vocab, cfg.rms_eps, cfg.rope_theta
+    c.dtype = DTYPE_BF16 if cfg.dtype == "bf16" else DTYPE_F32
+    c.tree_kind = TREE_STATIC if cfg.tree == "static" else TREE_DYNAMIC
+    c.feat_kind = FEAT_FUSED if cfg.feat == "fused" else FEAT_F
+    c.depth, c.k, c.m = cfg.depth, cfg.k, cfg.m
+    for i, b in enumerate(cfg.branching):
+        c.branching[i] = b
+    c.max_batch = cfg.B if max_batch is None else max_batch
+    c.max_prefix = cfg.prefix[1] if max_prefix is None else max_prefix
+    c.flags = flags
+    return c
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def device_weights(W: dict, device="cuda"):
+    """numpy weights (bf16 as uint16 bits) -> device tensors (bf16 kept as int16 bits)."""
+    import torch
+    out = {}
+    for k, v in W.items():
+        arr = v.view(np.int16) if v.dtype == np.uint16 else v
+        out[k] = torch.from_numpy(np.ascontiguousarray(arr)).to(device)
+    return out
+
+
+def device_inputs(I: dict, device="cuda"):
+    return device_weights(I, device)
+
+
+class EagleDraft:
+    """One handle of the C library bound to device weights (torch tensors)."""
+
+    def __init__(self, cfg: DraftConfig, dW: dict, max_batch: int | None = None,
+                 max_prefix: int | None = None, flags: int = 0):
+        lib = load()
+        self.cfg = cfg
+        self._dW = dW  # keep the weights alive
+        w = Weights(**{n: _ptr(dW.get(n)) for n, _ in Weights._fields_})
+        self._ccfg = make_config(cfg, max_batch, max_prefix, flags)
+        h = C.c_void_p()
+        _check(lib.eagle_draft_create(C.byref(self._ccfg), C.byref(w), C.byref(h)))
+        self.h = h
+        info = Info()
+        _check(lib.eagle_draft_query(self.h, C.byref(info)))
+        self.info = {n: getattr(info, n) for n, _ in Info._fields_}
+
+    def close(self):
+        if getattr(self, "h", None):
+            load().eagle_draft_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc_outputs(self, B: int, device="cuda"):
+        import torch
+        S = self.info["slots"]
+        return {"tokens": torch.empty((B, S), dtype=torch.int32, device=device),
+                "parents": torch.empty((B, S), dtype=torch.int32, device=device),
+                "positions": torch.empty((B, S), dtype=torch.int32, device=device),
+                "logv": torch.empty((B, S), dtype=torch.float32, device=device),
+                "mask": torch.empty((B, S, S), dtype=torch.uint8, device=device)}
+
+    def alloc_trace(self, device="cuda"):
+        import torch
+        c, i = self.cfg, self.info
+        D, N, k = c.depth, i["n_max"], i["k_max"]
+        Bm, hq = self._ccfg.max_batch, c.n_heads * c.head_dim
+        f = dict(dtype=torch.float32, device=device)
+        n = dict(dtype=torch.int32, device=device)
+        return {"h": torch.zeros((D, N, c.d), **f), "q": torch.zeros((D, N, hq), **f),
+                "attn": torch.zeros((D, N, hq), **f), "y": torch.zeros((D, N, c.d), **f),
+                "a": torch.zeros((D, N, c.d), **f), "lse": torch.zeros((D, N), **f),
+                "children": torch.full((D, N, k), -1, **n), "child_logp": torch.zeros((D, N, k), **f),
+                "frontier": torch.full((D, Bm, i["f_max"]), -1, **n),
+                "final_nodes": torch.full((Bm, i["slots"]), -1, **n),
+                "tree_k": torch.zeros((Bm, i["rows"], c.n_kv_heads, c.head_dim), **f),
+                "tree_v": torch.zeros((Bm, i["rows"], c.n_kv_heads, c.head_dim), **f)}
+
+    def tree(self, dI: dict, out: dict | None = None, trace: dict | None = None, stream=None):
+        """Enqueue one draft tree; returns the output tensors (device)."""
+        B = int(dI["root_tok"].shape[0])
+        out = self.alloc_outputs(B, dI["root_tok"].device) if out is None else out
+        inp = Inputs(B=B, root_feat=_ptr(dI["root_feat"]), root_tok=_ptr(dI["root_tok"]),
+                     k_cache=_ptr(dI["k_cache"]), v_cache=_ptr(dI["v_cache"]),
+                     cu_seqlens=_ptr(dI["cu_seqlens"]))
+        o = Outputs(**{n: _ptr(out[n]) for n, _ in Outputs._fields_})
+        tr = None if trace is None else C.byref(Trace(**{n: _ptr(trace.get(n)) for n in TRACE_FIELDS}))
+        st = None if stream is None else stream.cuda_stream
+        _check(load().eagle_draft_tree(self.h, C.byref(inp), C.byref(o), tr, st))
+        return out
+
+    def lm_head_topk(self, a, k: int, stream=None):
+        import torch
+        N = int(a.shape[0])
+        ids = torch.empty((N, k), dtype=torch.int32, device=a.device)
+        logp = torch.empty((N, k), dtype=torch.float32, device=a.device)
+        lse = torch.empty((N,), dtype=torch.float32, device=a.device)
+        st = None if stream is None else stream.cuda_stream
+        _check(load().eagle_draft_lm_head_topk(self.h, _ptr(a), N, k, _ptr(ids), _ptr(logp), _ptr(lse), st))
+        return ids, logp, lse
+
+    def check(self) -> int:
+        """Synchronise; raise on a device error word or CUDA error."""
+        w = C.c_uint32(0)
+        st = load().eagle_draft_check(self.h, C.byref(w))
+        if st != EAGLE_OK:
+            raise EagleError(st, load().eagle_draft_last_error().decode())
+        return w.value

@@ -1,0 +1,275 @@
+// Shared device utilities and kernel-argument structs of the draft-tree library.
+// sm_103a only: tcgen05 / TMA / mbarrier through inline PTX.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#define EAGLE_DEV __device__ __forceinline__
+#define EAGLE_MAX_DEPTH_INTERNAL 16
+
+namespace eagle {
+
+// ------------------------------------------------------------------ constants
+constexpr int BM = 128;            // GEMM tile: output features per tile (TMEM lanes)
+constexpr int BK = 64;             // GEMM tile: K per pipeline stage (one 128-byte swizzle row)
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int MAX_ROWS_PER_BLOCK = 128;   // rows of one row block (hi+lo = 256 MMA columns)
+constexpr int KMAX = 16;                  // max children per node
+constexpr int ATT_CHUNK = 64;             // prefix keys per attention split
+constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;   // ~1 s at 2 GHz
+
+constexpr unsigned DEVERR_TIMEOUT = 0x1u;
+constexpr unsigned DEVERR_PREFIX = 0x2u;
+
+// ---------------------------------------------------------- small helpers
+EAGLE_DEV uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+EAGLE_DEV float bf16_to_f32(uint16_t u) { return __uint_as_float(static_cast<uint32_t>(u) << 16); }
+
+// round-to-nearest-even float -> bf16 bits (hardware conversion)
+EAGLE_DEV uint16_t f32_to_bf16(float x) {
+  __nv_bfloat16 b = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): ~16 significant bits in two bf16s
+EAGLE_DEV void split_hilo(float x, uint16_t& hi, uint16_t& lo) {
+  hi = f32_to_bf16(x);
+  lo = f32_to_bf16(x - bf16_to_f32(hi));
+}
+
+EAGLE_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+EAGLE_DEV float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// total order used for every top-k of this library: larger value first, then smaller id
+EAGLE_DEV bool beats(float v, int id, float w, int wid) {
+  return v > w || (v == w && id < wid);
+}
+
+// named barrier among `nthreads` threads (id 1.. ; 0 is __syncthreads)
+EAGLE_DEV void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// programmatic dependent launch
+EAGLE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+EAGLE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------- mbarrier
+EAGLE_DEV void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+EAGLE_DEV void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+EAGLE_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
+}
+EAGLE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete.  Returns false (and
+// sets DEVERR_TIMEOUT in *err and the CTA-wide abort flag) when the limit runs out or
+// another role of the CTA already aborted.
+EAGLE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+        atomicOr(err, DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+EAGLE_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+EAGLE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// --------------------------------------------------------------------- TMA
+EAGLE_DEV uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+EAGLE_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, uint32_t bar,
+                           uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+EAGLE_DEV void tma_prefetch_desc(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+// ----------------------------------------------------------------- tcgen05
+EAGLE_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+EAGLE_DEV void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+EAGLE_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+EAGLE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+EAGLE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, f32 accumulate
+EAGLE_DEV void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on `bar` once every tcgen05 op issued so far by this thread has completed
+EAGLE_DEV void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes
+EAGLE_DEV void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+      " [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+EAGLE_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle layout that
+// TMA's SWIZZLE_128B writes (rows of 128 bytes, 8-row atoms of 1024 bytes).
+EAGLE_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address, 16-byte units
+  d |= static_cast<uint64_t>(1) << 16;                     // leading byte offset (unused for SW128 K-major)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;             // stride byte offset: next 8-row atom
+  d |= static_cast<uint64_t>(1) << 46;                     // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                     // layout: 128-byte swizzle
+  return d;
+}
+// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, f32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled tile
+EAGLE_DEV uint32_t sw128_offset(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------- GEMM argument structs
+// How the GEMM's activation operand (rows x K) is formed from global memory.
+enum BMode : int {
+  B_F32 = 0,      // x[row][k] f32
+  B_NORM = 1,     // RMSNorm: x[row][k] * rstd[row] * gamma[k], rstd from sum-of-squares partials
+  B_FC = 2,       // [feat(row_feat[row]) ; emb(row_tok[row])]: K = 2 * split
+  B_SWIGLU = 3,   // silu(x[row][k]) * x[row][split + k] (gate | up halves)
+  B_BF16 = 4      // x[row][k] bf16
+};
+
+struct BSrc {
+  int mode;
+  const float* x;          // B_F32 / B_NORM / B_SWIGLU / B_FC (feature rows)
+  int ldx;                 // row stride (elements)
+  const uint16_t* xb;      // B_BF16
+  // B_NORM
+  const float* ss;         // [ss_tiles][ss_ld] partial sums of squares
+  int ss_tiles, ss_ld;
+  const float* gamma;
+  float eps;
+  int dnorm;
+  // B_FC / B_SWIGLU
+  int split;               // B_FC: d (feature part width); B_SWIGLU: d_ff
+  const int* row_feat;     // B_FC: feature row of each GEMM row
+  const int* row_tok;      // B_FC: token of each GEMM row
+  const void* emb;         // B_FC: embedding table [vocab][split]
+  int emb_bf16;
+};
+
+enum EpiKind : int { EPI_STORE = 0, EPI_QKV = 1, EPI_LMHEAD = 2 };
+
+struct EpiArgs {
+  int kind;
+  // EPI_STORE: out[row][m] = acc (+ resid[row][m]); ss[tile][row] = sum over the tile of out^2
+  float* out;
+  int ldo;
+  const float* resid;
+  int ldr;
+  float* ss;
+  int ss_ld;
+  // EPI_QKV: rotary embedding, queries to q, keys/values to the tree KV rows
+  float* q;
+  float* tk;
+  float* tv;
+  const int* row_req;      // request of each GEMM row
+  const int* row_slot;     // request-local tree row
+  const int* row_pos;      // position id
+  const float* rope_cos;   // [max_pos][hd/2]
+  const float* rope_sin;
+  int max_pos;
+  int Hq, Hkv, hd, tree_rows;
+  // EPI_LMHEAD: per CTA and row: running max, sum of exp, top-k (value, id) partials
+  float* lm_max;           // [grid][N]
+  float* lm_sum;           // [grid][N]
+  float* lm_val;           // [grid][N][k]
+  int* lm_id;              // [grid][N][k]
+  int topk;
+};
+
+struct GemmArgs {
+  int M, K, N;             // N = rows
+  int MT, KB;              // tiles of M (per weight map), K blocks
+  int m_split;             // rows [0, m_split) from weight map 0, [m_split, M) from map 1
+  int npad;                // padded rows per row block (multiple of 16)
+  int nrb;                 // row blocks
+  int tmem_cols;           // allocated TMEM columns
+  int nbuf;                // accumulator buffers in TMEM (2 = epilogue overlaps next unit)
+  int stages;
+  BSrc b;
+  EpiArgs e;
+  float* part;             // split-K partial scratch [grid][2][nrb*npad][BM]
+  int* counters;           // per tile arrival counters (zero between launches)
+  unsigned* err;
+};
+
+}  // namespace eagle

@@ -1,0 +1,805 @@
+// Skinny-M GEMMs of the draft step: y[row][m] = sum_k W[m][k] * x[row][k].
+//
+// W (the weights, [M][K] row-major) is streamed from HBM once per launch; the rows
+// (frontier nodes, at most a few hundred) are the N side.  Two mainloops share one
+// operand loader and one set of fused epilogues:
+//   * gemm_tc_kernel: bf16 weights.  Persistent CTAs split the (tile, k-block) space
+//     evenly; a TMA warp streams 128x64 weight tiles into a shared-memory ring, loader
+//     warps build the activation tile (gather / RMSNorm / SwiGLU applied on the fly,
+//     fp32 split into bf16 hi + lo rows), one thread issues tcgen05.mma with the
+//     accumulator in TMEM, and four epilogue warps drain TMEM.  Tiles split across CTAs
+//     are finished by the last CTA to arrive (fixed summation order: deterministic).
+//   * gemm_simt_kernel: f32 weights (small shapes), one CTA per 128-feature tile.
+// Epilogues: EPI_STORE (residual add, per-tile sums of squares for the next RMSNorm),
+// EPI_QKV (rotary embedding, queries and tree KV rows), EPI_LMHEAD (online log-sum-exp
+// and per-row top-k over the vocabulary; no logits are written).
+#include "common.cuh"
+#include "internal.h"
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+
+namespace eagle {
+
+// ============================================================== operand loader
+EAGLE_DEV void f4_to(float* v, float4 a, float4 b) {
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+EAGLE_DEV void bf8_to(float* v, uint4 u) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+EAGLE_DEV float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+// Eight consecutive activation values x[row n][k .. k+7] of the GEMM operand.
+EAGLE_DEV void load_b8(const BSrc& b, int n, int k, const float* rstd, float* v) {
+  switch (b.mode) {
+    case B_F32: {
+      const float4* p = reinterpret_cast<const float4*>(b.x + static_cast<size_t>(n) * b.ldx + k);
+      f4_to(v, __ldcg(p), __ldcg(p + 1));
+      break;
+    }
+    case B_NORM: {
+      const float4* p = reinterpret_cast<const float4*>(b.x + static_cast<size_t>(n) * b.ldx + k);
+      const float4* gp = reinterpret_cast<const float4*>(b.gamma + k);
+      float g[8];
+      f4_to(v, __ldcg(p), __ldcg(p + 1));
+      f4_to(g, __ldg(gp), __ldg(gp + 1));
+      const float r = rstd[n];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = v[i] * r * g[i];
+      break;
+    }
+    case B_FC: {
+      if (k < b.split) {
+        const int fr = __ldcg(b.row_feat + n);
+        const float4* p = reinterpret_cast<const float4*>(b.x + static_cast<size_t>(fr) * b.ldx + k);
+        f4_to(v, __ldcg(p), __ldcg(p + 1));
+      } else {
+        const int t = __ldcg(b.row_tok + n);
+        const size_t off = static_cast<size_t>(t) * b.split + (k - b.split);
+        if (b.emb_bf16) {
+          bf8_to(v, __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(b.emb) + off)));
+        } else {
+          const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(b.emb) + off);
+          f4_to(v, __ldg(p), __ldg(p + 1));
+        }
+      }
+      break;
+    }
+    case B_SWIGLU: {
+      const float* row = b.x + static_cast<size_t>(n) * b.ldx;
+      const float4* gp = reinterpret_cast<const float4*>(row + k);
+      const float4* up = reinterpret_cast<const float4*>(row + b.split + k);
+      float gg[8], uu[8];
+      f4_to(gg, __ldcg(gp), __ldcg(gp + 1));
+      f4_to(uu, __ldcg(up), __ldcg(up + 1));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = silu_f(gg[i]) * uu[i];
+      break;
+    }
+    default: {  // B_BF16
+      bf8_to(v, __ldcg(reinterpret_cast<const uint4*>(b.xb + static_cast<size_t>(n) * b.ldx + k)));
+      break;
+    }
+  }
+}
+
+// 1 / sqrt(mean(x^2) + eps) of each row from the producer's per-tile sums of squares
+// (summed in tile order).
+EAGLE_DEV void compute_rstd(const BSrc& b, int N, float* rstd, int tid, int nthreads) {
+  if (b.mode != B_NORM) return;
+  for (int n = tid; n < N; n += nthreads) {
+    float s = 0.f;
+    for (int t = 0; t < b.ss_tiles; ++t) s += __ldcg(b.ss + static_cast<size_t>(t) * b.ss_ld + n);
+    rstd[n] = 1.0f / sqrtf(s / static_cast<float>(b.dnorm) + b.eps);
+  }
+}
+
+// ==================================================================== epilogues
+// Shared-memory scratch of the 128 epilogue threads.
+struct EpiScratch {
+  float xch[16][BM];       // row-major exchange tile (rotary partners, LM-head transpose)
+  float red[4][16];        // per-warp partial sums of squares
+};
+// Views of the epilogue's shared memory (the pointers themselves live in registers).
+struct EpiSmem {
+  EpiScratch* s;
+  float* st_max;           // LM head, per row: running max, running sum of exp, list length
+  float* st_sum;
+  int* st_cnt;
+  float* lv;               // [N][k] running top-k values (sorted)
+  int* li;                 // [N][k] and their token ids
+};
+
+EAGLE_DEV EpiSmem epi_views(void* scratch, void* lm, int N, int topk) {
+  EpiSmem es;
+  es.s = reinterpret_cast<EpiScratch*>(scratch);
+  float* f = reinterpret_cast<float*>(lm);
+  es.st_max = f;
+  es.st_sum = f + N;
+  es.st_cnt = reinterpret_cast<int*>(f + 2 * N);
+  es.lv = f + 3 * N;
+  es.li = reinterpret_cast<int*>(f + 3 * N + N * topk);
+  return es;
+}
+
+// AND of a predicate over the 128 epilogue threads (named barrier 1).
+EAGLE_DEV bool epi_all(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, 1, 128, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"(p ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+// Merge a warp's 128 new (value, id) candidates (4 per lane) into a row's sorted top-k
+// list (length cnt <= k) held in shared memory; k rounds of warp arg-max.
+EAGLE_DEV void warp_topk_merge(float* lv, int* li, int* cnt_p, int k, const float* nv, const int* nid,
+                               int lane) {
+  const int cnt = *cnt_p;
+  float cv[5];
+  int ci[5];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) { cv[j] = nv[j]; ci[j] = nid[j]; }
+  cv[4] = lane < cnt ? lv[lane] : -INFINITY;
+  ci[4] = lane < cnt ? li[lane] : INT_MAX;
+  unsigned taken = 0;
+  float outv = -INFINITY;
+  int outi = INT_MAX;
+  int rounds = 0;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int j = 0; j < 5; ++j)
+      if (!(taken >> j & 1u) && ci[j] != INT_MAX && beats(cv[j], ci[j], bv, bi)) { bv = cv[j]; bi = ci[j]; }
+    float wv = bv;
+    int wi = bi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+      if (beats(ov, oi, wv, wi)) { wv = ov; wi = oi; }
+    }
+    if (wi == INT_MAX) break;
+#pragma unroll
+    for (int j = 0; j < 5; ++j)
+      if (ci[j] == wi) taken |= 1u << j;
+    if (lane == r) { outv = wv; outi = wi; }
+    ++rounds;
+  }
+  __syncwarp();
+  if (lane < rounds) { lv[lane] = outv; li[lane] = outi; }
+  if (lane == 0) *cnt_p = rounds;
+  __syncwarp();
+}
+
+// One 16-row chunk of accumulators: thread tl (0..127) holds feature m0 + tl of rows
+// n0 .. n0+15 in v[].  All 128 epilogue threads call this together.
+EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, const float* v, int tl) {
+  const EpiArgs& e = g.e;
+  const int m = mt * BM + tl;
+  const bool mvalid = m < g.M;
+  const int warp_q = tl >> 5, lane = tl & 31;
+  if (e.kind == EPI_STORE) {
+    float sq[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int n = n0 + i;
+      float val = v[i];
+      sq[i] = 0.f;
+      if (n < g.N && mvalid) {
+        if (e.resid) val += __ldcg(e.resid + static_cast<size_t>(n) * e.ldr + m);
+        e.out[static_cast<size_t>(n) * e.ldo + m] = val;
+        sq[i] = val * val;
+      }
+    }
+    if (e.ss) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float s = warp_sum(sq[i]);
+        if (lane == 0) es.s->red[warp_q][i] = s;
+      }
+      named_bar(1, 128);
+      if (tl < 16 && n0 + tl < g.N)
+        e.ss[static_cast<size_t>(mt) * e.ss_ld + n0 + tl] =
+            es.s->red[0][tl] + es.s->red[1][tl] + es.s->red[2][tl] + es.s->red[3][tl];
+      named_bar(1, 128);
+    }
+  } else if (e.kind == EPI_QKV) {
+    const int hd = e.hd, half = hd >> 1;
+    const int head = m / hd, i = m - head * hd;
+    const bool rotate = head < e.Hq + e.Hkv;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) es.s->xch[r][tl] = v[r];
+    named_bar(1, 128);
+    const int partner = tl + (i < half ? half : -half);
+#pragma unroll 4
+    for (int r = 0; r < 16; ++r) {
+      const int n = n0 + r;
+      if (n >= g.N || !mvalid) continue;
+      float val = v[r];
+      const int pos = __ldcg(e.row_pos + n);
+      if (rotate) {
+        const int j = i < half ? i : i - half;
+        const float c = __ldg(e.rope_cos + static_cast<size_t>(pos) * half + j);
+        const float s = __ldg(e.rope_sin + static_cast<size_t>(pos) * half + j);
+        const float p = es.s->xch[r][partner];
+        val = i < half ? val * c - p * s : val * c + p * s;
+      }
+      if (head < e.Hq) {
+        e.q[static_cast<size_t>(n) * e.Hq * hd + m] = val;
+      } else {
+        const int b = __ldcg(e.row_req + n), slot = __ldcg(e.row_slot + n);
+        const bool isk = head < e.Hq + e.Hkv;
+        const int kvh = isk ? head - e.Hq : head - e.Hq - e.Hkv;
+        float* dst = isk ? e.tk : e.tv;
+        dst[((static_cast<size_t>(b) * e.tree_rows + slot) * e.Hkv + kvh) * hd + i] = val;
+      }
+    }
+    named_bar(1, 128);
+  } else {  // EPI_LMHEAD
+#pragma unroll
+    for (int r = 0; r < 16; ++r) es.s->xch[r][tl] = v[r];
+    named_bar(1, 128);
+    const int k = e.topk;
+    for (int r = warp_q; r < 16; r += 4) {
+      const int n = n0 + r;
+      if (n >= g.N) continue;                       // warp-uniform
+      float val[4];
+      int id[4];
+      float lmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        id[j] = mt * BM + lane + 32 * j;
+        val[j] = id[j] < g.M ? es.s->xch[r][lane + 32 * j] : -INFINITY;
+        if (id[j] >= g.M) id[j] = INT_MAX;
+        lmax = fmaxf(lmax, val[j]);
+      }
+      // online log-sum-exp
+      const float tmax = warp_max(lmax);
+      const float mold = es.st_max[n];
+      const float mnew = fmaxf(mold, tmax);
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s += id[j] != INT_MAX ? expf(val[j] - mnew) : 0.f;
+      s = warp_sum(s);
+      // top-k
+      const int cnt = es.st_cnt[n];
+      float* lv = es.lv + static_cast<size_t>(n) * k;
+      int* li = es.li + static_cast<size_t>(n) * k;
+      const float tv = cnt < k ? -INFINITY : lv[k - 1];
+      const int ti = cnt < k ? INT_MAX : li[k - 1];
+      bool cand = false;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cand |= id[j] != INT_MAX && beats(val[j], id[j], tv, ti);
+      __syncwarp();
+      if (lane == 0) {
+        es.st_sum[n] = es.st_sum[n] * expf(mold - mnew) + s;
+        es.st_max[n] = mnew;
+      }
+      if (__any_sync(0xffffffffu, cand)) warp_topk_merge(lv, li, es.st_cnt + n, k, val, id, lane);
+      __syncwarp();
+    }
+    named_bar(1, 128);
+  }
+}
+
+// Per-CTA LM-head state: reset before the first tile, written out after the last.
+EAGLE_DEV void lmhead_init(const GemmArgs& g, EpiSmem& es, int tl) {
+  for (int n = tl; n < g.N; n += 128) { es.st_max[n] = -INFINITY; es.st_sum[n] = 0.f; es.st_cnt[n] = 0; }
+  named_bar(1, 128);
+}
+EAGLE_DEV void lmhead_flush(const GemmArgs& g, EpiSmem& es, int cta, int tl) {
+  const EpiArgs& e = g.e;
+  const int k = e.topk;
+  named_bar(1, 128);
+  for (int n = tl; n < g.N; n += 128) {
+    const size_t o = static_cast<size_t>(cta) * g.N + n;
+    e.lm_max[o] = es.st_max[n];
+    e.lm_sum[o] = es.st_sum[n];
+    const int cnt = es.st_cnt[n];
+    for (int j = 0; j < k; ++j) {
+      e.lm_val[o * k + j] = j < cnt ? es.lv[static_cast<size_t>(n) * k + j] : -INFINITY;
+      e.lm_id[o * k + j] = j < cnt ? es.li[static_cast<size_t>(n) * k + j] : -1;
+    }
+  }
+}
+
+// ============================================================ work decomposition
+struct Sched {
+  long long total;
+  int grid;
+  EAGLE_DEV long long begin(int c) const { return static_cast<long long>(c) * total / grid; }
+  // CTA whose range holds unit index i
+  EAGLE_DEV int owner(long long i) const {
+    return static_cast<int>(((i + 1) * grid + total - 1) / total - 1);
+  }
+};
+
+// ============================================================ tcgen05 mainloop
+struct TcLayout {
+  uint32_t stage_bytes, b_off;
+  uint32_t bar_off, misc_off, epi_off, rstd_off, lm_off;
+};
+
+__host__ __device__ inline TcLayout tc_layout(int npad, int stages, int N, int topk) {
+  TcLayout L;
+  L.b_off = A_STAGE_BYTES;
+  L.stage_bytes = A_STAGE_BYTES + npad * 2 * 128;
+  L.bar_off = L.stage_bytes * stages;
+  L.misc_off = L.bar_off + (2 * stages + 4) * 8;
+  L.epi_off = (L.misc_off + 64 + 127) & ~127u;
+  L.rstd_off = L.epi_off + static_cast<uint32_t>((sizeof(EpiScratch) + 127) & ~size_t(127));
+  L.lm_off = L.rstd_off + sizeof(float) * 256;
+  (void)N;
+  (void)topk;
+  return L;
+}
+__host__ __device__ inline uint32_t tc_smem_bytes(int npad, int stages, int N, int topk) {
+  TcLayout L = tc_layout(npad, stages, N, topk);
+  return L.lm_off + static_cast<uint32_t>(N) * (3 + 2 * topk) * 4 + 1024;  // +1024: base alignment
+}
+
+template <int NLW>
+__global__ void __launch_bounds__((6 + NLW) * 32, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+               const GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const TcLayout L = tc_layout(g.npad, g.stages, g.N, g.e.topk);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + L.bar_off;
+  const uint32_t bar_empty = bar_full + 8 * g.stages;
+  const uint32_t bar_accf = bar_empty + 8 * g.stages;
+  const uint32_t bar_acce = bar_accf + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
+  int* last_flag = reinterpret_cast<int*>(smem + L.misc_off + 8);
+  float* rstd = reinterpret_cast<float*>(smem + L.rstd_off);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KB = g.KB;
+  const int npad = g.npad, nrb = g.nrb, np2 = 2 * npad;
+  const Sched sc{static_cast<long long>(g.MT) * KB, static_cast<int>(gridDim.x)};
+  const long long u0 = sc.begin(blockIdx.x), u1 = sc.begin(blockIdx.x + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < g.stages; ++s) {
+      mbar_init(bar_full + 8 * s, 2);        // TMA bytes + one loader warp
+      mbar_init(bar_empty + 8 * s, 1);       // tcgen05.commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_accf + 8 * b, 1);
+      mbar_init(bar_acce + 8 * b, 4);        // one arrive per epilogue warp
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), g.tmem_cols);
+    tmem_relinquish();
+  }
+  if (warp == 1 && lane == 0) {
+    tma_prefetch_desc(&tm0);
+    tma_prefetch_desc(&tm1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+
+  if (warp == 0) {
+    // ---------------------------------------------------- TMA producer (weights)
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (long long i = u0; i < u1 && ok;) {
+        const int mt = static_cast<int>(i / KB), kb0 = static_cast<int>(i % KB);
+        const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
+        const bool second = mt * BM >= g.m_split;
+        const CUtensorMap* tm = second ? &tm1 : &tm0;
+        const int mrow = second ? mt * BM - g.m_split : mt * BM;
+        for (int kb = kb0; kb < kb1 && ok; ++kb) {
+          for (int rb = 0; rb < nrb && ok; ++rb) {
+            if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar_full + 8 * stage, A_STAGE_BYTES);
+            tma_load_2d(sbase + stage * L.stage_bytes, tm, kb * BK, mrow, bar_full + 8 * stage, pol);
+            if (++stage == g.stages) { stage = 0; phase ^= 1; }
+          }
+        }
+        i += kb1 - kb0;
+      }
+      if (!ok) {
+        // let copies already issued land before the CTA releases its shared memory
+        const long long t0 = clock64();
+        while (clock64() - t0 < 4000000) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, np2);
+      int stage = 0;
+      uint32_t phase = 0;
+      long long uc = 0;
+      bool ok = true;
+      for (long long i = u0; i < u1 && ok; ++uc) {
+        const int kb0 = static_cast<int>(i % KB);
+        const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
+        const int ab = static_cast<int>(uc % g.nbuf);
+        const uint32_t ap = static_cast<uint32_t>((uc / g.nbuf) & 1);
+        if (!mbar_wait(bar_acce + 8 * ab, ap ^ 1, g.err, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        for (int kb = kb0; kb < kb1 && ok; ++kb) {
+          for (int rb = 0; rb < nrb; ++rb) {
+            if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a_addr = sbase + stage * L.stage_bytes;
+            const uint32_t b_addr = a_addr + L.b_off;
+            const uint32_t d = tmem + static_cast<uint32_t>((ab * nrb + rb) * np2);
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j)
+              tc_mma_bf16(d, smem_desc_sw128(a_addr + 32 * j), smem_desc_sw128(b_addr + 32 * j), idesc,
+                          (kb > kb0 || j > 0) ? 1u : 0u);
+            tc_commit(bar_empty + 8 * stage);
+            if (++stage == g.stages) { stage = 0; phase ^= 1; }
+          }
+        }
+        if (ok) tc_commit(bar_accf + 8 * ab);
+        i += kb1 - kb0;
+      }
+      if (!ok) {
+        // let MMAs already issued finish before TMEM is released
+        const long long t0 = clock64();
+        while (clock64() - t0 < 4000000) {
+        }
+      }
+    }
+  } else if (warp >= 6) {
+    // --------------------------------------------- activation operand loaders
+    const int lw = warp - 6;
+    pdl_wait();
+    compute_rstd(g.b, g.N, rstd, (warp - 6) * 32 + lane, NLW * 32);
+    named_bar(2, NLW * 32);
+    int stage = 0;
+    uint32_t phase = 0;
+    long long it = 0;
+    bool ok = true;
+    for (long long i = u0; i < u1 && ok;) {
+      const int kb0 = static_cast<int>(i % KB);
+      const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
+      for (int kb = kb0; kb < kb1 && ok; ++kb) {
+        for (int rb = 0; rb < nrb; ++rb, ++it) {
+          if (it % NLW == lw) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag));
+            if (!ok) break;
+            uint8_t* bs = smem + stage * L.stage_bytes + L.b_off;
+            const int items = npad * 8;
+            for (int base = 0; base < items; base += 32 * 4) {
+              float vals[4][8];
+              int rr[4], cc[4];
+              bool valid[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int item = base + u * 32 + lane;
+                rr[u] = item >> 3;
+                cc[u] = item & 7;
+                const int n = rb * npad + rr[u];
+                valid[u] = item < items && n < g.N;
+                if (valid[u]) load_b8(g.b, n, kb * BK + cc[u] * 8, rstd, vals[u]);
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                if (base + u * 32 + lane >= items) continue;
+                uint32_t hw[4] = {0, 0, 0, 0}, lw4[4] = {0, 0, 0, 0};
+                if (valid[u]) {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    uint16_t h0, l0, h1, l1;
+                    split_hilo(vals[u][2 * e], h0, l0);
+                    split_hilo(vals[u][2 * e + 1], h1, l1);
+                    hw[e] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+                    lw4[e] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+                  }
+                }
+                *reinterpret_cast<uint4*>(bs + sw128_offset(rr[u], cc[u])) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(bs + sw128_offset(npad + rr[u], cc[u])) =
+                    make_uint4(lw4[0], lw4[1], lw4[2], lw4[3]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_full + 8 * stage);
+          }
+          if (++stage == g.stages) { stage = 0; phase ^= 1; }
+        }
+      }
+      i += kb1 - kb0;
+    }
+  } else {
+    // ------------------------------------------------------ epilogue (warps 2-5)
+    const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    const int tl = q * 32 + lane;           // feature row of the tile = TMEM lane
+    EpiSmem es = epi_views(smem + L.epi_off, smem + L.lm_off, g.N, g.e.topk);
+    pdl_wait();
+    if (g.e.kind == EPI_LMHEAD) lmhead_init(g, es, tl);
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int rows_total = nrb * npad;
+    long long uc = 0;
+    bool ok = true;
+    for (long long i = u0; i < u1 && ok; ++uc) {
+      const int mt = static_cast<int>(i / KB), kb0 = static_cast<int>(i % KB);
+      const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
+      const int ab = static_cast<int>(uc % g.nbuf);
+      const uint32_t ap = static_cast<uint32_t>((uc / g.nbuf) & 1);
+      ok = epi_all(mbar_wait(bar_accf + 8 * ab, ap, g.err, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const bool complete = kb0 == 0 && kb1 == KB;
+      const int slot = (i == u0) ? 0 : 1;   // the CTA's first unit or its last
+      float* mypart = g.part + (static_cast<size_t>(blockIdx.x) * 2 + slot) * rows_total * BM;
+      for (int rb = 0; rb < nrb; ++rb) {
+        for (int c0 = 0; c0 < npad; c0 += 16) {
+          const int n0 = rb * npad + c0;
+          if (n0 >= g.N) break;
+          const uint32_t col = static_cast<uint32_t>((ab * nrb + rb) * np2 + c0);
+          float hi[16], lo[16], v[16];
+          __syncwarp();
+          tmem_ld16(tmem + lane_base + col, hi);
+          tmem_ld16(tmem + lane_base + col + npad, lo);
+          tmem_wait_ld();
+#pragma unroll
+          for (int r = 0; r < 16; ++r) v[r] = hi[r] + lo[r];
+          if (complete) {
+            epilogue_chunk(g, es, mt, n0, v, tl);
+          } else {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) mypart[static_cast<size_t>(n0 + r) * BM + tl] = v[r];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
+      if (!complete) {
+        __threadfence();
+        named_bar(1, 128);
+        const int cf = sc.owner(static_cast<long long>(mt) * KB);
+        const int cl = sc.owner(static_cast<long long>(mt + 1) * KB - 1);
+        if (tl == 0) {
+          const int old = atomicAdd(g.counters + mt, 1);
+          *last_flag = (old == cl - cf);
+        }
+        named_bar(1, 128);
+        if (*last_flag) {
+          __threadfence();
+          if (tl == 0) g.counters[mt] = 0;
+          for (int rb = 0; rb < nrb; ++rb) {
+            for (int c0 = 0; c0 < npad; c0 += 16) {
+              const int n0 = rb * npad + c0;
+              if (n0 >= g.N) break;
+              float v[16];
+#pragma unroll
+              for (int r = 0; r < 16; ++r) v[r] = 0.f;
+              for (int c = cf; c <= cl; ++c) {
+                const int s = (sc.begin(c) / KB == mt) ? 0 : 1;
+                const float* p = g.part + (static_cast<size_t>(c) * 2 + s) * rows_total * BM;
+#pragma unroll
+                for (int r = 0; r < 16; ++r) v[r] += __ldcg(p + static_cast<size_t>(n0 + r) * BM + tl);
+              }
+              epilogue_chunk(g, es, mt, n0, v, tl);
+            }
+          }
+        }
+        named_bar(1, 128);
+      }
+      i += kb1 - kb0;
+    }
+    if (g.e.kind == EPI_LMHEAD) lmhead_flush(g, es, blockIdx.x, tl);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, g.tmem_cols);
+  }
+}
+
+// ============================================================ SIMT mainloop (f32)
+// One CTA (256 threads) per (128-feature tile, 16-row block); full K per CTA.
+constexpr int SIMT_ROWS = 16;
+
+__global__ void __launch_bounds__(256)
+gemm_simt_kernel(const float* __restrict__ W0, const float* __restrict__ W1, const GemmArgs g) {
+  extern __shared__ float sm[];
+  float* xs = sm;                                   // [16][K] activation rows
+  float* acc = xs + SIMT_ROWS * g.K;                // [16][128]
+  float* rstd = acc + SIMT_ROWS * BM;               // [N]
+  EpiScratch* scr = reinterpret_cast<EpiScratch*>(rstd + ((g.N + 31) & ~31));
+  float* lm = reinterpret_cast<float*>(scr + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = blockIdx.x, n0 = blockIdx.y * SIMT_ROWS;
+  pdl_wait();
+  pdl_trigger();
+  compute_rstd(g.b, g.N, rstd, tid, 256);
+  __syncthreads();
+  for (int idx = tid; idx < SIMT_ROWS * (g.K / 8); idx += 256) {
+    const int r = idx / (g.K / 8), k = (idx % (g.K / 8)) * 8;
+    float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (n0 + r < g.N) load_b8(g.b, n0 + r, k, rstd, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xs[r * g.K + k + i] = v[i];
+  }
+  __syncthreads();
+  for (int f = warp; f < BM; f += 8) {
+    const int m = mt * BM + f;
+    float a[SIMT_ROWS];
+#pragma unroll
+    for (int r = 0; r < SIMT_ROWS; ++r) a[r] = 0.f;
+    if (m < g.M) {
+      const float* w = (m < g.m_split) ? W0 + static_cast<size_t>(m) * g.K
+                                       : W1 + static_cast<size_t>(m - g.m_split) * g.K;
+      for (int k = lane; k < g.K; k += 32) {
+        const float wk = __ldg(w + k);
+#pragma unroll
+        for (int r = 0; r < SIMT_ROWS; ++r) a[r] += wk * xs[r * g.K + k];
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < SIMT_ROWS; ++r) {
+      const float s = warp_sum(a[r]);
+      if (lane == 0) acc[r * BM + f] = s;
+    }
+  }
+  __syncthreads();
+  if (tid < 128) {
+    EpiSmem es = epi_views(scr, lm, g.N, g.e.topk);
+    if (g.e.kind == EPI_LMHEAD) lmhead_init(g, es, tid);
+    float v[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) v[r] = acc[r * BM + tid];
+    epilogue_chunk(g, es, mt, n0, v, tid);
+    if (g.e.kind == EPI_LMHEAD) {
+      // this CTA owns rows [n0, n0+16) of tile mt: partial slot = tile
+      named_bar(1, 128);
+      const int k = g.e.topk;
+      for (int r = tid; r < SIMT_ROWS; r += 128) {
+        const int n = n0 + r;
+        if (n >= g.N) continue;
+        const size_t o = static_cast<size_t>(mt) * g.N + n;
+        g.e.lm_max[o] = es.st_max[n];
+        g.e.lm_sum[o] = es.st_sum[n];
+        const int cnt = es.st_cnt[n];
+        for (int j = 0; j < k; ++j) {
+          g.e.lm_val[o * k + j] = j < cnt ? es.lv[static_cast<size_t>(n) * k + j] : -INFINITY;
+          g.e.lm_id[o * k + j] = j < cnt ? es.li[static_cast<size_t>(n) * k + j] : -1;
+        }
+      }
+    }
+  }
+}
+
+// ================================================================== host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int g_num_sms = 0;
+int num_sms() {
+  if (!g_num_sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  return g_num_sms;
+}
+
+constexpr int TC_NLW = 4;
+constexpr int TC_MAX_SMEM = 232448;
+
+// Fill the launch geometry of a GEMM over N rows.
+bool plan_gemm(GemmPlan& p, int N) {
+  GemmArgs& g = p.args;
+  g.N = N;
+  g.KB = (g.K + BK - 1) / BK;
+  g.MT = (g.M + BM - 1) / BM;
+  if (!p.tc) {
+    p.grid = g.MT;
+    p.grid_y = (N + SIMT_ROWS - 1) / SIMT_ROWS;
+    p.smem = sizeof(float) * (SIMT_ROWS * g.K + SIMT_ROWS * BM + ((N + 31) & ~31)) + sizeof(EpiScratch) +
+             static_cast<size_t>(N) * (3 + 2 * std::max(1, g.e.topk)) * 4 + 64;
+    return p.smem <= static_cast<size_t>(TC_MAX_SMEM);
+  }
+  g.nrb = (N + MAX_ROWS_PER_BLOCK - 1) / MAX_ROWS_PER_BLOCK;
+  const int per = (N + g.nrb - 1) / g.nrb;
+  g.npad = std::max(16, (per + 15) / 16 * 16);
+  const int accum_cols = g.nrb * 2 * g.npad;
+  g.nbuf = (2 * accum_cols <= 512) ? 2 : 1;
+  int cols = 32;
+  while (cols < g.nbuf * accum_cols) cols <<= 1;
+  g.tmem_cols = cols;
+  const long long total = static_cast<long long>(g.MT) * g.KB;
+  p.grid = static_cast<int>(std::min<long long>(num_sms(), total));
+  p.grid_y = 1;
+  const int topk = std::max(1, g.e.topk);
+  const uint32_t fixed = tc_smem_bytes(g.npad, 0, g.e.kind == EPI_LMHEAD ? N : 0, topk);
+  const uint32_t stage = A_STAGE_BYTES + g.npad * 256;
+  int stages = static_cast<int>((TC_MAX_SMEM - fixed) / stage);
+  stages = std::min(stages, 12);
+  if (stages < 2) return false;
+  g.stages = stages;
+  p.smem = tc_smem_bytes(g.npad, stages, g.e.kind == EPI_LMHEAD ? N : 0, topk);
+  return true;
+}
+
+cudaError_t gemm_setup_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<TC_NLW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TC_MAX_SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_MAX_SMEM);
+}
+
+cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.stream = st;
+  cfg.dynamicSmemBytes = p.smem;
+  if (p.tc) {
+    cfg.gridDim = dim3(p.grid, 1, 1);
+    cfg.blockDim = dim3((6 + TC_NLW) * 32, 1, 1);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_NLW>, p.tm0, p.tm1, p.args);
+  }
+  cfg.gridDim = dim3(p.grid, p.grid_y, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  return cudaLaunchKernelEx(&cfg, gemm_simt_kernel, p.w0f, p.w1f, p.args);
+}
+
+}  // namespace eagle

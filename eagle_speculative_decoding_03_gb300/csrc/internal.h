@@ -1,0 +1,120 @@
+// Host-side declarations shared by the translation units of the library.
+#pragma once
+
+#include "common.cuh"
+
+namespace eagle {
+
+// ----------------------------------------------------------------- GEMM
+struct GemmPlan {
+  bool tc = false;               // tcgen05 mainloop (bf16 weights) or SIMT (f32 weights)
+  CUtensorMap tm0, tm1;          // weight maps (tc): rows [0, m_split) and [m_split, M)
+  const float* w0f = nullptr;    // f32 weights (simt)
+  const float* w1f = nullptr;
+  GemmArgs args{};
+  int grid = 0, grid_y = 1;
+  size_t smem = 0;
+};
+
+bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K);
+int num_sms();
+bool plan_gemm(GemmPlan& p, int N);
+cudaError_t gemm_setup_attributes();
+cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t st, bool pdl);
+
+// ------------------------------------------------------------ attention
+struct AttnArgs {
+  const float* q;           // [N][Hq*hd] rotated queries of this depth's rows
+  const void* k_cache;      // [sum n][Hkv][hd] prefix keys (post-RoPE), bf16 or f32
+  const void* v_cache;
+  int cache_bf16;
+  const int* cu_seqlens;    // [B+1]
+  const int* n_eff;         // [B] validated prefix lengths
+  const float* tk;          // [B][tree_rows][Hkv][hd] rotated keys of tree rows
+  const float* tv;
+  const unsigned long long* row_mask;  // [N] ancestor-or-self bits over request-local rows
+  int rows_per_req;         // rows of this depth per request
+  int tree_rows;            // request-local row capacity
+  int tree_upto;            // rows that exist so far (through this depth)
+  int B, Hq, Hkv, hd;
+  int max_splits;           // prefix splits + 1 (tree split)
+  float* part;              // [B][Hkv][max_splits][qv][hd + 2]
+  int* counters;            // [B][Hkv]
+  float* out;               // [N][Hq*hd]
+};
+size_t attn_smem_bytes(int qv, int hd);
+cudaError_t attn_setup_attributes();
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl);
+
+// --------------------------------------------------------- tree kernels
+struct TreeArgs {
+  int B, depth, tree_kind, k, m, slots;
+  int kids[EAGLE_MAX_DEPTH_INTERNAL];       // children per row at each depth
+  int rows[EAGLE_MAX_DEPTH_INTERNAL];       // rows per request at each depth
+  int row_base[EAGLE_MAX_DEPTH_INTERNAL + 1];
+  int node_base[EAGLE_MAX_DEPTH_INTERNAL + 1];
+  int tree_rows;            // R: rows per request over all depths
+  int max_nodes;            // generated + 1 (root)
+  int max_prefix;
+  // inputs
+  const int* root_tok;
+  const int* cu_seqlens;
+  // node table [B][max_nodes]
+  int* node_tok;
+  int* node_parent;
+  int* node_depth;
+  int* node_row;            // request-local row that generated the node
+  float* node_logv;
+  // per-request state
+  int* n_eff;               // [B]
+  int* frontier;            // [B][64] node ids of the current frontier
+  unsigned long long* slot_mask;  // [B][tree_rows] ancestor-or-self bits of every row
+  unsigned* err;
+};
+
+// Row metadata of one depth (N = B * rows rows).
+struct RowMeta {
+  int* req;                 // request
+  int* slot;                // request-local row id
+  int* pos;                 // position id n_b + depth
+  int* tok;                 // input token
+  int* feat;                // feature row (index into the previous feature buffer)
+  int* node;                // tree node the row expands
+  unsigned long long* mask; // ancestor-or-self bits
+};
+
+struct LmPartials {
+  float* max;               // [G][N]
+  float* sum;               // [G][N]
+  float* val;               // [G][N][k]
+  int* id;                  // [G][N][k]
+  int G;
+};
+
+struct OutArgs {
+  int* tokens;
+  int* parents;
+  int* positions;
+  float* logv;
+  unsigned char* mask;
+  int* final_nodes;         // trace (nullable)
+};
+
+struct ExpandTrace {
+  int* children;            // [N][k_max] (nullable)
+  float* child_logp;
+  float* lse;               // [N]
+  int* frontier;            // [B][f_max]
+  int k_max;
+  int f_max;
+};
+
+cudaError_t tree_setup_attributes();
+cudaError_t launch_tree_init(const TreeArgs& t, const RowMeta& rows0, cudaStream_t st, bool pdl);
+cudaError_t launch_expand(const TreeArgs& t, int s, const LmPartials& lm, const RowMeta& cur,
+                          const RowMeta& next, const ExpandTrace& tr, cudaStream_t st, bool pdl);
+cudaError_t launch_rerank(const TreeArgs& t, const OutArgs& o, cudaStream_t st, bool pdl);
+cudaError_t launch_lm_merge(const LmPartials& lm, int N, int k, int* ids, float* logp, float* lse,
+                            cudaStream_t st, bool pdl);
+
+}  // namespace eagle

@@ -1,0 +1,214 @@
+/*
+ * eagle_draft.h - C ABI of the GB300 draft-tree expansion step for EAGLE-style
+ * speculative decoding (EAGLE-1 static tree, EAGLE-2 expand-and-rerank dynamic
+ * tree, EAGLE-3 fused-feature input).
+ *
+ * What one call computes (sources: four pages on EAGLE):
+ *   - the draft recurrence x = [feat ; emb(tok)] -> fc (2d -> d) -> one decoder
+ *     layer over the verified-prefix KV cache -> frozen LM head
+ *     ("The recurrence, written out", aicassindra.com tm_eagle_deep; "The Mechanism",
+ *     stable-lab "EAGLE: Drafting in Feature Space");
+ *   - at each of `depth` sequential steps every frontier node gets its top-k children
+ *     by draft probability; path value V = sum of log confidences along the path
+ *     ("EAGLE-2 - context-aware dynamic tree", zackli.ai "Speculative Decoding Deep
+ *     Dive III"; "EAGLE-2: expand and rerank", aicassindra.com);
+ *   - static trees (EAGLE-1) expand every node with a fixed per-depth branching
+ *     ("Drafting a Tree, Not a Chain", stable-lab); dynamic trees keep the top-k nodes
+ *     of each depth as the next frontier and, after the last depth, the top-m of all
+ *     generated nodes;
+ *   - EAGLE-3: the root feature is g = FC([l; m; h]) (3d -> d); later steps feed back the
+ *     draft's own output a ("EAGLE-3 - free representation + training-time test +
+ *     feature fusion", zackli.ai; "Multi-layer feature fusion", aicassindra.com);
+ *   - the emitted tree: token ids, parent slots, position ids and the ancestor-only
+ *     attention mask ("Tree attention in one verification pass", aicassindra.com).
+ *
+ * Names follow the pages' notation: B requests, n verified prefix length, depth =
+ * gamma, k branching, m kept nodes, d hidden size, vocab = |V|.
+ *
+ * Memory: every pointer below is a DEVICE pointer unless marked host.  Weights are
+ * borrowed for the lifetime of the handle; inputs, outputs and trace buffers for the
+ * duration of the call (the call is stream-ordered: they must stay valid until the
+ * stream reaches the end of the call).  The handle owns its device workspace.
+ * Errors: functions return eagle_status_t; eagle_draft_last_error() gives a
+ * thread-local message.  Kernel-side problems (a prefix longer than max_prefix, a
+ * wait that ran out) are recorded in a device error word that eagle_draft_check()
+ * reads after synchronising.  Calls on one handle must not overlap on the GPU.
+ */
+#ifndef EAGLE_DRAFT_H
+#define EAGLE_DRAFT_H
+
+#include <stdint.h>
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define EAGLE_API __attribute__((visibility("default")))
+#else
+#define EAGLE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EAGLE_OK = 0,
+  EAGLE_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, B > max_batch, ... */
+  EAGLE_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels implement */
+  EAGLE_ERR_OOM = 3,           /* workspace allocation failed */
+  EAGLE_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
+  EAGLE_ERR_DEVICE = 5         /* the device error word is set (see eagle_draft_check) */
+} eagle_status_t;
+
+typedef enum { EAGLE_DTYPE_F32 = 0, EAGLE_DTYPE_BF16 = 1 } eagle_dtype_t;
+typedef enum { EAGLE_TREE_STATIC = 1, EAGLE_TREE_DYNAMIC = 2 } eagle_tree_kind_t;
+typedef enum { EAGLE_FEAT_F = 1, EAGLE_FEAT_FUSED = 3 } eagle_feat_kind_t;
+
+#define EAGLE_MAX_DEPTH 16
+
+/* Device error word bits (eagle_draft_check). */
+#define EAGLE_DEVERR_TIMEOUT     0x1u   /* a bounded wait inside a kernel ran out */
+#define EAGLE_DEVERR_PREFIX      0x2u   /* a request's prefix length was < 0 or > max_prefix */
+
+typedef struct {
+  int32_t d;            /* hidden size; d % 128 == 0 for bf16 weights */
+  int32_t n_heads;      /* query heads Hq */
+  int32_t n_kv_heads;   /* key/value heads Hkv; Hq % Hkv == 0 (grouped-query attention) */
+  int32_t head_dim;     /* hd: 128 for bf16 weights, 64 or 128 for f32 */
+  int32_t d_ff;         /* SwiGLU hidden size */
+  int32_t vocab;        /* |V| */
+  float   rms_eps;      /* RMSNorm epsilon */
+  float   rope_theta;   /* rotary base: inv_freq_i = theta^(-2i/hd), rotate-half pairs (i, i+hd/2) */
+  int32_t dtype;        /* eagle_dtype_t of the weights, embedding table and KV cache */
+  int32_t tree_kind;    /* eagle_tree_kind_t */
+  int32_t feat_kind;    /* eagle_feat_kind_t */
+  int32_t depth;        /* gamma: sequential draft steps, 1..EAGLE_MAX_DEPTH */
+  int32_t k;            /* dynamic: children per expanded node and frontier width, 1..16 */
+  int32_t m;            /* dynamic: nodes kept by the rerank (static trees keep all) */
+  int32_t branching[EAGLE_MAX_DEPTH]; /* static: children per node at depth 1..depth, 1..16 */
+  int32_t max_batch;    /* workspace sizing: largest B a call may pass */
+  int32_t max_prefix;   /* workspace sizing: largest prefix length n_b a call may pass */
+  int32_t flags;        /* EAGLE_FLAG_*; 0 = CUDA-graph replay and programmatic dependent launch */
+} eagle_draft_config_t;
+
+#define EAGLE_FLAG_NO_GRAPH 0x1   /* enqueue the kernels directly on every call */
+#define EAGLE_FLAG_NO_PDL   0x2   /* plain stream order between kernels */
+
+/* Weights, stored [out, in] row-major in `dtype` (the norm gains are always f32).
+ * w_qkv stacks the query rows, then the key rows, then the value rows.
+ * w_fc multiplies [feat ; emb(tok)] (the feature first).  w_fc3 (EAGLE-3 only) multiplies
+ * [l ; m ; h].  w_lm is the frozen LM head [vocab, d]; embed the frozen table [vocab, d]. */
+typedef struct {
+  const void*  embed;      /* [vocab, d] */
+  const void*  w_fc;       /* [d, 2d] */
+  const void*  w_fc3;      /* [d, 3d] or NULL unless feat_kind == EAGLE_FEAT_FUSED */
+  const float* attn_norm;  /* [d] */
+  const void*  w_qkv;      /* [(Hq + 2 Hkv) hd, d] */
+  const void*  w_o;        /* [d, Hq hd] */
+  const float* mlp_norm;   /* [d] */
+  const void*  w_gate;     /* [d_ff, d] */
+  const void*  w_up;       /* [d_ff, d] */
+  const void*  w_down;     /* [d, d_ff] */
+  const void*  w_lm;       /* [vocab, d] */
+} eagle_draft_weights_t;
+
+/* One call's inputs (device).  The prefix KV cache is the draft layer's own cache of
+ * the verified positions, packed over requests and already rotated (post-RoPE). */
+typedef struct {
+  int32_t        B;          /* requests, 1..max_batch */
+  const void*    root_feat;  /* EAGLE-1/2: f32 [B, d] target feature f; EAGLE-3: `dtype` [B, 3d] = [l;m;h] */
+  const int32_t* root_tok;   /* [B] the token sampled from f (the tree root) */
+  const void*    k_cache;    /* `dtype` [sum n_b, Hkv, hd] */
+  const void*    v_cache;    /* `dtype` [sum n_b, Hkv, hd] */
+  const int32_t* cu_seqlens; /* [B + 1], cu_seqlens[0] = 0, n_b = cu_seqlens[b+1] - cu_seqlens[b] */
+} eagle_draft_inputs_t;
+
+/* Outputs (device).  S = kept + 1 slots per request (eagle_draft_info_t.slots):
+ * slot 0 is the root (token root_tok, parent -1, position n_b, logv 0); slots 1.. are the
+ * kept nodes in generation order (depth, then the parent's frontier slot, then token id),
+ * so a parent always precedes its children. */
+typedef struct {
+  int32_t* tokens;     /* [B, S] */
+  int32_t* parents;    /* [B, S] parent slot, -1 for the root */
+  int32_t* positions;  /* [B, S] n_b + depth */
+  float*   logv;       /* [B, S] path value V = sum of log draft probabilities */
+  uint8_t* mask;       /* [B, S, S] mask[b][i][j] = 1 iff slot j is an ancestor of slot i or i itself */
+} eagle_draft_outputs_t;
+
+/* Optional per-depth intermediates for parity testing (any member may be NULL).
+ * N_max = max_batch * max rows per depth; rows of depth s (0-based) sit at
+ * [s][b * rows_s + i]; dimensions per row as named. */
+typedef struct {
+  float*   h;           /* [depth][N_max][d]       fc output */
+  float*   q;           /* [depth][N_max][Hq*hd]   queries after rotation */
+  float*   attn;        /* [depth][N_max][Hq*hd]   attention output */
+  float*   y;           /* [depth][N_max][d]       after O-proj + residual */
+  float*   a;           /* [depth][N_max][d]       layer output (next feature f' / latent a) */
+  float*   lse;         /* [depth][N_max]          log-sum-exp of the row's logits */
+  int32_t* children;    /* [depth][N_max][k_max]   children token ids (ascending) */
+  float*   child_logp;  /* [depth][N_max][k_max]   their log-probabilities */
+  int32_t* frontier;    /* [depth][max_batch][f_max] node ids expanded at the next depth */
+  int32_t* final_nodes; /* [max_batch][S]          node id of every emitted slot */
+  float*   tree_k;      /* [max_batch][R][Hkv][hd] rotated keys of every row (R rows per request) */
+  float*   tree_v;      /* [max_batch][R][Hkv][hd] */
+} eagle_draft_trace_t;
+
+typedef struct {
+  int32_t slots;            /* S = kept + 1 */
+  int32_t generated;        /* nodes generated per request */
+  int32_t rows;             /* R: draft-layer rows per request over all depths */
+  int32_t n_max;            /* max_batch * max rows per depth */
+  int32_t k_max;            /* max children per row over depths */
+  int32_t f_max;            /* max rows per request at one depth */
+  int32_t launches_per_tree;/* kernels one eagle_draft_tree launches */
+  int32_t tensor_core_gemm; /* 1 when the GEMMs run on tcgen05 (bf16 weights) */
+  int64_t workspace_bytes;
+} eagle_draft_info_t;
+
+typedef struct eagle_draft eagle_draft_t;
+
+/* Validates the config, allocates the workspace, builds the TMA descriptors of the
+ * weights and the rotary tables.  The current CUDA device must be the one holding the
+ * weights.  Returns EAGLE_ERR_UNSUPPORTED for shapes the kernels do not implement:
+ * bf16 needs d, d_ff, vocab, (Hq+2Hkv)hd multiples of 128 and hd == 128; every config
+ * needs at most 64 rows per request, at most 63 kept nodes, k and branching <= 16. */
+EAGLE_API eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg,
+                                  const eagle_draft_weights_t* weights,
+                                  eagle_draft_t** out_handle);
+
+/* Enqueues one draft-tree expansion on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and returns.  Without a trace the launches are replayed from a CUDA graph
+ * captured on the first call with the same B and pointers.  `trace` may be NULL. */
+EAGLE_API eagle_status_t eagle_draft_tree(eagle_draft_t* handle,
+                                const eagle_draft_inputs_t* inputs,
+                                const eagle_draft_outputs_t* outputs,
+                                const eagle_draft_trace_t* trace,
+                                void* stream);
+
+/* One launch of the fused LM-head kernel (frozen LM head + online log-softmax + per-row
+ * top-k, ties to the lower token id; no [rows x |V|] logits are written) followed by the
+ * cross-CTA merge, on the handle's weights and workspace.
+ * a: f32 [N, d] device; N <= n_max; k <= 16.
+ * Outputs (device): ids int32 [N, k] sorted by descending logit, logp f32 [N, k],
+ * lse f32 [N].  This is the same kernel the tree step launches at every depth. */
+EAGLE_API eagle_status_t eagle_draft_lm_head_topk(eagle_draft_t* handle, const float* a, int32_t N,
+                                        int32_t k, int32_t* ids, float* logp, float* lse,
+                                        void* stream);
+
+/* Sizes of the handle's buffers (host struct). */
+EAGLE_API eagle_status_t eagle_draft_query(const eagle_draft_t* handle, eagle_draft_info_t* info);
+
+/* Synchronises the device and returns EAGLE_ERR_DEVICE if the device error word is set
+ * (its bits in *word if word != NULL, host), EAGLE_ERR_CUDA on a sticky CUDA error, and
+ * EAGLE_OK otherwise.  Clears the word. */
+EAGLE_API eagle_status_t eagle_draft_check(eagle_draft_t* handle, uint32_t* word);
+
+/* Frees the workspace and the handle.  NULL is accepted. */
+EAGLE_API void eagle_draft_destroy(eagle_draft_t* handle);
+
+/* Thread-local description of the last error (never NULL). */
+EAGLE_API const char* eagle_draft_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE_DRAFT_H */

@@ -1,0 +1,88 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every function that
+include/eagle_draft.h declares, and rejects invalid arguments before any GPU work."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from eagle_speculative_decoding_03_gb300 import binding as eb, configs
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "eagle_draft.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from eagle_speculative_decoding_03_gb300 import build
+    build.build()
+    return eb.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"EAGLE_API\s+[\w\s\*]*?\b(eagle_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    fns = declared_functions()
+    for f in ("eagle_draft_create", "eagle_draft_tree", "eagle_draft_destroy", "eagle_draft_last_error"):
+        assert f in fns
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for f in declared_functions():
+        assert hasattr(lib, f), f
+
+
+def _weights_dummy():
+    w = eb.Weights()
+    for n, _ in eb.Weights._fields_:
+        setattr(w, n, 256)   # never dereferenced: validation fails first
+    return w
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (dict(d=0), eb.EAGLE_ERR_INVALID_ARG),
+    (dict(n_heads=3, n_kv_heads=2), eb.EAGLE_ERR_INVALID_ARG),
+    (dict(depth=0), eb.EAGLE_ERR_INVALID_ARG),
+    (dict(depth=17), eb.EAGLE_ERR_INVALID_ARG),
+    (dict(k=17), eb.EAGLE_ERR_INVALID_ARG),
+    (dict(head_dim=96), eb.EAGLE_ERR_UNSUPPORTED),
+    (dict(d=4000), eb.EAGLE_ERR_UNSUPPORTED),
+    (dict(vocab=1000), eb.EAGLE_ERR_UNSUPPORTED),
+    (dict(max_batch=0), eb.EAGLE_ERR_INVALID_ARG),
+])
+def test_create_rejects_invalid_config(lib, mutate, status):
+    c = eb.make_config(configs.get("eagle2_b1"))
+    for k, v in mutate.items():
+        setattr(c, k, v)
+    h = C.c_void_p()
+    st = lib.eagle_draft_create(C.byref(c), C.byref(_weights_dummy()), C.byref(h))
+    assert st == status, lib.eagle_draft_last_error()
+    assert not h.value
+    assert lib.eagle_draft_last_error()
+
+
+def test_create_rejects_null_weights(lib):
+    c = eb.make_config(configs.get("eagle2_b1"))
+    w = _weights_dummy()
+    w.w_lm = None
+    h = C.c_void_p()
+    assert lib.eagle_draft_create(C.byref(c), C.byref(w), C.byref(h)) == eb.EAGLE_ERR_INVALID_ARG
+    assert b"null weight" in lib.eagle_draft_last_error()
+
+
+def test_null_handles(lib):
+    assert lib.eagle_draft_tree(None, None, None, None, None) == eb.EAGLE_ERR_INVALID_ARG
+    assert lib.eagle_draft_lm_head_topk(None, None, 1, 1, None, None, None, None) == eb.EAGLE_ERR_INVALID_ARG
+    assert lib.eagle_draft_query(None, None) == eb.EAGLE_ERR_INVALID_ARG
+    assert lib.eagle_draft_check(None, None) == eb.EAGLE_ERR_INVALID_ARG
+    lib.eagle_draft_destroy(None)
+
+
+def test_struct_layout_matches_header():
+    # the config struct: 14 int/float fields + 16 branching + 3 = 33 four-byte fields
+    assert C.sizeof(eb.Config) == 33 * 4
+    assert C.sizeof(eb.Weights) == 11 * 8
+    assert C.sizeof(eb.Inputs) == 6 * 8
+    assert C.sizeof(eb.Info) == 8 * 4 + 8

@@ -1,0 +1,91 @@
+"""End-to-end GPU parity of the draft-tree step through the C ABI against the float64
+oracle: tree structure bit-exact (near-ties within 1e-3 reported), features within 2e-2
+relative, path values within 1e-2."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from eagle_speculative_decoding_03_gb300 import binding as eb, configs, synth
+from oracle import parity
+from tests.gpu_util import run_tree
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from eagle_speculative_decoding_03_gb300 import build
+    build.build()
+    return eb.load()
+
+
+SMALL = ["tiny_chain", "small_f32", "small_dyn", "small_static", "small_fused"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_tree_parity_small(lib, name):
+    cfg = configs.get(name)
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    d, out, tr = run_tree(cfg, W, I)
+    rep = parity.compare(synth.oracle_cfg(cfg), W, I, out, tr, d.info["slots"])
+    print(name, {k: f"{v:.2e}" for k, v in rep["stats"].items()}, "forced:", rep["forced"])
+    assert rep["ok"], rep["errors"]
+
+
+@pytest.mark.parametrize("name", ["small_dyn", "small_static", "small_fused"])
+def test_graph_replay_matches_direct_launch(lib, name):
+    cfg = configs.get(name)
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    d, out_trace, _ = run_tree(cfg, W, I, trace=True)
+    _, out_graph, _ = run_tree(cfg, W, I, trace=False, handle=d)
+    _, out_graph2, _ = run_tree(cfg, W, I, trace=False, handle=d)
+    _, out_plain, _ = run_tree(cfg, W, I, trace=False, flags=eb.FLAG_NO_GRAPH | eb.FLAG_NO_PDL)
+    for k in out_trace:
+        assert np.array_equal(out_trace[k], out_graph[k]), k
+        assert np.array_equal(out_graph[k], out_graph2[k]), k
+        assert np.array_equal(out_graph[k], out_plain[k]), k
+
+
+def test_partial_batch_and_empty_prefix(lib):
+    cfg = configs.get("small_dyn")
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg, B=2, seed_offset=5)
+    # request 0 has no verified prefix at all: it attends to its tree rows only
+    n1 = int(I["cu_seqlens"][2] - I["cu_seqlens"][1])
+    I["k_cache"], I["v_cache"] = I["k_cache"][-n1:], I["v_cache"][-n1:]
+    I["cu_seqlens"] = np.array([0, 0, n1], np.int32)
+    d, out, tr = run_tree(cfg, W, I, max_batch=3)
+    rep = parity.compare(synth.oracle_cfg(cfg), W, I, out, tr, d.info["slots"])
+    assert rep["ok"], rep["errors"]
+    assert out["positions"][0][0] == 0
+
+
+def test_zero_lm_head_ties(lib):
+    cfg = configs.get("small_dyn")
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    W["w_lm"] = np.zeros_like(W["w_lm"])
+    d, out, tr = run_tree(cfg, W, I)
+    rep = parity.compare(synth.oracle_cfg(cfg), W, I, out, tr, d.info["slots"])
+    assert rep["ok"], rep["errors"]
+    assert rep["forced"] == []
+    # all children are tokens 0..k-1; the frontier and the rerank keep the lowest node ids
+    assert out["tokens"][0][1:cfg.k + 1].tolist() == list(range(cfg.k))
+
+
+def test_prefix_longer_than_max_prefix_is_reported(lib):
+    cfg = configs.get("small_dyn")
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    d = eb.EagleDraft(cfg, eb.device_weights(W), max_prefix=16)
+    d.tree(eb.device_inputs(I))
+    with pytest.raises(eb.EagleError) as ei:
+        d.check()
+    assert ei.value.status == eb.EAGLE_ERR_DEVICE
+    d.check()   # the word was cleared
+
+
+def test_invalid_batch_rejected(lib):
+    cfg = configs.get("small_dyn")
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    d = eb.EagleDraft(cfg, eb.device_weights(W), max_batch=2)
+    with pytest.raises(eb.EagleError) as ei:
+        d.tree(eb.device_inputs(I))
+    assert ei.value.status == eb.EAGLE_ERR_INVALID_ARG
