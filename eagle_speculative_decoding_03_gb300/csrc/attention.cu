@@ -203,7 +203,7 @@ tree_attention_kernel(const AttnArgs a) {
 }
 
 cudaError_t attn_setup_attributes() {
-  return cudaFuncSetAttribute(tree_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  return allow_max_smem(reinterpret_cast<const void*>(tree_attention_kernel));
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {

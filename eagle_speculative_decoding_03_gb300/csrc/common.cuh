@@ -248,9 +248,9 @@ struct EpiArgs {
   const float* rope_sin;
   int max_pos;
   int Hq, Hkv, hd, tree_rows;
-  // EPI_LMHEAD: per CTA and row: running max, sum of exp, top-k (value, id) partials
-  float* lm_max;           // [grid][N]
-  float* lm_sum;           // [grid][N]
+  // EPI_LMHEAD: per vocabulary tile and row: max and sum of exp; per CTA and row: top-k
+  float* lm_max;           // [tiles][N]
+  float* lm_sum;           // [tiles][N]
   float* lm_val;           // [grid][N][k]
   int* lm_id;              // [grid][N][k]
   int topk;

@@ -146,8 +146,9 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   h->part = cv.take<float>(static_cast<size_t>(num_sms()) * 2 * 256 * BM);
   h->att_part = cv.take<float>(static_cast<size_t>(B) * c.n_kv_heads * h->max_splits * h->qv_max * (c.head_dim + 2));
   const size_t lmn = static_cast<size_t>(h->lm_G) * n;
-  h->lm_max = cv.take<float>(lmn);
-  h->lm_sum = cv.take<float>(lmn);
+  const size_t lmt = static_cast<size_t>(ceil_div(c.vocab, BM)) * n;
+  h->lm_max = cv.take<float>(lmt);
+  h->lm_sum = cv.take<float>(lmt);
   h->lm_val = cv.take<float>(lmn * KMAX);
   h->lm_id = cv.take<int>(lmn * KMAX);
   h->counters = cv.take<int>(16384);
@@ -228,7 +229,7 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
   h->max_pos = c.max_prefix + c.depth + 1;
   h->max_splits = ceil_div(c.max_prefix, ATT_CHUNK) + 1;
   h->qv_max = nmax_rows * (c.n_heads / c.n_kv_heads);
-  if (attn_smem_bytes(h->qv_max, c.head_dim) > 232448) {
+  if (attn_smem_bytes(h->qv_max, c.head_dim) > 227 * 1024 - 64) {
     delete h;
     return fail(EAGLE_ERR_UNSUPPORTED, "too many query vectors per KV group (%d)", h->qv_max);
   }
@@ -393,6 +394,7 @@ static LmPartials lm_partials(eagle_draft* h, int N) {
   lm.sum = h->lm_sum;
   lm.val = h->lm_val;
   lm.id = h->lm_id;
+  lm.T = ceil_div(h->cfg.vocab, BM);
   lm.G = h->tc ? std::min<long long>(num_sms(), static_cast<long long>(ceil_div(h->cfg.vocab, BM)) * ceil_div(h->cfg.d, BK))
                : ceil_div(h->cfg.vocab, BM);
   (void)N;

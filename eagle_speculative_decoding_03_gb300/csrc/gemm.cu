@@ -268,14 +268,16 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
         if (id[j] >= g.M) id[j] = INT_MAX;
         lmax = fmaxf(lmax, val[j]);
       }
-      // online log-sum-exp
+      // this tile's log-sum-exp state (max, sum of exp) of the row, merged later in tile order
       const float tmax = warp_max(lmax);
-      const float mold = es.st_max[n];
-      const float mnew = fmaxf(mold, tmax);
       float s = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) s += id[j] != INT_MAX ? expf(val[j] - mnew) : 0.f;
+      for (int j = 0; j < 4; ++j) s += id[j] != INT_MAX ? expf(val[j] - tmax) : 0.f;
       s = warp_sum(s);
+      if (lane == 0) {
+        e.lm_max[static_cast<size_t>(mt) * g.N + n] = tmax;
+        e.lm_sum[static_cast<size_t>(mt) * g.N + n] = s;
+      }
       // top-k
       const int cnt = es.st_cnt[n];
       float* lv = es.lv + static_cast<size_t>(n) * k;
@@ -286,10 +288,6 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
 #pragma unroll
       for (int j = 0; j < 4; ++j) cand |= id[j] != INT_MAX && beats(val[j], id[j], tv, ti);
       __syncwarp();
-      if (lane == 0) {
-        es.st_sum[n] = es.st_sum[n] * expf(mold - mnew) + s;
-        es.st_max[n] = mnew;
-      }
       if (__any_sync(0xffffffffu, cand)) warp_topk_merge(lv, li, es.st_cnt + n, k, val, id, lane);
       __syncwarp();
     }
@@ -299,7 +297,7 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
 
 // Per-CTA LM-head state: reset before the first tile, written out after the last.
 EAGLE_DEV void lmhead_init(const GemmArgs& g, EpiSmem& es, int tl) {
-  for (int n = tl; n < g.N; n += 128) { es.st_max[n] = -INFINITY; es.st_sum[n] = 0.f; es.st_cnt[n] = 0; }
+  for (int n = tl; n < g.N; n += 128) es.st_cnt[n] = 0;
   named_bar(1, 128);
 }
 EAGLE_DEV void lmhead_flush(const GemmArgs& g, EpiSmem& es, int cta, int tl) {
@@ -308,8 +306,6 @@ EAGLE_DEV void lmhead_flush(const GemmArgs& g, EpiSmem& es, int cta, int tl) {
   named_bar(1, 128);
   for (int n = tl; n < g.N; n += 128) {
     const size_t o = static_cast<size_t>(cta) * g.N + n;
-    e.lm_max[o] = es.st_max[n];
-    e.lm_sum[o] = es.st_sum[n];
     const int cnt = es.st_cnt[n];
     for (int j = 0; j < k; ++j) {
       e.lm_val[o * k + j] = j < cnt ? es.lv[static_cast<size_t>(n) * k + j] : -INFINITY;
@@ -686,8 +682,6 @@ gemm_simt_kernel(const float* __restrict__ W0, const float* __restrict__ W1, con
         const int n = n0 + r;
         if (n >= g.N) continue;
         const size_t o = static_cast<size_t>(mt) * g.N + n;
-        g.e.lm_max[o] = es.st_max[n];
-        g.e.lm_sum[o] = es.st_sum[n];
         const int cnt = es.st_cnt[n];
         for (int j = 0; j < k; ++j) {
           g.e.lm_val[o * k + j] = j < cnt ? es.lv[static_cast<size_t>(n) * k + j] : -INFINITY;
@@ -740,6 +734,23 @@ int num_sms() {
 
 constexpr int TC_NLW = 4;
 constexpr int TC_MAX_SMEM = 232448;
+static size_t g_tc_smem_cap = 0, g_simt_smem_cap = 0;
+
+size_t max_dyn_smem(const void* func) {
+  int dev = 0, optin = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) return 0;
+  return optin > static_cast<int>(fa.sharedSizeBytes) ? optin - fa.sharedSizeBytes : 0;
+}
+
+cudaError_t allow_max_smem(const void* func, size_t* granted) {
+  const size_t m = max_dyn_smem(func);
+  if (granted) *granted = m;
+  if (m == 0) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(m));
+}
 
 // Fill the launch geometry of a GEMM over N rows.
 bool plan_gemm(GemmPlan& p, int N) {
@@ -752,7 +763,7 @@ bool plan_gemm(GemmPlan& p, int N) {
     p.grid_y = (N + SIMT_ROWS - 1) / SIMT_ROWS;
     p.smem = sizeof(float) * (SIMT_ROWS * g.K + SIMT_ROWS * BM + ((N + 31) & ~31)) + sizeof(EpiScratch) +
              static_cast<size_t>(N) * (3 + 2 * std::max(1, g.e.topk)) * 4 + 64;
-    return p.smem <= static_cast<size_t>(TC_MAX_SMEM);
+    return p.smem <= (g_simt_smem_cap ? g_simt_smem_cap : static_cast<size_t>(TC_MAX_SMEM));
   }
   g.nrb = (N + MAX_ROWS_PER_BLOCK - 1) / MAX_ROWS_PER_BLOCK;
   const int per = (N + g.nrb - 1) / g.nrb;
@@ -768,7 +779,9 @@ bool plan_gemm(GemmPlan& p, int N) {
   const int topk = std::max(1, g.e.topk);
   const uint32_t fixed = tc_smem_bytes(g.npad, 0, g.e.kind == EPI_LMHEAD ? N : 0, topk);
   const uint32_t stage = A_STAGE_BYTES + g.npad * 256;
-  int stages = static_cast<int>((TC_MAX_SMEM - fixed) / stage);
+  const uint32_t cap = static_cast<uint32_t>(g_tc_smem_cap ? g_tc_smem_cap : TC_MAX_SMEM);
+  if (fixed + 2 * stage > cap) return false;
+  int stages = static_cast<int>((cap - fixed) / stage);
   stages = std::min(stages, 12);
   if (stages < 2) return false;
   g.stages = stages;
@@ -777,10 +790,9 @@ bool plan_gemm(GemmPlan& p, int N) {
 }
 
 cudaError_t gemm_setup_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<TC_NLW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       TC_MAX_SMEM);
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_NLW>), &g_tc_smem_cap);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemm_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_MAX_SMEM);
+  return allow_max_smem(reinterpret_cast<const void*>(gemm_simt_kernel), &g_simt_smem_cap);
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t st, bool pdl) {

@@ -16,6 +16,10 @@ struct GemmPlan {
   size_t smem = 0;
 };
 
+// Allow `func` the device's opt-in maximum of dynamic shared memory (minus its static use).
+cudaError_t allow_max_smem(const void* func, size_t* granted = nullptr);
+size_t max_dyn_smem(const void* func);
+
 bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K);
 int num_sms();
 bool plan_gemm(GemmPlan& p, int N);
@@ -84,11 +88,12 @@ struct RowMeta {
 };
 
 struct LmPartials {
-  float* max;               // [G][N]
-  float* sum;               // [G][N]
-  float* val;               // [G][N][k]
+  float* max;               // [T][N] per vocabulary tile
+  float* sum;               // [T][N]
+  float* val;               // [G][N][k] per CTA
   int* id;                  // [G][N][k]
-  int G;
+  int G;                    // CTAs that wrote top-k partials
+  int T;                    // vocabulary tiles
 };
 
 struct OutArgs {

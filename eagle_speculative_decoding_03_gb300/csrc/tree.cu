@@ -49,14 +49,14 @@ __global__ void tree_init_kernel(const TreeArgs t, const RowMeta r0) {
 // `cand` is the warp's shared-memory staging area (G * kp entries).
 EAGLE_DEV void merge_lm_row(const LmPartials& lm, int N, int kp, int n, int kout, float2* cand,
                             float& lse, float& my_val, int& my_id, int lane) {
-  const int G = lm.G;
+  const int G = lm.G, T = lm.T;
   float M = -INFINITY;
-  for (int g = lane; g < G; g += 32) M = fmaxf(M, __ldcg(lm.max + static_cast<size_t>(g) * N + n));
+  for (int t = lane; t < T; t += 32) M = fmaxf(M, __ldcg(lm.max + static_cast<size_t>(t) * N + n));
   M = warp_max(M);
   float s = 0.f;
-  for (int g = lane; g < G; g += 32) {
-    const float mg = __ldcg(lm.max + static_cast<size_t>(g) * N + n);
-    if (mg != -INFINITY) s += __ldcg(lm.sum + static_cast<size_t>(g) * N + n) * expf(mg - M);
+  for (int t = lane; t < T; t += 32) {
+    const float mt = __ldcg(lm.max + static_cast<size_t>(t) * N + n);
+    if (mt != -INFINITY) s += __ldcg(lm.sum + static_cast<size_t>(t) * N + n) * expf(mt - M);
   }
   s = warp_sum(s);
   lse = M + logf(s);
@@ -298,9 +298,9 @@ static cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStrea
 }
 
 cudaError_t tree_setup_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(expand_kernel));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(lm_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  return allow_max_smem(reinterpret_cast<const void*>(lm_merge_kernel));
 }
 
 cudaError_t launch_tree_init(const TreeArgs& t, const RowMeta& rows0, cudaStream_t st, bool pdl) {

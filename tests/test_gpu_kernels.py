@@ -38,7 +38,8 @@ def test_lm_head_topk_small(lib, name, N, k):
     W = synth.make_weights(cfg)
     rng = np.random.default_rng(N * 100 + k)
     a = (rng.standard_normal((N, cfg.d)) * 1.17).astype(np.float32)
-    d = eb.EagleDraft(cfg, eb.device_weights(W), max_batch=4 if N < 40 else 8)
+    rows = max(cfg.rows_at(s) for s in range(1, cfg.depth + 1))
+    d = eb.EagleDraft(cfg, eb.device_weights(W), max_batch=-(-N // rows))
     ids, logp, lse = d.lm_head_topk(torch.from_numpy(a).cuda(), k)
     d.check()
     _check_topk(a, W["w_lm"], ids.cpu().numpy(), logp.cpu().numpy(), lse.cpu().numpy(), k)
