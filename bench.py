@@ -1,0 +1,363 @@
+#!/usr/bin/env python3
+"""Benchmark of the EAGLE draft-tree expansion step on GB300; prints one JSON line.
+
+A step is one whole draft tree (every depth: fc, decoder layer, LM head + top-k, tree
+expansion; then the rerank) over one batch of synthetic requests.  The headline
+workload is the EAGLE-2 dynamic tree (k=10, depth 6, m=60) on a Llama-3-8B-shaped head
+(d=4096, 32 query / 8 KV heads of 128, SwiGLU 14336, |V|=128256) at B=1 with a verified
+prefix of 2048 tokens; the same head at B=32 (k=8, m=48, prefixes U[256,4096]) is
+reported alongside.  Weights, prefix KV and features are seeded synthetic data.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica on its own GPU (requests are
+independent: no collective on the data path); the timed region is bracketed by a
+barrier and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from eagle_speculative_decoding_03_gb300 import configs, synth  # noqa: E402
+
+METRIC = "draft-tree nodes/sec + µs/step, Llama-3-8B head, B=1/32; % HBM roofline"
+UNIT = "nodes/s"
+
+
+# ------------------------------------------------------------------ helpers
+def algorithmic_bytes(cfg, n_prefix_total: int, N_rows_per_depth):
+    """Bytes one tree must move: every weight once per depth, the prefix KV once per depth,
+    the embedding rows of the rows; plus the EAGLE-3 fuse weights once."""
+    d, ff, V, hq = cfg.d, cfg.d_ff, cfg.vocab, cfg.n_heads * cfg.head_dim
+    w = 2 if cfg.dtype == "bf16" else 4
+    weights = w * (2 * d * d + cfg.qkv_dim * d + d * hq + 3 * d * ff + V * d)
+    kv = n_prefix_total * cfg.n_kv_heads * cfg.head_dim * 2 * w
+    emb = sum(N_rows_per_depth) * d * w
+    fc3 = w * 3 * d * d if cfg.feat == "fused" else 0
+    return weights * cfg.depth + kv * cfg.depth + emb + fc3, weights, kv
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"samples": 0}
+        time.sleep(0.06)
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_uuid(dev) -> str:
+    import torch
+    u = str(torch.cuda.get_device_properties(dev).uuid)
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_step_sample(cfg, W, I):
+    """One draft step of the oracle at full width (the rows of depth 2 of every request:
+    fc, decoder layer over the prefix + own KV, LM head, log-softmax, top-k).  Returns
+    seconds."""
+    from oracle import eagle_oracle as O
+    ocfg = synth.oracle_cfg(cfg)
+    R = cfg.rows_at(2) if cfg.depth > 1 else 1
+    N = cfg.B * R
+    rng = np.random.default_rng(0)
+    cu = np.asarray(I["cu_seqlens"], np.int64)
+    feats = rng.standard_normal((N, cfg.d)) * synth.FEATURE_RMS
+    toks = rng.integers(0, cfg.vocab, N)
+    pos = np.array([cu[i // R + 1] - cu[i // R] + 1 for i in range(N)])
+    Kc, Vc = O.as_f64(I["k_cache"]), O.as_f64(I["v_cache"])
+
+    def attend(i, k_i, v_i):
+        b = i // R
+        return (np.concatenate([Kc[cu[b]:cu[b + 1]], k_i[None]]),
+                np.concatenate([Vc[cu[b]:cu[b + 1]], v_i[None]]))
+
+    t0 = time.perf_counter()
+    x_in = np.concatenate([feats, O.as_f64(W["embed"][toks])], axis=1)
+    out = O.decoder_rows(ocfg, W, x_in, pos, attend)
+    for i in range(N):
+        O.top_k(out["logp"][i], cfg.children_at(2))
+    return time.perf_counter() - t0
+
+
+# ------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cfg = configs.get(args.workload)
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    for _ in range(args.warmup):
+        oracle_step_sample(cfg, W, I)
+    ts = [oracle_step_sample(cfg, W, I) for _ in range(args.steps)]
+    t = float(np.mean(ts))
+    nodes_per_step = cfg.B * cfg.kept_per_request() / cfg.depth
+    value = nodes_per_step / t
+    sample = (f"one draft step of the float64 oracle at full width ({cfg.B * cfg.rows_at(2)} rows: fc, decoder "
+              f"layer, LM head, top-k); nodes/s = (B*m/depth) / step time")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 * cfg.depth,
+            "us_per_draft_step": t * 1e6, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "global_batch": cfg.B, "seq_len": cfg.prefix[1]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- our arm
+def time_trees(d, dI, out, stream, steps, warmup, dist, clock_id=None):
+    import torch
+    for _ in range(warmup):
+        d.tree(dI, out=out, stream=stream)
+    d.check()
+    sampler = ClockSampler(clock_id) if clock_id else None
+    if dist:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        d.tree(dI, out=out, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = e0.elapsed_time(e1) / steps
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    d.check()
+    return ms, clocks
+
+
+def run_ours(args):
+    import torch
+    from eagle_speculative_decoding_03_gb300 import binding as eb
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = world > 1
+    torch.cuda.set_device(local)
+    if dist:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    eb.load()
+    cfg = configs.get(args.workload)
+    W = synth.make_weights(cfg)
+    I = synth.make_inputs(cfg, seed_offset=rank)
+    dW = eb.device_weights(W)
+    dI = eb.device_inputs(I)
+    d = eb.EagleDraft(cfg, dW)
+    stream = torch.cuda.current_stream()
+    B = cfg.B
+    out = d.alloc_outputs(B)
+    nodes_per_tree = B * cfg.kept_per_request()
+
+    # ---- device-timed tree (graph replay, inputs resident in HBM)
+    ms, clocks = time_trees(d, dI, out, stream, args.steps, args.warmup, dist, gpu_uuid(local))
+    value = world * nodes_per_tree / (ms * 1e-3)
+    n_prefix = int(I["cu_seqlens"][-1])
+    rows = [B * cfg.rows_at(s) for s in range(1, cfg.depth + 1)]
+    algo, wbytes, kvbytes = algorithmic_bytes(cfg, n_prefix, rows)
+    peak, peak_kind = peaks()
+    step_gbs = algo / (ms * 1e-3) / 1e9
+
+    # ---- per-kernel times (profiling mode: direct launches with events per kernel)
+    d.profile(True)
+    prof_trees = max(3, min(20, args.steps))
+    for _ in range(prof_trees):
+        d.tree(dI, out=out, stream=stream)
+    prof = d.profile_read()
+    d.profile(False)
+    lm_ms, lm_n = prof.get("lm_head", (0.0, 1))
+    lm_avg_ms = lm_ms / max(lm_n, 1)
+    lm_bytes = (2 if cfg.dtype == "bf16" else 4) * cfg.vocab * cfg.d
+    lm_gbs = lm_bytes / (lm_avg_ms * 1e-3) / 1e9
+    prof_total = sum(v[0] for v in prof.values())
+    kernels = {k: {"ms_per_tree": v[0] / prof_trees, "share": v[0] / prof_total} for k, v in prof.items()}
+
+    # ---- end to end through the public API: pinned host inputs in, results out
+    pin = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v)).pin_memory()
+           for k, v in I.items()}
+    hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        for k, t in pin.items():
+            dI[k].copy_(t, non_blocking=True)
+        d.tree(dI, out=out, stream=stream)
+        for k, t in hout.items():
+            t.copy_(out[k], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * nodes_per_tree / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    # ---- the same head at B=32 (batched serving), sharing the weights
+    b32 = None
+    if args.workload == "eagle2_b1" and not args.no_b32:
+        c4 = configs.get("eagle2_b32")
+        I4 = synth.make_inputs(c4, seed_offset=rank)
+        dI4 = eb.device_inputs(I4)
+        d4 = eb.EagleDraft(c4, dW)
+        out4 = d4.alloc_outputs(c4.B)
+        steps4 = max(3, args.steps // 4)
+        ms4, _ = time_trees(d4, dI4, out4, stream, steps4, args.warmup, dist)
+        rows4 = [c4.B * c4.rows_at(s) for s in range(1, c4.depth + 1)]
+        algo4, _, _ = algorithmic_bytes(c4, int(I4["cu_seqlens"][-1]), rows4)
+        d4.profile(True)
+        for _ in range(3):
+            d4.tree(dI4, out=out4, stream=stream)
+        p4 = d4.profile_read()
+        d4.profile(False)
+        b32 = {"workload": "eagle2_b32", "value": world * c4.B * c4.kept_per_request() / (ms4 * 1e-3),
+               "unit": UNIT, "ms_per_step": ms4, "us_per_draft_step": ms4 * 1e3 / c4.depth,
+               "hbm_frac_step": algo4 / (ms4 * 1e-3) / 1e9 / peak,
+               "kernels_ms_per_tree": {k: v[0] / 3 for k, v in p4.items()}}
+        d4.close()
+
+    # ---- CPU baseline: the float64 oracle on host cores (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t = oracle_step_sample(cfg, W, I)
+        v = (B * cfg.kept_per_request() / cfg.depth) / t
+        cpu = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"one draft step of the float64 oracle at full width ({B * cfg.rows_at(2)} rows), "
+                         f"{t:.1f} s; nodes/s = (B*m/depth) / step time"}
+
+    launches = d.info["launches_per_tree"] * args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "us_per_draft_step": ms * 1e3 / cfg.depth,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: EAGLE-2 dynamic tree k={cfg.k} depth={cfg.depth} m={cfg.m}, "
+                               f"Llama-3-8B-shaped head (d={cfg.d}, {cfg.n_heads}q/{cfg.n_kv_heads}kv x "
+                               f"{cfg.head_dim}, ff={cfg.d_ff}, |V|={cfg.vocab}), prefix n={cfg.prefix[1]}, "
+                               f"B={B} per GPU",
+                   "global_batch": B * world, "seq_len": cfg.prefix[1], "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: every tree streams the 1.55 GB of head weights from HBM",
+                   "nodes_per_tree": nodes_per_tree, "timing": "graph replay, CUDA events on the stream"},
+        "hbm_frac_step": step_gbs / peak,
+        "step_algorithmic_bytes": algo,
+        "roofline": {"bound": "hbm", "kernel": "lm_head (gemm_tc_kernel, LM-head epilogue)",
+                     "achieved": lm_gbs, "peak": peak, "unit": "GB/s", "frac": lm_gbs / peak,
+                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": lm_bytes,
+                     "avg_launch_ms": lm_avg_ms, "traffic": None},
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    if b32:
+        line["b32"] = b32
+    if cpu:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    d.close()
+    if dist:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="eagle2_b1", choices=sorted(configs.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-b32", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

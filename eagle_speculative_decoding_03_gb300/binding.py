@@ -22,6 +22,7 @@ TREE_STATIC, TREE_DYNAMIC = 1, 2
 FEAT_F, FEAT_FUSED = 1, 3
 FLAG_NO_GRAPH, FLAG_NO_PDL = 1, 2
 MAX_DEPTH = 16
+KERNEL_KINDS = 12
 DEVERR_TIMEOUT, DEVERR_PREFIX = 1, 2
 
 
@@ -88,6 +89,12 @@ def load(path: str = LIB_PATH):
     lib.eagle_draft_check.restype = C.c_int
     lib.eagle_draft_destroy.argtypes = [P]
     lib.eagle_draft_destroy.restype = None
+    lib.eagle_draft_profile.argtypes = [P, C.c_int32]
+    lib.eagle_draft_profile.restype = C.c_int
+    lib.eagle_draft_profile_read.argtypes = [P, C.POINTER(C.c_float), C.POINTER(C.c_int32)]
+    lib.eagle_draft_profile_read.restype = C.c_int
+    lib.eagle_draft_kernel_name.argtypes = [C.c_int32]
+    lib.eagle_draft_kernel_name.restype = C.c_char_p
     lib.eagle_draft_last_error.argtypes = []
     lib.eagle_draft_last_error.restype = C.c_char_p
     _lib = lib
@@ -215,6 +222,17 @@ class EagleDraft:
         st = None if stream is None else stream.cuda_stream
         _check(load().eagle_draft_lm_head_topk(self.h, _ptr(a), N, k, _ptr(ids), _ptr(logp), _ptr(lse), st))
         return ids, logp, lse
+
+    def profile(self, enable: bool):
+        _check(load().eagle_draft_profile(self.h, 1 if enable else 0))
+
+    def profile_read(self) -> dict:
+        """{kernel name: (total ms, launches)} since the last read (synchronises)."""
+        ms = (C.c_float * KERNEL_KINDS)()
+        n = (C.c_int32 * KERNEL_KINDS)()
+        _check(load().eagle_draft_profile_read(self.h, ms, n))
+        lib = load()
+        return {lib.eagle_draft_kernel_name(i).decode(): (ms[i], n[i]) for i in range(KERNEL_KINDS) if n[i]}
 
     def check(self) -> int:
         """Synchronise; raise on a device error word or CUDA error."""

@@ -74,6 +74,37 @@ struct eagle_draft {
   cudaGraphExec_t graph = nullptr;
   std::vector<const void*> graph_key;
   int launches = 0;
+  // profiling: (kind, start, stop) per launch
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  std::vector<int> ev_kind;
+};
+
+static const char* kKernelNames[EAGLE_K_COUNT] = {"init", "fc3", "fc", "qkv_rope", "attention", "o_proj",
+                                                  "gate_up", "down", "lm_head", "expand", "rerank", "lm_merge"};
+
+// Event pair around one launch (profiling mode only).
+struct ProfScope {
+  eagle_draft* h;
+  cudaStream_t st;
+  int kind;
+  cudaEvent_t stop = nullptr;
+  ProfScope(eagle_draft* h_, int kind_, cudaStream_t st_) : h(h_), st(st_), kind(kind_) {
+    if (!h->profiling) return;
+    while (h->ev_pool.size() < h->ev_used + 2) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return;
+      h->ev_pool.push_back(e);
+    }
+    cudaEventRecord(h->ev_pool[h->ev_used], st);
+    stop = h->ev_pool[h->ev_used + 1];
+    h->ev_used += 2;
+    h->ev_kind.push_back(kind);
+  }
+  ~ProfScope() {
+    if (stop) cudaEventRecord(stop, st);
+  }
 };
 
 static int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -296,6 +327,7 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
 extern "C" void eagle_draft_destroy(eagle_draft_t* h) {
   if (!h) return;
   if (h->graph) cudaGraphExecDestroy(h->graph);
+  for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   if (h->ws) cudaFree(h->ws);
   delete h;
@@ -366,9 +398,10 @@ static EpiArgs epi_store(float* out, int ldo, const float* resid, int ldr, float
   return e;
 }
 
-static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t st) {
+static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t st, int kind) {
   if (!plan_gemm(p, N)) return fail(EAGLE_ERR_UNSUPPORTED, "GEMM M=%d K=%d N=%d does not fit", p.args.M, p.args.K, N);
-  CU(launch_gemm(p, st, h->use_pdl));
+  ProfScope ps(h, kind, st);
+  CU(launch_gemm(p, st, h->use_pdl && !h->profiling));
   return EAGLE_OK;
 }
 
@@ -385,7 +418,7 @@ static eagle_status_t lm_head(eagle_draft* h, const float* a, int N, int topk, c
   e.lm_val = h->lm_val;
   e.lm_id = h->lm_id;
   e.topk = topk;
-  return run_gemm(h, p, N, st);
+  return run_gemm(h, p, N, st, EAGLE_K_LMHEAD);
 }
 
 static LmPartials lm_partials(eagle_draft* h, int N) {
@@ -406,7 +439,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
                                    const eagle_draft_trace_t* trc, cudaStream_t st) {
   const eagle_draft_config_t& c = h->cfg;
   const int B = in->B, d = c.d, hq = c.n_heads * c.head_dim, ff = c.d_ff;
-  const bool pdl = h->use_pdl;
+  const bool pdl = h->use_pdl && !h->profiling;
   TreeArgs t;
   memset(&t, 0, sizeof(t));
   t.B = B;
@@ -437,7 +470,10 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
   t.frontier = h->frontier;
   t.slot_mask = h->slot_mask;
   t.err = h->err;
-  CU(launch_tree_init(t, h->meta[0], st, pdl));
+  {
+    ProfScope ps(h, EAGLE_K_INIT, st);
+    CU(launch_tree_init(t, h->meta[0], st, pdl));
+  }
 
   const float* feat0 = static_cast<const float*>(in->root_feat);
   if (c.feat_kind == EAGLE_FEAT_FUSED) {
@@ -452,7 +488,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
     }
     p.args.b.ldx = 3 * d;
     p.args.e = epi_store(h->g_root, d, nullptr, 0, nullptr, 0);
-    eagle_status_t r = run_gemm(h, p, B, st);
+    eagle_status_t r = run_gemm(h, p, B, st, EAGLE_K_FC3);
     if (r != EAGLE_OK) return r;
     feat0 = h->g_root;
   }
@@ -478,7 +514,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       b.emb = h->w.embed;
       b.emb_bf16 = h->tc ? 1 : 0;
       p.args.e = epi_store(h->h, d, nullptr, 0, h->ss_h, static_cast<int>(nmax));
-      if ((r = run_gemm(h, p, N, st)) != EAGLE_OK) return r;
+      if ((r = run_gemm(h, p, N, st, EAGLE_K_FC)) != EAGLE_OK) return r;
     }
     // RMSNorm + QKV + rotary
     {
@@ -510,7 +546,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       e.Hkv = c.n_kv_heads;
       e.hd = c.head_dim;
       e.tree_rows = h->R;
-      if ((r = run_gemm(h, p, N, st)) != EAGLE_OK) return r;
+      if ((r = run_gemm(h, p, N, st, EAGLE_K_QKV)) != EAGLE_OK) return r;
     }
     // tree-masked attention
     {
@@ -536,6 +572,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       a.part = h->att_part;
       a.counters = h->att_counters;
       a.out = h->o;
+      ProfScope ps(h, EAGLE_K_ATTN, st);
       CU(launch_attention(a, st, pdl));
     }
     // O projection + residual
@@ -545,7 +582,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       p.args.b.x = h->o;
       p.args.b.ldx = hq;
       p.args.e = epi_store(h->y, d, h->h, d, h->ss_y, static_cast<int>(nmax));
-      if ((r = run_gemm(h, p, N, st)) != EAGLE_OK) return r;
+      if ((r = run_gemm(h, p, N, st, EAGLE_K_OPROJ)) != EAGLE_OK) return r;
     }
     // RMSNorm + gate | up
     {
@@ -561,7 +598,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       b.eps = c.rms_eps;
       b.dnorm = d;
       p.args.e = epi_store(h->gu, 2 * ff, nullptr, 0, nullptr, 0);
-      if ((r = run_gemm(h, p, N, st)) != EAGLE_OK) return r;
+      if ((r = run_gemm(h, p, N, st, EAGLE_K_GATEUP)) != EAGLE_OK) return r;
     }
     // down projection of silu(g) * u + residual -> the next feature
     {
@@ -572,7 +609,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       b.ldx = 2 * ff;
       b.split = ff;
       p.args.e = epi_store(a_cur, d, h->y, d, nullptr, 0);
-      if ((r = run_gemm(h, p, N, st)) != EAGLE_OK) return r;
+      if ((r = run_gemm(h, p, N, st, EAGLE_K_DOWN)) != EAGLE_OK) return r;
     }
     // frozen LM head: online log-sum-exp + top-k partials
     if ((r = lm_head(h, a_cur, N, h->kids[s - 1], st)) != EAGLE_OK) return r;
@@ -589,6 +626,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
         if (trc->frontier) tr.frontier = trc->frontier + static_cast<size_t>(s - 1) * c.max_batch * h->f_max;
       }
       tr.f_max = h->f_max;
+      ProfScope ps(h, EAGLE_K_EXPAND, st);
       CU(launch_expand(t, s, lm_partials(h, N), cur, nxt, tr, st, pdl));
     }
     if (trc) {
@@ -607,7 +645,10 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
   o.logv = out->logv;
   o.mask = out->mask;
   o.final_nodes = trc ? trc->final_nodes : nullptr;
-  CU(launch_rerank(t, o, st, pdl));
+  {
+    ProfScope ps(h, EAGLE_K_RERANK, st);
+    CU(launch_rerank(t, o, st, pdl));
+  }
   if (trc && (trc->tree_k || trc->tree_v)) {
     const size_t n = static_cast<size_t>(B) * h->R * c.n_kv_heads * c.head_dim;
     if (trc->tree_k) CU(cudaMemcpyAsync(trc->tree_k, h->tk, n * 4, cudaMemcpyDeviceToDevice, st));
@@ -626,7 +667,7 @@ extern "C" eagle_status_t eagle_draft_tree(eagle_draft_t* h, const eagle_draft_i
   if (!out->tokens || !out->parents || !out->positions || !out->logv || !out->mask)
     return fail(EAGLE_ERR_INVALID_ARG, "null output pointer");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (trc || !h->use_graph) return enqueue_tree(h, in, out, trc, st);
+  if (trc || !h->use_graph || h->profiling) return enqueue_tree(h, in, out, trc, st);
   std::vector<const void*> key = {reinterpret_cast<const void*>(static_cast<intptr_t>(in->B)), in->root_feat,
                                   in->root_tok, in->k_cache, in->v_cache, in->cu_seqlens, out->tokens,
                                   out->parents, out->positions, out->logv, out->mask};
@@ -664,6 +705,35 @@ extern "C" eagle_status_t eagle_draft_lm_head_topk(eagle_draft_t* h, const float
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   eagle_status_t r = lm_head(h, a, N, k, st);
   if (r != EAGLE_OK) return r;
-  CU(launch_lm_merge(lm_partials(h, N), N, k, ids, logp, lse, st, h->use_pdl));
+  ProfScope ps(h, EAGLE_K_MERGE, st);
+  CU(launch_lm_merge(lm_partials(h, N), N, k, ids, logp, lse, st, h->use_pdl && !h->profiling));
   return EAGLE_OK;
+}
+
+extern "C" eagle_status_t eagle_draft_profile(eagle_draft_t* h, int32_t enable) {
+  if (!h) return fail(EAGLE_ERR_INVALID_ARG, "null handle");
+  h->profiling = enable != 0;
+  return EAGLE_OK;
+}
+
+extern "C" eagle_status_t eagle_draft_profile_read(eagle_draft_t* h, float* ms, int32_t* launches) {
+  if (!h || !ms || !launches) return fail(EAGLE_ERR_INVALID_ARG, "null argument");
+  for (int i = 0; i < EAGLE_K_COUNT; ++i) {
+    ms[i] = 0.f;
+    launches[i] = 0;
+  }
+  if (h->ev_used) CU(cudaEventSynchronize(h->ev_pool[h->ev_used - 1]));
+  for (size_t i = 0; i < h->ev_kind.size(); ++i) {
+    float t = 0.f;
+    CU(cudaEventElapsedTime(&t, h->ev_pool[2 * i], h->ev_pool[2 * i + 1]));
+    ms[h->ev_kind[i]] += t;
+    launches[h->ev_kind[i]] += 1;
+  }
+  h->ev_used = 0;
+  h->ev_kind.clear();
+  return EAGLE_OK;
+}
+
+extern "C" const char* eagle_draft_kernel_name(int32_t kind) {
+  return (kind >= 0 && kind < EAGLE_K_COUNT) ? kKernelNames[kind] : "?";
 }

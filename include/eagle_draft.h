@@ -194,6 +194,24 @@ EAGLE_API eagle_status_t eagle_draft_lm_head_topk(eagle_draft_t* handle, const f
                                         int32_t k, int32_t* ids, float* logp, float* lse,
                                         void* stream);
 
+/* Kernel kinds reported by the profiler. */
+typedef enum {
+  EAGLE_K_INIT = 0, EAGLE_K_FC3 = 1, EAGLE_K_FC = 2, EAGLE_K_QKV = 3, EAGLE_K_ATTN = 4,
+  EAGLE_K_OPROJ = 5, EAGLE_K_GATEUP = 6, EAGLE_K_DOWN = 7, EAGLE_K_LMHEAD = 8,
+  EAGLE_K_EXPAND = 9, EAGLE_K_RERANK = 10, EAGLE_K_MERGE = 11, EAGLE_K_COUNT = 12
+} eagle_kernel_kind_t;
+
+/* Profiling mode (enable != 0): every later call launches its kernels directly (no graph,
+ * no programmatic dependent launch) with a CUDA event recorded on the call's stream
+ * before and after each kernel.  eagle_draft_profile_read() synchronises, returns per
+ * kind the summed kernel time in ms (host array ms[EAGLE_K_COUNT]) and the number of
+ * launches (host array launches[EAGLE_K_COUNT]), and clears the records.  Disabling
+ * returns to graph replay. */
+EAGLE_API eagle_status_t eagle_draft_profile(eagle_draft_t* handle, int32_t enable);
+EAGLE_API eagle_status_t eagle_draft_profile_read(eagle_draft_t* handle, float* ms, int32_t* launches);
+/* Short name of a kernel kind ("lm_head", ...); "?" outside the range. */
+EAGLE_API const char* eagle_draft_kernel_name(int32_t kind);
+
 /* Sizes of the handle's buffers (host struct). */
 EAGLE_API eagle_status_t eagle_draft_query(const eagle_draft_t* handle, eagle_draft_info_t* info);
 
