@@ -95,6 +95,8 @@ def load(path: str = LIB_PATH):
     lib.eagle_draft_profile_read.restype = C.c_int
     lib.eagle_draft_kernel_name.argtypes = [C.c_int32]
     lib.eagle_draft_kernel_name.restype = C.c_char_p
+    lib.eagle_lm_head_topk_noalloc.argtypes = [P, C.c_int32, C.c_int32, P, C.c_int32, C.c_int32, P, P, P, P]
+    lib.eagle_lm_head_topk_noalloc.restype = C.c_int
     lib.eagle_draft_last_error.argtypes = []
     lib.eagle_draft_last_error.restype = C.c_char_p
     _lib = lib
@@ -145,6 +147,20 @@ def device_weights(W: dict, device="cuda"):
 
 def device_inputs(I: dict, device="cuda"):
     return device_weights(I, device)
+
+
+def lm_head_topk_noalloc(w_lm, a, k: int, stream=None):
+    """LM-head top-k without a handle and without any device allocation inside the
+    library (for callers that cannot allocate); outputs are allocated here by torch."""
+    import torch
+    N, d = int(a.shape[0]), int(a.shape[1])
+    ids = torch.empty((N, k), dtype=torch.int32, device=a.device)
+    logp = torch.empty((N, k), dtype=torch.float32, device=a.device)
+    lse = torch.empty((N,), dtype=torch.float32, device=a.device)
+    st = None if stream is None else stream.cuda_stream
+    _check(load().eagle_lm_head_topk_noalloc(_ptr(w_lm), int(w_lm.shape[0]), d, _ptr(a), N, k,
+                                             _ptr(ids), _ptr(logp), _ptr(lse), st))
+    return ids, logp, lse
 
 
 class EagleDraft:

@@ -335,6 +335,9 @@ extern "C" void eagle_draft_destroy(eagle_draft_t* h) {
 
 extern "C" const char* eagle_draft_last_error(void) { return g_last_error.c_str(); }
 
+// Lets the other translation units of the library report through eagle_draft_last_error().
+void eagle::set_last_error(const char* msg) { g_last_error = msg; }
+
 extern "C" eagle_status_t eagle_draft_query(const eagle_draft_t* h, eagle_draft_info_t* info) {
   if (!h || !info) return fail(EAGLE_ERR_INVALID_ARG, "null argument");
   info->slots = h->S;

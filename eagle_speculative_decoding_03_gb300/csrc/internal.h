@@ -5,6 +5,9 @@
 
 namespace eagle {
 
+// Message returned by eagle_draft_last_error() on this thread.
+void set_last_error(const char* msg);
+
 // ----------------------------------------------------------------- GEMM
 struct GemmPlan {
   bool tc = false;               // tcgen05 mainloop (bf16 weights) or SIMT (f32 weights)

@@ -194,6 +194,28 @@ EAGLE_API eagle_status_t eagle_draft_lm_head_topk(eagle_draft_t* handle, const f
                                         int32_t k, int32_t* ids, float* logp, float* lse,
                                         void* stream);
 
+/* Allocation-free variant of eagle_draft_lm_head_topk, with no handle.  The pages on
+ * EAGLE have no counterpart: this exists for callers that cannot call cudaMalloc - e.g.
+ * a serving engine that reserved nearly all device memory for its own pools at start-up,
+ * or a latency-critical loop where an allocation would synchronise the device.  The
+ * same LM-head and merge kernels run, but their scratch (split-K partial tiles, arrival
+ * counters, per-tile log-sum-exp and per-CTA top-k partials) lives in one 4 MiB
+ * file-scope device array that every GPU loading the library holds until exit; the call
+ * allocates nothing.
+ * w_lm: bf16 [vocab, d]; a: f32 [N, d]; ids int32 [N, k] (descending logit, ties to the
+ * lower id), logp f32 [N, k], lse f32 [N]; all device pointers, 16-byte aligned.
+ * Limits (EAGLE_ERR_INVALID_ARG beyond them, message in eagle_draft_last_error()):
+ * 1 <= N <= 16, 1 <= k <= 16, vocab and d multiples of 128 with vocab <= 131072 and
+ * d <= 16384; EAGLE_ERR_UNSUPPORTED on a device with more than 192 SMs.
+ * The first call on a device looks up the array's device address and sets the kernels'
+ * shared-memory limits (make that first call before any stream capture).  Every call
+ * shares the array and clears the parts that must start at zero; calls whose kernels
+ * overlap on the GPU (other streams, other threads) race on it and give wrong results. */
+EAGLE_API eagle_status_t eagle_lm_head_topk_noalloc(const void* w_lm, int32_t vocab, int32_t d,
+                                                    const float* a, int32_t N, int32_t k,
+                                                    int32_t* ids, float* logp, float* lse,
+                                                    void* stream);
+
 /* Kernel kinds reported by the profiler. */
 typedef enum {
   EAGLE_K_INIT = 0, EAGLE_K_FC3 = 1, EAGLE_K_FC = 2, EAGLE_K_QKV = 3, EAGLE_K_ATTN = 4,
