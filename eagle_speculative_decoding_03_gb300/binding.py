@@ -23,7 +23,7 @@ FEAT_F, FEAT_FUSED = 1, 3
 FLAG_NO_GRAPH, FLAG_NO_PDL = 1, 2
 MAX_DEPTH = 16
 KERNEL_KINDS = 12
-DEVERR_TIMEOUT, DEVERR_PREFIX = 1, 2
+DEVERR_TIMEOUT, DEVERR_PREFIX, DEVERR_TOKEN = 1, 2, 4
 
 
 class Config(C.Structure):

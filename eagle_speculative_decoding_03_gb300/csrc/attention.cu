@@ -198,7 +198,15 @@ tree_attention_kernel(const AttnArgs a) {
       O += w * __ldcg(ps + 2 + d);
     }
     const int i = v / gq, gh = v - i * gq;
-    a.out[(static_cast<size_t>(row0 + i) * a.Hq + kvh * gq + gh) * hd + d] = O / L;
+    const float val = O / L;
+    a.out[(static_cast<size_t>(row0 + i) * a.Hq + kvh * gq + gh) * hd + d] = val;
+    if (a.out_hl) {   // bf16 hi / lo rows: the O projection's operand copy
+      uint16_t hi, lo;
+      split_hilo(val, hi, lo);
+      const size_t ld = static_cast<size_t>(a.Hq) * hd, col = static_cast<size_t>(kvh * gq + gh) * hd + d;
+      a.out_hl[2 * static_cast<size_t>(row0 + i) * ld + col] = hi;
+      a.out_hl[(2 * static_cast<size_t>(row0 + i) + 1) * ld + col] = lo;
+    }
   }
 }
 

@@ -23,6 +23,7 @@ constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;   // ~1 s at 2 GHz
 
 constexpr unsigned DEVERR_TIMEOUT = 0x1u;
 constexpr unsigned DEVERR_PREFIX = 0x2u;
+constexpr unsigned DEVERR_TOKEN = 0x4u;
 
 // ---------------------------------------------------------- small helpers
 EAGLE_DEV uint32_t smem_u32(const void* p) {
@@ -204,7 +205,8 @@ enum BMode : int {
   B_NORM = 1,     // RMSNorm: x[row][k] * rstd[row] * gamma[k], rstd from sum-of-squares partials
   B_FC = 2,       // [feat(row_feat[row]) ; emb(row_tok[row])]: K = 2 * split
   B_SWIGLU = 3,   // silu(x[row][k]) * x[row][split + k] (gate | up halves)
-  B_BF16 = 4      // x[row][k] bf16
+  B_BF16 = 4,     // x[row][k] bf16
+  B_TMA = 5       // tile loaded by TMA from an operand copy: bf16 rows 2r = hi(x_r), 2r+1 = lo(x_r)
 };
 
 struct BSrc {
@@ -226,7 +228,7 @@ struct BSrc {
   int emb_bf16;
 };
 
-enum EpiKind : int { EPI_STORE = 0, EPI_QKV = 1, EPI_LMHEAD = 2 };
+enum EpiKind : int { EPI_STORE = 0, EPI_QKV = 1, EPI_LMHEAD = 2, EPI_SWIGLU = 3 };
 
 struct EpiArgs {
   int kind;
@@ -254,12 +256,24 @@ struct EpiArgs {
   float* lm_val;           // [grid][N][k]
   int* lm_id;              // [grid][N][k]
   int topk;
+  // operand copy for the next GEMM (EPI_STORE, EPI_SWIGLU):
+  // hl[2 row][m] = hi, hl[2 row + 1][m] = lo of value * hl_gamma[m] (hl_gamma may be null)
+  uint16_t* hl;
+  int hl_ld;
+  const float* hl_gamma;
+  // factored RMSNorm of the operand (EPI_QKV, EPI_SWIGLU): acc[row] *= 1/sqrt(mean + eps),
+  // mean from the producer's per-tile sums of squares nss[tile][row]
+  const float* nss;
+  int nss_tiles, nss_ld, nss_d;
+  float nss_eps;
 };
 
 struct GemmArgs {
   int M, K, N;             // N = rows
   int MT, KB;              // tiles of M (per weight map), K blocks
   int m_split;             // rows [0, m_split) from weight map 0, [m_split, M) from map 1
+  int a_pair;              // tile = 64 rows of map 0 + the same 64 rows of map 1 (gate | up)
+  int b_tma;               // activation tile by TMA (operand copy) instead of the converter warps
   int npad;                // padded rows per row block (multiple of 16)
   int nrb;                 // row blocks
   int tmem_cols;           // allocated TMEM columns

@@ -62,6 +62,8 @@ struct eagle_draft {
   float *ss_h = nullptr, *ss_y = nullptr, *g_root = nullptr, *tk = nullptr, *tv = nullptr;
   float *rope_cos = nullptr, *rope_sin = nullptr, *part = nullptr, *att_part = nullptr;
   float *lm_max = nullptr, *lm_sum = nullptr, *lm_val = nullptr;
+  // bf16 hi/lo operand copies [2 N_max][K] written by the producing epilogue (tensor-core path)
+  uint16_t *xa_hl = nullptr, *o_hl = nullptr, *xm_hl = nullptr, *s_hl = nullptr, *a_hl = nullptr;
   int *lm_id = nullptr, *counters = nullptr, *att_counters = nullptr;
   int *node_tok = nullptr, *node_parent = nullptr, *node_depth = nullptr, *node_row = nullptr;
   float* node_logv = nullptr;
@@ -166,6 +168,11 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   h->q = cv.take<float>(static_cast<size_t>(n) * hq);
   h->o = cv.take<float>(static_cast<size_t>(n) * hq);
   h->gu = cv.take<float>(static_cast<size_t>(n) * 2 * c.d_ff);
+  h->xa_hl = cv.take<uint16_t>(static_cast<size_t>(2 * n) * d);
+  h->o_hl = cv.take<uint16_t>(static_cast<size_t>(2 * n) * hq);
+  h->xm_hl = cv.take<uint16_t>(static_cast<size_t>(2 * n) * d);
+  h->s_hl = cv.take<uint16_t>(static_cast<size_t>(2 * n) * c.d_ff);
+  h->a_hl = cv.take<uint16_t>(static_cast<size_t>(2 * n) * d);
   h->ss_h = cv.take<float>(static_cast<size_t>(dt) * n);
   h->ss_y = cv.take<float>(static_cast<size_t>(dt) * n);
   h->g_root = cv.take<float>(static_cast<size_t>(B) * d);
@@ -277,8 +284,8 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
     const int d = c.d, ff = c.d_ff, hq = c.n_heads * c.head_dim;
     const int qkv = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
     bool ok = make_weight_map(&h->tm_fc, h->w.w_fc, d, 2 * d) && make_weight_map(&h->tm_qkv, h->w.w_qkv, qkv, d) &&
-              make_weight_map(&h->tm_o, h->w.w_o, d, hq) && make_weight_map(&h->tm_gate, h->w.w_gate, ff, d) &&
-              make_weight_map(&h->tm_up, h->w.w_up, ff, d) && make_weight_map(&h->tm_down, h->w.w_down, d, ff) &&
+              make_weight_map(&h->tm_o, h->w.w_o, d, hq) && make_weight_map(&h->tm_gate, h->w.w_gate, ff, d, BM / 2) &&
+              make_weight_map(&h->tm_up, h->w.w_up, ff, d, BM / 2) && make_weight_map(&h->tm_down, h->w.w_down, d, ff) &&
               make_weight_map(&h->tm_lm, h->w.w_lm, c.vocab, d);
     if (ok && c.feat_kind == EAGLE_FEAT_FUSED) ok = make_weight_map(&h->tm_fc3, h->w.w_fc3, d, 3 * d);
     if (!ok) { delete h; return fail(EAGLE_ERR_CUDA, "cuTensorMapEncodeTiled failed (weights must be 16-byte aligned)"); }
@@ -401,6 +408,29 @@ static EpiArgs epi_store(float* out, int ldo, const float* resid, int ldr, float
   return e;
 }
 
+// Operand tile loaded by TMA from a bf16 hi/lo copy written by the producing kernel.
+static void tma_operand(GemmPlan& p, const uint16_t* hl) {
+  p.args.b.mode = B_TMA;
+  p.args.b_tma = 1;
+  p.b_hl = hl;
+}
+
+// The producing epilogue also writes the next GEMM's operand copy (value * gamma).
+static void write_operand(EpiArgs& e, uint16_t* hl, int ld, const float* gamma) {
+  e.hl = hl;
+  e.hl_ld = ld;
+  e.hl_gamma = gamma;
+}
+
+// The consumer applies the RMSNorm row scale in its epilogue.
+static void factored_norm(EpiArgs& e, const float* ss, int tiles, int ld, int d, float eps) {
+  e.nss = ss;
+  e.nss_tiles = tiles;
+  e.nss_ld = ld;
+  e.nss_d = d;
+  e.nss_eps = eps;
+}
+
 static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t st, int kind) {
   if (!plan_gemm(p, N)) return fail(EAGLE_ERR_UNSUPPORTED, "GEMM M=%d K=%d N=%d does not fit", p.args.M, p.args.K, N);
   ProfScope ps(h, kind, st);
@@ -408,12 +438,14 @@ static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t 
   return EAGLE_OK;
 }
 
-static eagle_status_t lm_head(eagle_draft* h, const float* a, int N, int topk, cudaStream_t st) {
+static eagle_status_t lm_head(eagle_draft* h, const float* a, const uint16_t* a_hl, int N, int topk,
+                              cudaStream_t st) {
   const eagle_draft_config_t& c = h->cfg;
   GemmPlan p = base_plan(h, h->tm_lm, nullptr, h->w.w_lm, nullptr, c.vocab, c.d, c.vocab);
   p.args.b.mode = B_F32;
   p.args.b.x = a;
   p.args.b.ldx = c.d;
+  if (a_hl) tma_operand(p, a_hl);
   EpiArgs& e = p.args.e;
   e.kind = EPI_LMHEAD;
   e.lm_max = h->lm_max;
@@ -462,6 +494,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
   t.tree_rows = h->R;
   t.max_nodes = h->max_nodes;
   t.max_prefix = c.max_prefix;
+  t.vocab = c.vocab;
   t.root_tok = in->root_tok;
   t.cu_seqlens = in->cu_seqlens;
   t.node_tok = h->node_tok;
@@ -517,6 +550,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       b.emb = h->w.embed;
       b.emb_bf16 = h->tc ? 1 : 0;
       p.args.e = epi_store(h->h, d, nullptr, 0, h->ss_h, static_cast<int>(nmax));
+      if (h->tc) write_operand(p.args.e, h->xa_hl, d, h->w.attn_norm);
       if ((r = run_gemm(h, p, N, st, EAGLE_K_FC)) != EAGLE_OK) return r;
     }
     // RMSNorm + QKV + rotary
@@ -549,6 +583,10 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       e.Hkv = c.n_kv_heads;
       e.hd = c.head_dim;
       e.tree_rows = h->R;
+      if (h->tc) {
+        tma_operand(p, h->xa_hl);
+        factored_norm(e, h->ss_h, ceil_div(d, BM), static_cast<int>(nmax), d, c.rms_eps);
+      }
       if ((r = run_gemm(h, p, N, st, EAGLE_K_QKV)) != EAGLE_OK) return r;
     }
     // tree-masked attention
@@ -575,6 +613,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       a.part = h->att_part;
       a.counters = h->att_counters;
       a.out = h->o;
+      a.out_hl = h->tc ? h->o_hl : nullptr;
       ProfScope ps(h, EAGLE_K_ATTN, st);
       CU(launch_attention(a, st, pdl));
     }
@@ -585,11 +624,16 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       p.args.b.x = h->o;
       p.args.b.ldx = hq;
       p.args.e = epi_store(h->y, d, h->h, d, h->ss_y, static_cast<int>(nmax));
+      if (h->tc) {
+        tma_operand(p, h->o_hl);
+        write_operand(p.args.e, h->xm_hl, d, h->w.mlp_norm);
+      }
       if ((r = run_gemm(h, p, N, st, EAGLE_K_OPROJ)) != EAGLE_OK) return r;
     }
-    // RMSNorm + gate | up
+    // RMSNorm + gate | up; the tensor-core path emits silu(g) * u directly
     {
-      GemmPlan p = base_plan(h, h->tm_gate, &h->tm_up, h->w.w_gate, h->w.w_up, 2 * ff, d, ff);
+      GemmPlan p = h->tc ? base_plan(h, h->tm_gate, &h->tm_up, nullptr, nullptr, 2 * ff, d, 2 * ff)
+                         : base_plan(h, h->tm_gate, &h->tm_up, h->w.w_gate, h->w.w_up, 2 * ff, d, ff);
       BSrc& b = p.args.b;
       b.mode = B_NORM;
       b.x = h->y;
@@ -600,22 +644,36 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       b.gamma = h->w.mlp_norm;
       b.eps = c.rms_eps;
       b.dnorm = d;
-      p.args.e = epi_store(h->gu, 2 * ff, nullptr, 0, nullptr, 0);
+      if (h->tc) {
+        p.args.a_pair = 1;
+        p.args.e = epi_store(nullptr, ff, nullptr, 0, nullptr, 0);
+        p.args.e.kind = EPI_SWIGLU;
+        tma_operand(p, h->xm_hl);
+        factored_norm(p.args.e, h->ss_y, ceil_div(d, BM), static_cast<int>(nmax), d, c.rms_eps);
+        write_operand(p.args.e, h->s_hl, ff, nullptr);
+      } else {
+        p.args.e = epi_store(h->gu, 2 * ff, nullptr, 0, nullptr, 0);
+      }
       if ((r = run_gemm(h, p, N, st, EAGLE_K_GATEUP)) != EAGLE_OK) return r;
     }
     // down projection of silu(g) * u + residual -> the next feature
     {
       GemmPlan p = base_plan(h, h->tm_down, nullptr, h->w.w_down, nullptr, d, ff, d);
       BSrc& b = p.args.b;
-      b.mode = B_SWIGLU;
-      b.x = h->gu;
-      b.ldx = 2 * ff;
-      b.split = ff;
+      if (h->tc) {
+        tma_operand(p, h->s_hl);
+      } else {
+        b.mode = B_SWIGLU;
+        b.x = h->gu;
+        b.ldx = 2 * ff;
+        b.split = ff;
+      }
       p.args.e = epi_store(a_cur, d, h->y, d, nullptr, 0);
+      if (h->tc) write_operand(p.args.e, h->a_hl, d, nullptr);
       if ((r = run_gemm(h, p, N, st, EAGLE_K_DOWN)) != EAGLE_OK) return r;
     }
     // frozen LM head: online log-sum-exp + top-k partials
-    if ((r = lm_head(h, a_cur, N, h->kids[s - 1], st)) != EAGLE_OK) return r;
+    if ((r = lm_head(h, a_cur, h->tc ? h->a_hl : nullptr, N, h->kids[s - 1], st)) != EAGLE_OK) return r;
     // children, values, next frontier
     {
       ExpandTrace tr;
@@ -705,8 +763,9 @@ extern "C" eagle_status_t eagle_draft_lm_head_topk(eagle_draft_t* h, const float
   if (!h || !a || !ids || !logp || !lse) return fail(EAGLE_ERR_INVALID_ARG, "null argument");
   if (N < 1 || N > h->n_max) return fail(EAGLE_ERR_INVALID_ARG, "N=%d outside 1..%d", N, h->n_max);
   if (k < 1 || k > KMAX) return fail(EAGLE_ERR_INVALID_ARG, "k=%d outside 1..%d", k, KMAX);
+  if (reinterpret_cast<uintptr_t>(a) % 16) return fail(EAGLE_ERR_INVALID_ARG, "a must be 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  eagle_status_t r = lm_head(h, a, N, k, st);
+  eagle_status_t r = lm_head(h, a, nullptr, N, k, st);
   if (r != EAGLE_OK) return r;
   ProfScope ps(h, EAGLE_K_MERGE, st);
   CU(launch_lm_merge(lm_partials(h, N), N, k, ids, logp, lse, st, h->use_pdl && !h->profiling));

@@ -116,6 +116,7 @@ struct EpiSmem {
   int* st_cnt;
   float* lv;               // [N][k] running top-k values (sorted)
   int* li;                 // [N][k] and their token ids
+  float* rstd;             // [N] factored RMSNorm scale of each row (EPI_QKV / EPI_SWIGLU)
 };
 
 EAGLE_DEV EpiSmem epi_views(void* scratch, void* lm, int N, int topk) {
@@ -127,7 +128,27 @@ EAGLE_DEV EpiSmem epi_views(void* scratch, void* lm, int N, int topk) {
   es.st_cnt = reinterpret_cast<int*>(f + 2 * N);
   es.lv = f + 3 * N;
   es.li = reinterpret_cast<int*>(f + 3 * N + N * topk);
+  es.rstd = nullptr;
   return es;
+}
+
+// hi / lo rows of the operand copy the next GEMM loads with TMA
+EAGLE_DEV void write_hl(const EpiArgs& e, int n, int m, float val) {
+  if (e.hl_gamma) val *= __ldg(e.hl_gamma + m);
+  uint16_t hi, lo;
+  split_hilo(val, hi, lo);
+  e.hl[static_cast<size_t>(2 * n) * e.hl_ld + m] = hi;
+  e.hl[static_cast<size_t>(2 * n + 1) * e.hl_ld + m] = lo;
+}
+
+// 1 / sqrt(mean(x^2) + eps) per row from the producer's per-tile sums of squares.
+EAGLE_DEV void epi_rstd(const EpiArgs& e, int N, float* rstd, int tl) {
+  for (int n = tl; n < N; n += 128) {
+    float s = 0.f;
+    for (int t = 0; t < e.nss_tiles; ++t) s += __ldcg(e.nss + static_cast<size_t>(t) * e.nss_ld + n);
+    rstd[n] = 1.0f / sqrtf(s / static_cast<float>(e.nss_d) + e.nss_eps);
+  }
+  named_bar(1, 128);
 }
 
 // AND of a predicate over the 128 epilogue threads (named barrier 1).
@@ -203,6 +224,7 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
       if (n < g.N && mvalid) {
         if (e.resid) val += __ldcg(e.resid + static_cast<size_t>(n) * e.ldr + m);
         e.out[static_cast<size_t>(n) * e.ldo + m] = val;
+        if (e.hl) write_hl(e, n, m, val);
         sq[i] = val * val;
       }
     }
@@ -222,15 +244,19 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
     const int hd = e.hd, half = hd >> 1;
     const int head = m / hd, i = m - head * hd;
     const bool rotate = head < e.Hq + e.Hkv;
+    float vn[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) es.s->xch[r][tl] = v[r];
+    for (int r = 0; r < 16; ++r) {
+      vn[r] = (e.nss && n0 + r < g.N) ? v[r] * es.rstd[n0 + r] : v[r];
+      es.s->xch[r][tl] = vn[r];
+    }
     named_bar(1, 128);
     const int partner = tl + (i < half ? half : -half);
 #pragma unroll 4
     for (int r = 0; r < 16; ++r) {
       const int n = n0 + r;
       if (n >= g.N || !mvalid) continue;
-      float val = v[r];
+      float val = vn[r];
       const int pos = __ldcg(e.row_pos + n);
       if (rotate) {
         const int j = i < half ? i : i - half;
@@ -247,6 +273,29 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
         const int kvh = isk ? head - e.Hq : head - e.Hq - e.Hkv;
         float* dst = isk ? e.tk : e.tv;
         dst[((static_cast<size_t>(b) * e.tree_rows + slot) * e.Hkv + kvh) * hd + i] = val;
+      }
+    }
+    named_bar(1, 128);
+  } else if (e.kind == EPI_SWIGLU) {
+    // tile = 64 gate rows (threads 0-63) + the 64 matching up rows (threads 64-127)
+#pragma unroll
+    for (int r = 0; r < 16; ++r) es.s->xch[r][tl] = v[r];
+    named_bar(1, 128);
+    if (tl < 64) {
+      const int j = mt * (BM / 2) + tl;
+#pragma unroll 4
+      for (int r = 0; r < 16; ++r) {
+        const int n = n0 + r;
+        if (n < g.N) {
+          float gt = es.s->xch[r][tl], up = es.s->xch[r][tl + 64];
+          if (e.nss) {
+            gt *= es.rstd[n];
+            up *= es.rstd[n];
+          }
+          const float sv = silu_f(gt) * up;
+          if (e.out) e.out[static_cast<size_t>(n) * e.ldo + j] = sv;
+          if (e.hl) write_hl(e, n, j, sv);
+        }
       }
     }
     named_bar(1, 128);
@@ -328,42 +377,61 @@ struct Sched {
 // ============================================================ tcgen05 mainloop
 struct TcLayout {
   uint32_t stage_bytes, b_off;
-  uint32_t bar_off, misc_off, epi_off, rstd_off, lm_off;
+  uint32_t bar_off, misc_off, idx_off, epi_off, rstd_off, erstd_off, lm_off;
 };
 
-__host__ __device__ inline TcLayout tc_layout(int npad, int stages, int N, int topk) {
+// Shared memory of gemm_tc_kernel: [stages x (A tile 16 KB | B tile npad*256 B)] |
+// mbarriers | misc words | gathered row indices | epilogue scratch | rstd | LM-head lists.
+__host__ __device__ inline TcLayout tc_layout(int npad, int stages) {
   TcLayout L;
   L.b_off = A_STAGE_BYTES;
-  L.stage_bytes = A_STAGE_BYTES + npad * 2 * 128;
+  L.stage_bytes = A_STAGE_BYTES + npad * 256;
   L.bar_off = L.stage_bytes * stages;
-  L.misc_off = L.bar_off + (2 * stages + 4) * 8;
-  L.epi_off = (L.misc_off + 64 + 127) & ~127u;
+  L.misc_off = L.bar_off + (3 * stages + 4) * 8;
+  L.idx_off = (L.misc_off + 64 + 15) & ~15u;
+  L.epi_off = (L.idx_off + 2 * 256 * 4 + 127) & ~127u;
   L.rstd_off = L.epi_off + static_cast<uint32_t>((sizeof(EpiScratch) + 127) & ~size_t(127));
-  L.lm_off = L.rstd_off + sizeof(float) * 256;
-  (void)N;
-  (void)topk;
+  L.erstd_off = L.rstd_off + sizeof(float) * 256;
+  L.lm_off = L.erstd_off + sizeof(float) * 256;
   return L;
 }
-__host__ __device__ inline uint32_t tc_smem_bytes(int npad, int stages, int N, int topk) {
-  TcLayout L = tc_layout(npad, stages, N, topk);
-  return L.lm_off + static_cast<uint32_t>(N) * (3 + 2 * topk) * 4 + 1024;  // +1024: base alignment
+__host__ __device__ inline uint32_t tc_smem_bytes(int npad, int stages, int lm_rows, int topk) {
+  TcLayout L = tc_layout(npad, stages);
+  return L.lm_off + static_cast<uint32_t>(lm_rows) * (3 + 2 * topk) * 4 + 1024;  // +1024: base alignment
 }
 
-template <int NLW>
-__global__ void __launch_bounds__((6 + NLW) * 32, 1)
+EAGLE_DEV void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+constexpr int TC_NCW = 4;                       // converter warps
+constexpr int TC_THREADS = (7 + TC_NCW) * 32;   // A producer, MMA, 4 epilogue, B producer, converters
+
+// Warp roles: 0 = weight TMA producer, 1 = MMA issuer, 2-5 = epilogue (TMEM lanes by
+// warp % 4), 6 = activation producer (bulk copies of the source rows into the B tile),
+// 7.. = converters (in place: fp32 / bf16 row -> bf16 hi row + bf16 lo row, swizzled).
+// B tile rows are interleaved: row 2r = hi of GEMM row r, row 2r+1 = its lo part, so the
+// accumulator column 2r + 1 holds the low-order correction of column 2r.
+__global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
-               const GemmArgs g) {
+               const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const TcLayout L = tc_layout(g.npad, g.stages, g.N, g.e.topk);
+  const TcLayout L = tc_layout(g.npad, g.stages);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + L.bar_off;
   const uint32_t bar_empty = bar_full + 8 * g.stages;
-  const uint32_t bar_accf = bar_empty + 8 * g.stages;
+  const uint32_t bar_bfull = bar_empty + 8 * g.stages;
+  const uint32_t bar_accf = bar_bfull + 8 * g.stages;
   const uint32_t bar_acce = bar_accf + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
   int* last_flag = reinterpret_cast<int*>(smem + L.misc_off + 8);
+  int* s_feat = reinterpret_cast<int*>(smem + L.idx_off);
+  int* s_tok = s_feat + 256;
   float* rstd = reinterpret_cast<float*>(smem + L.rstd_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -374,12 +442,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < g.stages; ++s) {
-      mbar_init(bar_full + 8 * s, 2);        // TMA bytes + one loader warp
-      mbar_init(bar_empty + 8 * s, 1);       // tcgen05.commit
+      mbar_init(bar_full + 8 * s, 2);            // weight bytes + activation (TMA bytes or converter)
+      mbar_init(bar_empty + 8 * s, 1);           // tcgen05.commit
+      mbar_init(bar_bfull + 8 * s, 1);           // bulk-copy bytes of the source rows
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_accf + 8 * b, 1);
-      mbar_init(bar_acce + 8 * b, 4);        // one arrive per epilogue warp
+      mbar_init(bar_acce + 8 * b, 4);            // one arrive per epilogue warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -391,6 +460,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
   if (warp == 1 && lane == 0) {
     tma_prefetch_desc(&tm0);
     tma_prefetch_desc(&tm1);
+    if (g.b_tma) tma_prefetch_desc(&tmB);
   }
   tc_fence_before();
   __syncthreads();
@@ -400,6 +470,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer (weights)
+    // Weights never depend on the previous kernel: streaming starts before its end.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int stage = 0;
@@ -408,14 +479,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
       for (long long i = u0; i < u1 && ok;) {
         const int mt = static_cast<int>(i / KB), kb0 = static_cast<int>(i % KB);
         const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
-        const bool second = mt * BM >= g.m_split;
+        const bool second = !g.a_pair && mt * BM >= g.m_split;
         const CUtensorMap* tm = second ? &tm1 : &tm0;
-        const int mrow = second ? mt * BM - g.m_split : mt * BM;
+        const int mrow = g.a_pair ? mt * (BM / 2) : (second ? mt * BM - g.m_split : mt * BM);
         for (int kb = kb0; kb < kb1 && ok; ++kb) {
           for (int rb = 0; rb < nrb && ok; ++rb) {
             if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
+            const uint32_t dst = sbase + stage * L.stage_bytes;
             mbar_arrive_expect_tx(bar_full + 8 * stage, A_STAGE_BYTES);
-            tma_load_2d(sbase + stage * L.stage_bytes, tm, kb * BK, mrow, bar_full + 8 * stage, pol);
+            if (g.a_pair) {  // rows 0-63 from map 0 (gate), rows 64-127 from map 1 (up)
+              tma_load_2d(dst, &tm0, kb * BK, mrow, bar_full + 8 * stage, pol);
+              tma_load_2d(dst + A_STAGE_BYTES / 2, &tm1, kb * BK, mrow, bar_full + 8 * stage, pol);
+            } else {
+              tma_load_2d(dst, tm, kb * BK, mrow, bar_full + 8 * stage, pol);
+            }
             if (++stage == g.stages) { stage = 0; phase ^= 1; }
           }
         }
@@ -468,57 +545,146 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
         }
       }
     }
-  } else if (warp >= 6) {
-    // --------------------------------------------- activation operand loaders
-    const int lw = warp - 6;
+  } else if (warp == 6 && g.b_tma) {
+    // ------------------------- activation producer: TMA of the operand copy's tile
+    // (written by the previous kernel: wait for it; the weight stream does not)
+    if (lane == 0) {
+      pdl_wait();
+      uint64_t pol_b;
+      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_b));
+      const uint32_t b_bytes = static_cast<uint32_t>(npad) * 256u;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (long long i = u0; i < u1 && ok;) {
+        const int kb0 = static_cast<int>(i % KB);
+        const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
+        for (int kb = kb0; kb < kb1 && ok; ++kb) {
+          for (int rb = 0; rb < nrb && ok; ++rb) {
+            if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar_full + 8 * stage, b_bytes);
+            tma_load_2d(sbase + stage * L.stage_bytes + L.b_off, &tmB, kb * BK, rb * np2, bar_full + 8 * stage,
+                        pol_b);
+            if (++stage == g.stages) { stage = 0; phase ^= 1; }
+          }
+        }
+        i += kb1 - kb0;
+      }
+      if (!ok) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 4000000) {
+        }
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------- activation producer: bulk copies of source rows
     pdl_wait();
-    compute_rstd(g.b, g.N, rstd, (warp - 6) * 32 + lane, NLW * 32);
-    named_bar(2, NLW * 32);
+    if (g.b.mode == B_FC) {
+      for (int n = lane; n < g.N; n += 32) {
+        s_feat[n] = __ldcg(g.b.row_feat + n);
+        s_tok[n] = __ldcg(g.b.row_tok + n);
+      }
+    }
+    __syncwarp();
     int stage = 0;
     uint32_t phase = 0;
-    long long it = 0;
     bool ok = true;
     for (long long i = u0; i < u1 && ok;) {
       const int kb0 = static_cast<int>(i % KB);
       const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
+        const int k0 = kb * BK;
+        const bool bf = g.b.mode == B_BF16 || (g.b.mode == B_FC && k0 >= g.b.split);
+        const uint32_t rowbytes = bf ? 128u : 256u;
+        for (int rb = 0; rb < nrb; ++rb) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag));
+          if (!ok) break;
+          const int r0 = rb * npad;
+          const int rows = min(npad, g.N - r0);
+          const uint32_t bdst = sbase + stage * L.stage_bytes + L.b_off;
+          if (lane == 0) mbar_arrive_expect_tx(bar_bfull + 8 * stage, static_cast<uint32_t>(rows) * rowbytes);
+          __syncwarp();
+          for (int r = lane; r < rows; r += 32) {
+            const int n = r0 + r;
+            const void* src;
+            if (g.b.mode == B_FC) {
+              src = k0 < g.b.split
+                        ? static_cast<const void*>(g.b.x + static_cast<size_t>(s_feat[n]) * g.b.ldx + k0)
+                        : static_cast<const void*>(static_cast<const uint16_t*>(g.b.emb) +
+                                                   static_cast<size_t>(s_tok[n]) * g.b.split + (k0 - g.b.split));
+            } else if (g.b.mode == B_BF16) {
+              src = g.b.xb + static_cast<size_t>(n) * g.b.ldx + k0;
+            } else {
+              src = g.b.x + static_cast<size_t>(n) * g.b.ldx + k0;
+            }
+            bulk_copy_g2s(bdst + 256u * r, src, rowbytes, bar_bfull + 8 * stage);
+          }
+          if (++stage == g.stages) { stage = 0; phase ^= 1; }
+        }
+      }
+      i += kb1 - kb0;
+    }
+    if (!ok) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < 4000000) {
+      }
+    }
+  } else if (warp >= 7 && !g.b_tma) {
+    // ------------------------------------ converters: source row -> bf16 hi / lo rows
+    // Stage-iteration it is converted by warp it % TC_NCW (all of its rows).
+    const int cw = warp - 7;
+    pdl_wait();
+    compute_rstd(g.b, g.N, rstd, cw * 32 + lane, TC_NCW * 32);
+    named_bar(2, TC_NCW * 32);
+    int stage = 0;
+    uint32_t phase = 0;
+    long long it = 0;
+    bool ok = true;
+    const uint32_t cbyte = (4u * lane) & 15u;
+    const int chunk = lane >> 2;
+    for (long long i = u0; i < u1 && ok;) {
+      const int kb0 = static_cast<int>(i % KB);
+      const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
+      for (int kb = kb0; kb < kb1 && ok; ++kb) {
+        const int k0 = kb * BK;
+        const bool bf = g.b.mode == B_BF16 || (g.b.mode == B_FC && k0 >= g.b.split);
         for (int rb = 0; rb < nrb; ++rb, ++it) {
-          if (it % NLW == lw) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag));
+          if (it % TC_NCW == cw) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_bfull + 8 * stage, phase, g.err, abort_flag));
             if (!ok) break;
+            float gm0 = 1.f, gm1 = 1.f;
+            if (g.b.mode == B_NORM) {
+              const float2 gg = __ldg(reinterpret_cast<const float2*>(g.b.gamma + k0) + lane);
+              gm0 = gg.x;
+              gm1 = gg.y;
+            }
+            const int r0 = rb * npad;
+            const int rows = min(npad, g.N - r0);
             uint8_t* bs = smem + stage * L.stage_bytes + L.b_off;
-            const int items = npad * 8;
-            for (int base = 0; base < items; base += 32 * 4) {
-              float vals[4][8];
-              int rr[4], cc[4];
-              bool valid[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int item = base + u * 32 + lane;
-                rr[u] = item >> 3;
-                cc[u] = item & 7;
-                const int n = rb * npad + rr[u];
-                valid[u] = item < items && n < g.N;
-                if (valid[u]) load_b8(g.b, n, kb * BK + cc[u] * 8, rstd, vals[u]);
+            for (int r = 0; r < rows; ++r) {
+              float x0, x1;
+              if (bf) {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(bs + 256 * r + 4 * lane);
+                x0 = __uint_as_float(w << 16);
+                x1 = __uint_as_float(w & 0xFFFF0000u);
+              } else {
+                const float2 f = *reinterpret_cast<const float2*>(bs + 256 * r + 8 * lane);
+                x0 = f.x;
+                x1 = f.y;
               }
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                if (base + u * 32 + lane >= items) continue;
-                uint32_t hw[4] = {0, 0, 0, 0}, lw4[4] = {0, 0, 0, 0};
-                if (valid[u]) {
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    uint16_t h0, l0, h1, l1;
-                    split_hilo(vals[u][2 * e], h0, l0);
-                    split_hilo(vals[u][2 * e + 1], h1, l1);
-                    hw[e] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
-                    lw4[e] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
-                  }
-                }
-                *reinterpret_cast<uint4*>(bs + sw128_offset(rr[u], cc[u])) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(bs + sw128_offset(npad + rr[u], cc[u])) =
-                    make_uint4(lw4[0], lw4[1], lw4[2], lw4[3]);
+              if (g.b.mode == B_NORM) {
+                const float rs = rstd[r0 + r];
+                x0 = x0 * rs * gm0;
+                x1 = x1 * rs * gm1;
               }
+              uint16_t h0, l0, h1, l1;
+              split_hilo(x0, h0, l0);
+              split_hilo(x1, h1, l1);
+              __syncwarp();   // every lane has read row r before it is overwritten
+              *reinterpret_cast<uint32_t*>(bs + sw128_offset(2 * r, chunk) + cbyte) =
+                  static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+              *reinterpret_cast<uint32_t*>(bs + sw128_offset(2 * r + 1, chunk) + cbyte) =
+                  static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -529,13 +695,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
       }
       i += kb1 - kb0;
     }
-  } else {
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------ epilogue (warps 2-5)
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
     const int tl = q * 32 + lane;           // feature row of the tile = TMEM lane
     EpiSmem es = epi_views(smem + L.epi_off, smem + L.lm_off, g.N, g.e.topk);
+    es.rstd = reinterpret_cast<float*>(smem + L.erstd_off);
     pdl_wait();
     if (g.e.kind == EPI_LMHEAD) lmhead_init(g, es, tl);
+    if (g.e.nss) epi_rstd(g.e, g.N, es.rstd, tl);
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int rows_total = nrb * npad;
     long long uc = 0;
@@ -555,14 +723,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
         for (int c0 = 0; c0 < npad; c0 += 16) {
           const int n0 = rb * npad + c0;
           if (n0 >= g.N) break;
-          const uint32_t col = static_cast<uint32_t>((ab * nrb + rb) * np2 + c0);
-          float hi[16], lo[16], v[16];
+          const uint32_t col = static_cast<uint32_t>((ab * nrb + rb) * np2 + 2 * c0);
+          float c[32], v[16];
           __syncwarp();
-          tmem_ld16(tmem + lane_base + col, hi);
-          tmem_ld16(tmem + lane_base + col + npad, lo);
+          tmem_ld16(tmem + lane_base + col, c);
+          tmem_ld16(tmem + lane_base + col + 16, c + 16);
           tmem_wait_ld();
 #pragma unroll
-          for (int r = 0; r < 16; ++r) v[r] = hi[r] + lo[r];
+          for (int r = 0; r < 16; ++r) v[r] = c[2 * r] + c[2 * r + 1];
           if (complete) {
             epilogue_chunk(g, es, mt, n0, v, tl);
           } else {
@@ -710,14 +878,26 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K) {
+bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_act_map(CUtensorMap* tm, const void* hl, int rows, int K, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(hl), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -732,7 +912,6 @@ int num_sms() {
   return g_num_sms;
 }
 
-constexpr int TC_NLW = 4;
 constexpr int TC_MAX_SMEM = 232448;
 static size_t g_tc_smem_cap = 0, g_simt_smem_cap = 0;
 
@@ -777,20 +956,24 @@ bool plan_gemm(GemmPlan& p, int N) {
   p.grid = static_cast<int>(std::min<long long>(num_sms(), total));
   p.grid_y = 1;
   const int topk = std::max(1, g.e.topk);
-  const uint32_t fixed = tc_smem_bytes(g.npad, 0, g.e.kind == EPI_LMHEAD ? N : 0, topk);
-  const uint32_t stage = A_STAGE_BYTES + g.npad * 256;
+  const int lm_rows = g.e.kind == EPI_LMHEAD ? N : 0;
   const uint32_t cap = static_cast<uint32_t>(g_tc_smem_cap ? g_tc_smem_cap : TC_MAX_SMEM);
-  if (fixed + 2 * stage > cap) return false;
-  int stages = static_cast<int>((cap - fixed) / stage);
-  stages = std::min(stages, 12);
+  int stages = 12;
+  while (stages >= 2 && tc_smem_bytes(g.npad, stages, lm_rows, topk) > cap) --stages;
   if (stages < 2) return false;
   g.stages = stages;
-  p.smem = tc_smem_bytes(g.npad, stages, g.e.kind == EPI_LMHEAD ? N : 0, topk);
+  p.smem = tc_smem_bytes(g.npad, stages, lm_rows, topk);
+  if (g.b_tma) {
+    // the operand copy holds 2 N rows (hi, lo); rows past them read as zero
+    if (!p.b_hl || !make_act_map(&p.tmB, p.b_hl, 2 * N, g.K, 2 * g.npad)) return false;
+  } else {
+    p.tmB = p.tm0;
+  }
   return true;
 }
 
 cudaError_t gemm_setup_attributes() {
-  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_NLW>), &g_tc_smem_cap);
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel), &g_tc_smem_cap);
   if (e != cudaSuccess) return e;
   return allow_max_smem(reinterpret_cast<const void*>(gemm_simt_kernel), &g_simt_smem_cap);
 }
@@ -806,8 +989,8 @@ cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t st, bool pdl) {
   cfg.dynamicSmemBytes = p.smem;
   if (p.tc) {
     cfg.gridDim = dim3(p.grid, 1, 1);
-    cfg.blockDim = dim3((6 + TC_NLW) * 32, 1, 1);
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_NLW>, p.tm0, p.tm1, p.args);
+    cfg.blockDim = dim3(TC_THREADS, 1, 1);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, p.tm0, p.tm1, p.tmB, p.args);
   }
   cfg.gridDim = dim3(p.grid, p.grid_y, 1);
   cfg.blockDim = dim3(256, 1, 1);

@@ -12,6 +12,8 @@ void set_last_error(const char* msg);
 struct GemmPlan {
   bool tc = false;               // tcgen05 mainloop (bf16 weights) or SIMT (f32 weights)
   CUtensorMap tm0, tm1;          // weight maps (tc): rows [0, m_split) and [m_split, M)
+  CUtensorMap tmB;               // activation operand copy (tc, args.b_tma)
+  const uint16_t* b_hl = nullptr;  // its base: bf16 [2 N][K], rows 2r / 2r+1 = hi / lo of row r
   const float* w0f = nullptr;    // f32 weights (simt)
   const float* w1f = nullptr;
   GemmArgs args{};
@@ -23,7 +25,7 @@ struct GemmPlan {
 cudaError_t allow_max_smem(const void* func, size_t* granted = nullptr);
 size_t max_dyn_smem(const void* func);
 
-bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K);
+bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K, int box_rows = BM);
 int num_sms();
 bool plan_gemm(GemmPlan& p, int N);
 cudaError_t gemm_setup_attributes();
@@ -48,6 +50,7 @@ struct AttnArgs {
   float* part;              // [B][Hkv][max_splits][qv][hd + 2]
   int* counters;            // [B][Hkv]
   float* out;               // [N][Hq*hd]
+  uint16_t* out_hl;         // [2N][Hq*hd] bf16 hi / lo rows of out (operand of the O projection)
 };
 size_t attn_smem_bytes(int qv, int hd);
 cudaError_t attn_setup_attributes();
@@ -63,6 +66,7 @@ struct TreeArgs {
   int tree_rows;            // R: rows per request over all depths
   int max_nodes;            // generated + 1 (root)
   int max_prefix;
+  int vocab;
   // inputs
   const int* root_tok;
   const int* cu_seqlens;

@@ -26,7 +26,11 @@ __global__ void tree_init_kernel(const TreeArgs t, const RowMeta r0) {
     nb = nb < 0 ? 0 : t.max_prefix;
   }
   t.n_eff[b] = nb;
-  const int tok = __ldg(t.root_tok + b);
+  int tok = __ldg(t.root_tok + b);
+  if (tok < 0 || tok >= t.vocab) {       // never let a bad id reach an embedding-row address
+    atomicOr(t.err, DEVERR_TOKEN);
+    tok = 0;
+  }
   const size_t nbase = static_cast<size_t>(b) * t.max_nodes;
   t.node_tok[nbase] = tok;
   t.node_parent[nbase] = -1;

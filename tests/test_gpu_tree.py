@@ -82,6 +82,18 @@ def test_prefix_longer_than_max_prefix_is_reported(lib):
     d.check()   # the word was cleared
 
 
+def test_out_of_range_root_token_is_reported(lib):
+    cfg = configs.get("small_dyn")
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    I["root_tok"] = I["root_tok"].copy()
+    I["root_tok"][1] = cfg.vocab + 5
+    d = eb.EagleDraft(cfg, eb.device_weights(W))
+    d.tree(eb.device_inputs(I))
+    with pytest.raises(eb.EagleError) as ei:
+        d.check()
+    assert ei.value.status == eb.EAGLE_ERR_DEVICE and "0x4" in str(ei.value)
+
+
 def test_invalid_batch_rejected(lib):
     cfg = configs.get("small_dyn")
     W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
