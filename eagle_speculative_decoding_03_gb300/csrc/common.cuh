@@ -251,10 +251,10 @@ struct EpiArgs {
   int max_pos;
   int Hq, Hkv, hd, tree_rows;
   // EPI_LMHEAD: per vocabulary tile and row: max and sum of exp; per CTA and row: top-k
-  float* lm_max;           // [tiles][N]
-  float* lm_sum;           // [tiles][N]
-  float* lm_val;           // [grid][N][k]
-  int* lm_id;              // [grid][N][k]
+  float* lm_max;           // [N][tiles]
+  float* lm_sum;           // [N][tiles]
+  float* lm_val;           // [N][grid][k]  (each row's CTA lists contiguous)
+  int* lm_id;              // [N][grid][k]
   int topk;
   // operand copy for the next GEMM (EPI_STORE, EPI_SWIGLU):
   // hl[2 row][m] = hi, hl[2 row + 1][m] = lo of value * hl_gamma[m] (hl_gamma may be null)

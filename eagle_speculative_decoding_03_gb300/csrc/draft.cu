@@ -49,7 +49,7 @@ struct eagle_draft {
   eagle_draft_config_t cfg;
   eagle_draft_weights_t w;
   bool tc = false;
-  bool use_graph = true, use_pdl = true;
+  bool use_graph = true, use_pdl = true, gemm_occ2 = true;
   int D = 0, R = 0, gen = 0, S = 0, n_max = 0, k_max = 0, f_max = 0, max_nodes = 0;
   int rows[EAGLE_MAX_DEPTH], kids[EAGLE_MAX_DEPTH];
   int row_base[EAGLE_MAX_DEPTH + 1], node_base[EAGLE_MAX_DEPTH + 1];
@@ -67,7 +67,8 @@ struct eagle_draft {
   int *lm_id = nullptr, *counters = nullptr, *att_counters = nullptr;
   int *node_tok = nullptr, *node_parent = nullptr, *node_depth = nullptr, *node_row = nullptr;
   float* node_logv = nullptr;
-  int *n_eff = nullptr, *frontier = nullptr;
+  int *n_eff = nullptr, *frontier = nullptr, *exp_counters = nullptr, *exp_tok = nullptr;
+  float* exp_v = nullptr;
   unsigned long long* slot_mask = nullptr;
   RowMeta meta[2];
   unsigned* err = nullptr;
@@ -99,13 +100,14 @@ struct ProfScope {
       if (cudaEventCreate(&e) != cudaSuccess) return;
       h->ev_pool.push_back(e);
     }
-    cudaEventRecord(h->ev_pool[h->ev_used], st);
+    // External: inside a stream capture this becomes an event-record node of the graph
+    cudaEventRecordWithFlags(h->ev_pool[h->ev_used], st, cudaEventRecordExternal);
     stop = h->ev_pool[h->ev_used + 1];
     h->ev_used += 2;
     h->ev_kind.push_back(kind);
   }
   ~ProfScope() {
-    if (stop) cudaEventRecord(stop, st);
+    if (stop) cudaEventRecordWithFlags(stop, st, cudaEventRecordExternal);
   }
 };
 
@@ -182,7 +184,7 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   h->rope_cos = cv.take<float>(static_cast<size_t>(h->max_pos) * c.head_dim / 2);
   h->rope_sin = cv.take<float>(static_cast<size_t>(h->max_pos) * c.head_dim / 2);
   h->part = cv.take<float>(static_cast<size_t>(num_sms()) * 2 * 256 * BM);
-  h->att_part = cv.take<float>(static_cast<size_t>(B) * c.n_kv_heads * h->max_splits * h->qv_max * (c.head_dim + 2));
+  h->att_part = cv.take<float>(static_cast<size_t>(B) * c.n_kv_heads * h->max_splits * h->qv_max * (c.head_dim + 4));
   const size_t lmn = static_cast<size_t>(h->lm_G) * n;
   const size_t lmt = static_cast<size_t>(ceil_div(c.vocab, BM)) * n;
   h->lm_max = cv.take<float>(lmt);
@@ -198,6 +200,9 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   h->node_row = cv.take<int>(nn);
   h->node_logv = cv.take<float>(nn);
   h->n_eff = cv.take<int>(B);
+  h->exp_counters = cv.take<int>(B);
+  h->exp_v = cv.take<float>(static_cast<size_t>(B) * 256);
+  h->exp_tok = cv.take<int>(static_cast<size_t>(B) * 256);
   h->frontier = cv.take<int>(static_cast<size_t>(B) * 64);
   h->slot_mask = cv.take<unsigned long long>(static_cast<size_t>(B) * h->R);
   for (int i = 0; i < 2; ++i) {
@@ -209,6 +214,7 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
     m.feat = cv.take<int>(n);
     m.node = cv.take<int>(n);
     m.mask = cv.take<unsigned long long>(n);
+    m.v = cv.take<float>(n);
   }
   h->err = cv.take<unsigned>(64);
   *total = cv.off + 256;
@@ -228,6 +234,7 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
   h->tc = c.dtype == EAGLE_DTYPE_BF16;
   h->use_graph = !(c.flags & EAGLE_FLAG_NO_GRAPH);
   h->use_pdl = !(c.flags & EAGLE_FLAG_NO_PDL);
+  h->gemm_occ2 = !(c.flags & EAGLE_FLAG_GEMM_ONE_CTA);
   h->D = c.depth;
   // tree geometry
   int rb = 0, nb = 1, kmax = 0, fmax = 0, nmax_rows = 0;
@@ -267,12 +274,17 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
   h->max_pos = c.max_prefix + c.depth + 1;
   h->max_splits = ceil_div(c.max_prefix, ATT_CHUNK) + 1;
   h->qv_max = nmax_rows * (c.n_heads / c.n_kv_heads);
+  if (static_cast<size_t>((h->qv_max + 3) & ~3) * c.head_dim > attn_merge_capacity(h->qv_max, c.head_dim)) {
+    delete h;
+    return fail(EAGLE_ERR_UNSUPPORTED, "too many query vectors per KV group (%d)", h->qv_max);
+  }
   if (attn_smem_bytes(h->qv_max, c.head_dim) > 227 * 1024 - 64) {
     delete h;
     return fail(EAGLE_ERR_UNSUPPORTED, "too many query vectors per KV group (%d)", h->qv_max);
   }
   if (h->tc && h->n_max > 256) { delete h; return fail(EAGLE_ERR_UNSUPPORTED, "more than 256 rows per depth"); }
   h->lm_G = h->tc ? num_sms() : ceil_div(c.vocab, BM);
+  if (h->lm_G > 256) { delete h; return fail(EAGLE_ERR_UNSUPPORTED, "more than 256 LM-head partial lists (SMs or vocabulary tiles)"); }
 
   cudaError_t e = cudaSuccess;
   if ((e = gemm_setup_attributes()) != cudaSuccess || (e = attn_setup_attributes()) != cudaSuccess ||
@@ -409,10 +421,11 @@ static EpiArgs epi_store(float* out, int ldo, const float* resid, int ldr, float
 }
 
 // Operand tile loaded by TMA from a bf16 hi/lo copy written by the producing kernel.
-static void tma_operand(GemmPlan& p, const uint16_t* hl) {
+static void tma_operand(GemmPlan& p, const uint16_t* hl, bool shared_sm = false) {
   p.args.b.mode = B_TMA;
   p.args.b_tma = 1;
   p.b_hl = hl;
+  p.occ = shared_sm ? 2 : 1;
 }
 
 // The producing epilogue also writes the next GEMM's operand copy (value * gamma).
@@ -505,6 +518,9 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
   t.n_eff = h->n_eff;
   t.frontier = h->frontier;
   t.slot_mask = h->slot_mask;
+  t.exp_counters = h->exp_counters;
+  t.exp_v = h->exp_v;
+  t.exp_tok = h->exp_tok;
   t.err = h->err;
   {
     ProfScope ps(h, EAGLE_K_INIT, st);
@@ -584,7 +600,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       e.hd = c.head_dim;
       e.tree_rows = h->R;
       if (h->tc) {
-        tma_operand(p, h->xa_hl);
+        tma_operand(p, h->xa_hl, h->gemm_occ2);
         factored_norm(e, h->ss_h, ceil_div(d, BM), static_cast<int>(nmax), d, c.rms_eps);
       }
       if ((r = run_gemm(h, p, N, st, EAGLE_K_QKV)) != EAGLE_OK) return r;
@@ -625,7 +641,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       p.args.b.ldx = hq;
       p.args.e = epi_store(h->y, d, h->h, d, h->ss_y, static_cast<int>(nmax));
       if (h->tc) {
-        tma_operand(p, h->o_hl);
+        tma_operand(p, h->o_hl, h->gemm_occ2);
         write_operand(p.args.e, h->xm_hl, d, h->w.mlp_norm);
       }
       if ((r = run_gemm(h, p, N, st, EAGLE_K_OPROJ)) != EAGLE_OK) return r;
@@ -648,7 +664,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
         p.args.a_pair = 1;
         p.args.e = epi_store(nullptr, ff, nullptr, 0, nullptr, 0);
         p.args.e.kind = EPI_SWIGLU;
-        tma_operand(p, h->xm_hl);
+        tma_operand(p, h->xm_hl, h->gemm_occ2);
         factored_norm(p.args.e, h->ss_y, ceil_div(d, BM), static_cast<int>(nmax), d, c.rms_eps);
         write_operand(p.args.e, h->s_hl, ff, nullptr);
       } else {
@@ -661,7 +677,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       GemmPlan p = base_plan(h, h->tm_down, nullptr, h->w.w_down, nullptr, d, ff, d);
       BSrc& b = p.args.b;
       if (h->tc) {
-        tma_operand(p, h->s_hl);
+        tma_operand(p, h->s_hl, h->gemm_occ2);
       } else {
         b.mode = B_SWIGLU;
         b.x = h->gu;
@@ -728,7 +744,28 @@ extern "C" eagle_status_t eagle_draft_tree(eagle_draft_t* h, const eagle_draft_i
   if (!out->tokens || !out->parents || !out->positions || !out->logv || !out->mask)
     return fail(EAGLE_ERR_INVALID_ARG, "null output pointer");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (trc || !h->use_graph || h->profiling) return enqueue_tree(h, in, out, trc, st);
+  if (h->profiling && !trc) {
+    // one-off graph holding the kernels and their event-record nodes: the GPU runs the
+    // kernels back to back, so the events time the kernels and not the host in between
+    CU(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+    eagle_status_t r = enqueue_tree(h, in, out, nullptr, h->cap_stream);
+    cudaGraph_t g = nullptr;
+    cudaError_t ec = cudaStreamEndCapture(h->cap_stream, &g);
+    if (r != EAGLE_OK) {
+      if (g) cudaGraphDestroy(g);
+      return r;
+    }
+    if (ec != cudaSuccess) return fail(EAGLE_ERR_CUDA, "stream capture: %s", cudaGetErrorString(ec));
+    cudaGraphExec_t ge = nullptr;
+    ec = cudaGraphInstantiate(&ge, g, 0);
+    cudaGraphDestroy(g);
+    if (ec != cudaSuccess) return fail(EAGLE_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(ec));
+    ec = cudaGraphLaunch(ge, st);
+    cudaGraphExecDestroy(ge);
+    if (ec != cudaSuccess) return fail(EAGLE_ERR_CUDA, "graph launch: %s", cudaGetErrorString(ec));
+    return EAGLE_OK;
+  }
+  if (trc || !h->use_graph) return enqueue_tree(h, in, out, trc, st);
   std::vector<const void*> key = {reinterpret_cast<const void*>(static_cast<intptr_t>(in->B)), in->root_feat,
                                   in->root_tok, in->k_cache, in->v_cache, in->cu_seqlens, out->tokens,
                                   out->parents, out->positions, out->logv, out->mask};

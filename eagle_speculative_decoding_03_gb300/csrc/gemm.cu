@@ -166,7 +166,8 @@ EAGLE_DEV bool epi_all(bool p) {
 }
 
 // Merge a warp's 128 new (value, id) candidates (4 per lane) into a row's sorted top-k
-// list (length cnt <= k) held in shared memory; k rounds of warp arg-max.
+// list (length cnt <= k) held in shared memory: k rounds of warp arg-max.  Used to fill
+// a list that is not full yet.
 EAGLE_DEV void warp_topk_merge(float* lv, int* li, int* cnt_p, int k, const float* nv, const int* nid,
                                int lane) {
   const int cnt = *cnt_p;
@@ -204,6 +205,46 @@ EAGLE_DEV void warp_topk_merge(float* lv, int* li, int* cnt_p, int k, const floa
   __syncwarp();
   if (lane < rounds) { lv[lane] = outv; li[lane] = outi; }
   if (lane == 0) *cnt_p = rounds;
+  __syncwarp();
+}
+
+// Insert the warp's candidates that beat the current k-th entry of a full list (best
+// first, in shared memory).  The list lives one entry per lane while inserting; each
+// candidate costs a ballot, a popcount and a shuffle-shift.  Only a few values per tile
+// qualify once the list holds the best of earlier tiles.
+EAGLE_DEV void warp_topk_insert(float* lv, int* li, int k, const float* nv, int* nid, int lane) {
+  float myv = lane < k ? lv[lane] : -INFINITY;
+  int myi = lane < k ? li[lane] : INT_MAX;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    for (;;) {
+      const float kv = __shfl_sync(0xffffffffu, myv, k - 1);
+      const int ki = __shfl_sync(0xffffffffu, myi, k - 1);
+      const unsigned m = __ballot_sync(0xffffffffu, nid[j] != INT_MAX && beats(nv[j], nid[j], kv, ki));
+      if (!m) break;
+      const int src = __ffs(m) - 1;
+      const float cv = __shfl_sync(0xffffffffu, nv[j], src);
+      const int ci = __shfl_sync(0xffffffffu, nid[j], src);
+      // entries better than the candidate stay; the rest move down one place
+      const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && beats(myv, myi, cv, ci)));
+      const float upv = __shfl_up_sync(0xffffffffu, myv, 1);
+      const int upi = __shfl_up_sync(0xffffffffu, myi, 1);
+      if (lane > pos) {
+        myv = upv;
+        myi = upi;
+      }
+      if (lane == pos) {
+        myv = cv;
+        myi = ci;
+      }
+      if (lane == src) nid[j] = INT_MAX;   // consumed
+    }
+  }
+  __syncwarp();
+  if (lane < k) {
+    lv[lane] = myv;
+    li[lane] = myi;
+  }
   __syncwarp();
 }
 
@@ -324,8 +365,8 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
       for (int j = 0; j < 4; ++j) s += id[j] != INT_MAX ? expf(val[j] - tmax) : 0.f;
       s = warp_sum(s);
       if (lane == 0) {
-        e.lm_max[static_cast<size_t>(mt) * g.N + n] = tmax;
-        e.lm_sum[static_cast<size_t>(mt) * g.N + n] = s;
+        e.lm_max[static_cast<size_t>(n) * g.MT + mt] = tmax;
+        e.lm_sum[static_cast<size_t>(n) * g.MT + mt] = s;
       }
       // top-k
       const int cnt = es.st_cnt[n];
@@ -337,7 +378,10 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
 #pragma unroll
       for (int j = 0; j < 4; ++j) cand |= id[j] != INT_MAX && beats(val[j], id[j], tv, ti);
       __syncwarp();
-      if (__any_sync(0xffffffffu, cand)) warp_topk_merge(lv, li, es.st_cnt + n, k, val, id, lane);
+      if (__any_sync(0xffffffffu, cand)) {
+        if (cnt < k) warp_topk_merge(lv, li, es.st_cnt + n, k, val, id, lane);
+        else warp_topk_insert(lv, li, k, val, id, lane);
+      }
       __syncwarp();
     }
     named_bar(1, 128);
@@ -354,7 +398,7 @@ EAGLE_DEV void lmhead_flush(const GemmArgs& g, EpiSmem& es, int cta, int tl) {
   const int k = e.topk;
   named_bar(1, 128);
   for (int n = tl; n < g.N; n += 128) {
-    const size_t o = static_cast<size_t>(cta) * g.N + n;
+    const size_t o = static_cast<size_t>(n) * gridDim.x + cta;   // lists of one row are contiguous
     const int cnt = es.st_cnt[n];
     for (int j = 0; j < k; ++j) {
       e.lm_val[o * k + j] = j < cnt ? es.lv[static_cast<size_t>(n) * k + j] : -INFINITY;
@@ -409,13 +453,18 @@ EAGLE_DEV void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint
 
 constexpr int TC_NCW = 4;                       // converter warps
 constexpr int TC_THREADS = (7 + TC_NCW) * 32;   // A producer, MMA, 4 epilogue, B producer, converters
+constexpr int TC_THREADS_TMA = 7 * 32;          // operand tile by TMA: no converter warps
+constexpr uint32_t TC_SMEM_OCC2 = 113 * 1024;   // two CTAs per SM
 
 // Warp roles: 0 = weight TMA producer, 1 = MMA issuer, 2-5 = epilogue (TMEM lanes by
 // warp % 4), 6 = activation producer (bulk copies of the source rows into the B tile),
 // 7.. = converters (in place: fp32 / bf16 row -> bf16 hi row + bf16 lo row, swizzled).
 // B tile rows are interleaved: row 2r = hi of GEMM row r, row 2r+1 = its lo part, so the
 // accumulator column 2r + 1 holds the low-order correction of column 2r.
-__global__ void __launch_bounds__(TC_THREADS, 1)
+// NT = TC_THREADS (converter warps present, one CTA per SM) or 7 warps (operand by TMA only;
+// MINB = 2 lets the next kernel's CTA share the SM and start its weight stream early).
+template <int NT, int MINB>
+__global__ void __launch_bounds__(NT, MINB)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
@@ -759,14 +808,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
             for (int c0 = 0; c0 < npad; c0 += 16) {
               const int n0 = rb * npad + c0;
               if (n0 >= g.N) break;
+              // partials summed in CTA order; loads of up to 4 segments issued together
               float v[16];
 #pragma unroll
               for (int r = 0; r < 16; ++r) v[r] = 0.f;
-              for (int c = cf; c <= cl; ++c) {
-                const int s = (sc.begin(c) / KB == mt) ? 0 : 1;
-                const float* p = g.part + (static_cast<size_t>(c) * 2 + s) * rows_total * BM;
+              for (int c0 = cf; c0 <= cl; c0 += 4) {
+                float pv[4][16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) v[r] += __ldcg(p + static_cast<size_t>(n0 + r) * BM + tl);
+                for (int u = 0; u < 4; ++u) {
+                  const int c = c0 + u;
+                  if (c <= cl) {
+                    const int sl = (sc.begin(c) / KB == mt) ? 0 : 1;
+                    const float* p = g.part + (static_cast<size_t>(c) * 2 + sl) * rows_total * BM;
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) pv[u][r] = __ldcg(p + static_cast<size_t>(n0 + r) * BM + tl);
+                  }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (c0 + u <= cl) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) v[r] += pv[u][r];
+                  }
               }
               epilogue_chunk(g, es, mt, n0, v, tl);
             }
@@ -849,7 +912,7 @@ gemm_simt_kernel(const float* __restrict__ W0, const float* __restrict__ W1, con
       for (int r = tid; r < SIMT_ROWS; r += 128) {
         const int n = n0 + r;
         if (n >= g.N) continue;
-        const size_t o = static_cast<size_t>(mt) * g.N + n;
+        const size_t o = static_cast<size_t>(n) * gridDim.x + mt;
         const int cnt = es.st_cnt[n];
         for (int j = 0; j < k; ++j) {
           g.e.lm_val[o * k + j] = j < cnt ? es.lv[static_cast<size_t>(n) * k + j] : -INFINITY;
@@ -957,7 +1020,9 @@ bool plan_gemm(GemmPlan& p, int N) {
   p.grid_y = 1;
   const int topk = std::max(1, g.e.topk);
   const int lm_rows = g.e.kind == EPI_LMHEAD ? N : 0;
-  const uint32_t cap = static_cast<uint32_t>(g_tc_smem_cap ? g_tc_smem_cap : TC_MAX_SMEM);
+  if (p.occ == 2 && (!g.b_tma || g.tmem_cols > 256)) p.occ = 1;
+  uint32_t cap = static_cast<uint32_t>(g_tc_smem_cap ? g_tc_smem_cap : TC_MAX_SMEM);
+  if (p.occ == 2) cap = std::min(cap, TC_SMEM_OCC2);
   int stages = 12;
   while (stages >= 2 && tc_smem_bytes(g.npad, stages, lm_rows, topk) > cap) --stages;
   if (stages < 2) return false;
@@ -973,7 +1038,9 @@ bool plan_gemm(GemmPlan& p, int N) {
 }
 
 cudaError_t gemm_setup_attributes() {
-  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel), &g_tc_smem_cap);
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS, 1>), &g_tc_smem_cap);
+  if (e != cudaSuccess) return e;
+  e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS_TMA, 2>));
   if (e != cudaSuccess) return e;
   return allow_max_smem(reinterpret_cast<const void*>(gemm_simt_kernel), &g_simt_smem_cap);
 }
@@ -989,8 +1056,12 @@ cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t st, bool pdl) {
   cfg.dynamicSmemBytes = p.smem;
   if (p.tc) {
     cfg.gridDim = dim3(p.grid, 1, 1);
+    if (p.occ == 2) {
+      cfg.blockDim = dim3(TC_THREADS_TMA, 1, 1);
+      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 2>, p.tm0, p.tm1, p.tmB, p.args);
+    }
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, p.tm0, p.tm1, p.tmB, p.args);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS, 1>, p.tm0, p.tm1, p.tmB, p.args);
   }
   cfg.gridDim = dim3(p.grid, p.grid_y, 1);
   cfg.blockDim = dim3(256, 1, 1);

@@ -19,6 +19,7 @@ struct GemmPlan {
   GemmArgs args{};
   int grid = 0, grid_y = 1;
   size_t smem = 0;
+  int occ = 1;                   // tc with TMA operand: 2 = two CTAs per SM (smaller ring)
 };
 
 // Allow `func` the device's opt-in maximum of dynamic shared memory (minus its static use).
@@ -53,6 +54,7 @@ struct AttnArgs {
   uint16_t* out_hl;         // [2N][Hq*hd] bf16 hi / lo rows of out (operand of the O projection)
 };
 size_t attn_smem_bytes(int qv, int hd);
+size_t attn_merge_capacity(int qv, int hd);
 cudaError_t attn_setup_attributes();
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl);
 
@@ -80,6 +82,9 @@ struct TreeArgs {
   int* n_eff;               // [B]
   int* frontier;            // [B][64] node ids of the current frontier
   unsigned long long* slot_mask;  // [B][tree_rows] ancestor-or-self bits of every row
+  int* exp_counters;        // [B] rows of the depth finished (zero between depths)
+  float* exp_v;             // [B][256] values of the depth's children
+  int* exp_tok;             // [B][256] their tokens
   unsigned* err;
 };
 
@@ -92,13 +97,14 @@ struct RowMeta {
   int* feat;                // feature row (index into the previous feature buffer)
   int* node;                // tree node the row expands
   unsigned long long* mask; // ancestor-or-self bits
+  float* v;                 // path value V of the node
 };
 
 struct LmPartials {
-  float* max;               // [T][N] per vocabulary tile
-  float* sum;               // [T][N]
-  float* val;               // [G][N][k] per CTA
-  int* id;                  // [G][N][k]
+  float* max;               // [N][T] per vocabulary tile
+  float* sum;               // [N][T]
+  float* val;               // [N][G][k] per CTA
+  int* id;                  // [N][G][k]
   int G;                    // CTAs that wrote top-k partials
   int T;                    // vocabulary tiles
 };

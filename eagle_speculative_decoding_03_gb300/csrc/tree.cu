@@ -45,152 +45,301 @@ __global__ void tree_init_kernel(const TreeArgs t, const RowMeta r0) {
   r0.feat[b] = b;
   r0.node[b] = 0;
   r0.mask[b] = 1ull;
+  r0.v[b] = 0.f;
 }
 
 // ---------------------------------------------- merge of LM-head partials
-// One warp merges the G per-CTA partial states of GEMM row n: log-sum-exp and the
-// top-`kout` (value, id).  Lane r < kout returns the r-th best (descending).
-// `cand` is the warp's shared-memory staging area (G * kp entries).
-EAGLE_DEV void merge_lm_row(const LmPartials& lm, int N, int kp, int n, int kout, float2* cand,
-                            float& lse, float& my_val, int& my_id, int lane) {
-  const int G = lm.G, T = lm.T;
-  float M = -INFINITY;
-  for (int t = lane; t < T; t += 32) M = fmaxf(M, __ldcg(lm.max + static_cast<size_t>(t) * N + n));
-  M = warp_max(M);
-  float s = 0.f;
-  for (int t = lane; t < T; t += 32) {
-    const float mt = __ldcg(lm.max + static_cast<size_t>(t) * N + n);
-    if (mt != -INFINITY) s += __ldcg(lm.sum + static_cast<size_t>(t) * N + n) * expf(mt - M);
-  }
-  s = warp_sum(s);
-  lse = M + logf(s);
+constexpr int MERGE_MAX_G = 256;   // CTAs (lists) one warp can merge: 8 lists per lane
 
-  const int tot = G * kp;
-  for (int c = lane; c < tot; c += 32) {
-    const int g = c / kp, j = c - g * kp;
-    const size_t o = (static_cast<size_t>(g) * N + n) * kp + j;
-    cand[c] = make_float2(__ldcg(lm.val + o), __int_as_float(__ldcg(lm.id + o)));
-  }
-  __syncwarp();
-  float lastv = INFINITY;
-  int lasti = -1;
+// The top-`kout` of G sorted (best first) lists of kp entries staged in shared memory,
+// as a tournament: kout rounds of warp arg-max over the list heads, advancing the
+// winner's list.  Lane r < kout returns the r-th best.
+EAGLE_DEV void tournament(const float2* cand, int G, int kp, int kout, float& my_val, int& my_id, int lane) {
+  int ptr[MERGE_MAX_G / 32];
+#pragma unroll
+  for (int i = 0; i < MERGE_MAX_G / 32; ++i) ptr[i] = 0;
   my_val = -INFINITY;
   my_id = -1;
   for (int r = 0; r < kout; ++r) {
     float bv = -INFINITY;
-    int bi = INT_MAX;
-    for (int c = lane; c < tot; c += 32) {
-      const float2 e = cand[c];
-      const int id = __float_as_int(e.y);
-      if (id < 0) continue;
-      if ((r == 0 || beats(lastv, lasti, e.x, id)) && beats(e.x, id, bv, bi)) { bv = e.x; bi = id; }
+    int bi = INT_MAX, bl = -1;
+#pragma unroll
+    for (int i = 0; i < MERGE_MAX_G / 32; ++i) {
+      const int c = lane + 32 * i;
+      if (c < G && ptr[i] < kp) {
+        const float2 e = cand[c * kp + ptr[i]];
+        const int id = __float_as_int(e.y);
+        if (id >= 0 && beats(e.x, id, bv, bi)) {
+          bv = e.x;
+          bi = id;
+          bl = i;
+        }
+      }
     }
+    float wv = bv;
+    int wi = bi;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+      if (beats(ov, oi, wv, wi)) { wv = ov; wi = oi; }
     }
-    if (bi == INT_MAX) break;
-    if (lane == r) { my_val = bv; my_id = bi; }
-    lastv = bv;
-    lasti = bi;
+    if (wi == INT_MAX) break;
+    if (bi == wi) {   // token ids are unique: this lane holds the winning head
+#pragma unroll
+      for (int i = 0; i < MERGE_MAX_G / 32; ++i)
+        if (i == bl) ++ptr[i];
+    }
+    if (lane == r) {
+      my_val = wv;
+      my_id = wi;
+    }
   }
   __syncwarp();
 }
 
-// ------------------------------------------------------------ expansion
-constexpr int EXP_WARPS = 8;
+// One warp merges the partial states of GEMM row n: the log-sum-exp over the per-tile
+// (max, sum of exp) pairs, and the top-`kout` (value, id) of the G per-CTA top-kp lists
+// (each sorted best first).  The lists are staged in shared memory (`cand`, G * kp) and
+// merged as a tournament: kout rounds of warp arg-max over the list heads, advancing the
+// winner's list.  Lane r < kout returns the r-th best.
+EAGLE_DEV void merge_lm_row(const LmPartials& lm, int N, int kp, int n, int kout, float2* cand,
+                            float& lse, float& my_val, int& my_id, int lane) {
+  // log-sum-exp: loads issued in independent batches, combined online per lane in tile
+  // order, then a symmetric butterfly (every lane ends with the same value)
+  float m = -INFINITY, sm = 0.f;
+  for (int t0 = 0; t0 < lm.T; t0 += 32 * 8) {
+    float mb[8], sb[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = t0 + u * 32 + lane;
+      mb[u] = t < lm.T ? __ldcg(lm.max + static_cast<size_t>(n) * lm.T + t) : -INFINITY;
+      sb[u] = t < lm.T ? __ldcg(lm.sum + static_cast<size_t>(n) * lm.T + t) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (mb[u] == -INFINITY) continue;
+      if (mb[u] > m) {
+        sm = sm * expf(m - mb[u]) + sb[u];
+        m = mb[u];
+      } else {
+        sm += sb[u] * expf(mb[u] - m);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const float os = __shfl_xor_sync(0xffffffffu, sm, o);
+    const float M = fmaxf(m, om);
+    sm = (m == -INFINITY ? 0.f : sm * expf(m - M)) + (om == -INFINITY ? 0.f : os * expf(om - M));
+    m = M;
+  }
+  lse = m + logf(sm);
 
-__global__ void __launch_bounds__(EXP_WARPS * 32)
+  // stage the lists (loads issued in independent batches of 8 per lane)
+  const int G = lm.G, tot = G * kp;
+  for (int c0 = 0; c0 < tot; c0 += 32 * 8) {
+    float vb[8];
+    int ib[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + u * 32 + lane;
+      if (c < tot) {
+        const size_t o = static_cast<size_t>(n) * tot + c;
+        vb[u] = __ldcg(lm.val + o);
+        ib[u] = __ldcg(lm.id + o);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + u * 32 + lane;
+      if (c < tot) cand[c] = make_float2(vb[u], __int_as_float(ib[u]));
+    }
+  }
+  __syncwarp();
+  tournament(cand, G, kp, kout, my_val, my_id, lane);
+}
+
+// ------------------------------------------------------------ expansion
+// One CTA per row (frontier node) of the depth: log-sum-exp and top-k children of the
+// row, written to the node table; the last CTA of a request to finish (arrival counter)
+// selects the request's next frontier and writes the next depth's row metadata.
+constexpr int EXR_THREADS = 256;
+constexpr int EXR_WARPS = EXR_THREADS / 32;
+constexpr int EXR_CAND = 4096;          // candidates a row can keep (G <= 256 lists of <= 16)
+
+__global__ void __launch_bounds__(EXR_THREADS)
 expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta cur, const RowMeta nxt,
-              const ExpandTrace tr, const int kp) {
-  extern __shared__ float2 exp_smem[];
-  __shared__ int sel_rank[256];
-  __shared__ int sel_pos[256];
+              const ExpandTrace tr, const int kp, int* counters, float* scratch_v, int* scratch_tok) {
+  extern __shared__ float2 cand[];                 // [EXR_CAND]
+  __shared__ float red_m[EXR_WARPS], red_s[EXR_WARPS], red_t[EXR_WARPS];
+  __shared__ float2 sel[KMAX];
+  __shared__ int ncand;
+  __shared__ float s_lse;
+  __shared__ int s_last;
+  __shared__ float sv[256];
+  __shared__ int srank[256], spos[256];
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = t.rows[s - 1], kids = t.kids[s - 1];
-  const int N = t.B * R;
+  const int n = blockIdx.x, b = n / R, i = n - b * R;
   const size_t nb0 = static_cast<size_t>(b) * t.max_nodes;
   const int base = t.node_base[s - 1];
-  float2* cand = exp_smem + static_cast<size_t>(warp) * lm.G * kp;
+  const int G = lm.G;
 
-  // children of every row of this request
-  for (int i = warp; i < R; i += EXP_WARPS) {
-    const int n = b * R + i;
-    float lse, v;
-    int id;
-    merge_lm_row(lm, N, kp, n, kids, cand, lse, v, id, lane);
-    // order the kids winners by token id
-    int rank = 0;
-    for (int j = 0; j < kids; ++j) {
-      const int oj = __shfl_sync(0xffffffffu, id, j);
-      rank += (lane < kids && oj < id) ? 1 : 0;
+  // ---- log-sum-exp over the row's per-tile pairs, and the pruning threshold: the best
+  // kp-th entry over the complete CTA lists (the row's kp-th value cannot be lower)
+  float m = -INFINITY, sm = 0.f;
+  for (int t0 = tid; t0 < lm.T; t0 += EXR_THREADS) {
+    const float mt = __ldcg(lm.max + static_cast<size_t>(n) * lm.T + t0);
+    const float st = __ldcg(lm.sum + static_cast<size_t>(n) * lm.T + t0);
+    if (mt == -INFINITY) continue;
+    if (mt > m) {
+      sm = sm * expf(m - mt) + st;
+      m = mt;
+    } else {
+      sm += st * expf(mt - m);
     }
-    const int u = __ldcg(cur.node + n);
-    const float vu = __ldcg(t.node_logv + nb0 + u);
-    if (lane < kids) {
-      const int c = base + i * kids + rank;
-      const float lp = v - lse;
-      t.node_tok[nb0 + c] = id;
-      t.node_parent[nb0 + c] = u;
-      t.node_depth[nb0 + c] = s;
-      t.node_row[nb0 + c] = __ldcg(cur.slot + n);
-      t.node_logv[nb0 + c] = vu + lp;
-      if (tr.children) {
-        tr.children[static_cast<size_t>(n) * tr.k_max + rank] = id;
-        tr.child_logp[static_cast<size_t>(n) * tr.k_max + rank] = lp;
-      }
-    }
-    if (tr.lse && lane == 0) tr.lse[n] = lse;
   }
-  if (s >= t.depth) return;
-  __syncthreads();
-
-  // next frontier among the R * kids children of this depth
-  const int nc = R * kids;
-  const int F = t.rows[s];
-  if (t.tree_kind == 1) {  // static: every child, in generation order
-    for (int c = tid; c < nc; c += blockDim.x) sel_pos[c] = c;
-  } else {
-    for (int c = tid; c < nc; c += blockDim.x) {
-      const float vc = __ldcg(t.node_logv + nb0 + base + c);
-      int rk = 0;
-      for (int c2 = 0; c2 < nc; ++c2) {
-        const float v2 = __ldcg(t.node_logv + nb0 + base + c2);
-        rk += beats(v2, c2, vc, c) ? 1 : 0;
+  float thr = -INFINITY;
+  float lv[KMAX];
+  int li[KMAX];
+  const size_t lbase = static_cast<size_t>(n) * G * kp;
+  if (tid < G) {   // this thread's CTA list, whole
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < kp) {
+        lv[j] = __ldcg(lm.val + lbase + static_cast<size_t>(tid) * kp + j);
+        li[j] = __ldcg(lm.id + lbase + static_cast<size_t>(tid) * kp + j);
+        if (j == kp - 1 && li[j] >= 0) thr = lv[j];
       }
-      sel_rank[c] = rk;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const float os = __shfl_xor_sync(0xffffffffu, sm, o);
+    const float M = fmaxf(m, om);
+    sm = (m == -INFINITY ? 0.f : sm * expf(m - M)) + (om == -INFINITY ? 0.f : os * expf(om - M));
+    m = M;
+    thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, o));
+  }
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_s[warp] = sm;
+    red_t[warp] = thr;
+  }
+  if (tid == 0) ncand = 0;
+  __syncthreads();
+  if (tid == 0) {
+    float M = -INFINITY, S = 0.f, T = -INFINITY;
+    for (int w = 0; w < EXR_WARPS; ++w) {
+      const float mw = red_m[w], sw = red_s[w];
+      const float MM = fmaxf(M, mw);
+      S = (M == -INFINITY ? 0.f : S * expf(M - MM)) + (mw == -INFINITY ? 0.f : sw * expf(mw - MM));
+      M = MM;
+      T = fmaxf(T, red_t[w]);
+    }
+    s_lse = M + logf(S);
+    red_t[0] = T;
+  }
+  __syncthreads();
+  thr = red_t[0];
+  // ---- candidates: list entries >= thr (each list is sorted best first)
+  if (tid < G) {
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < kp && li[j] >= 0 && lv[j] >= thr) cand[atomicAdd(&ncand, 1)] = make_float2(lv[j], __int_as_float(li[j]));
+  }
+  __syncthreads();
+  const int nc = ncand;
+  for (int c = tid; c < nc; c += EXR_THREADS) {
+    const float2 e = cand[c];
+    const int id = __float_as_int(e.y);
+    int rank = 0;
+    for (int c2 = 0; c2 < nc; ++c2) {
+      const float2 f = cand[c2];
+      rank += beats(f.x, __float_as_int(f.y), e.x, id) ? 1 : 0;
+    }
+    if (rank < kids) sel[rank] = e;
+  }
+  __syncthreads();
+  // ---- children in token-id order
+  const int u = __ldcg(cur.node + n);
+  if (tid < kids) {
+    const float v = sel[tid].x;
+    const int id = __float_as_int(sel[tid].y);
+    int rank = 0;
+    for (int j = 0; j < kids; ++j) rank += __float_as_int(sel[j].y) < id ? 1 : 0;
+    const int c = i * kids + rank;
+    const float lp = v - s_lse;
+    const float vc = __ldcg(cur.v + n) + lp;
+    t.node_tok[nb0 + base + c] = id;
+    t.node_parent[nb0 + base + c] = u;
+    t.node_depth[nb0 + base + c] = s;
+    t.node_row[nb0 + base + c] = __ldcg(cur.slot + n);
+    t.node_logv[nb0 + base + c] = vc;
+    scratch_v[b * 256 + c] = vc;
+    scratch_tok[b * 256 + c] = id;
+    if (tr.children) {
+      tr.children[static_cast<size_t>(n) * tr.k_max + rank] = id;
+      tr.child_logp[static_cast<size_t>(n) * tr.k_max + rank] = lp;
+    }
+  }
+  if (tr.lse && tid == 0) tr.lse[n] = s_lse;
+  if (s >= t.depth) return;
+
+  // ---- the last row of the request to finish selects the next frontier
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(counters + b, 1) == R - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid == 0) counters[b] = 0;
+  const int nc2 = R * kids;
+  const int F = t.rows[s];
+  for (int c = tid; c < nc2; c += EXR_THREADS) sv[c] = __ldcg(scratch_v + b * 256 + c);
+  __syncthreads();
+  if (t.tree_kind == 1) {  // static: every child, in generation order
+    for (int c = tid; c < nc2; c += EXR_THREADS) spos[c] = c;
+  } else {
+    for (int c = tid; c < nc2; c += EXR_THREADS) {
+      const float vc = sv[c];
+      int rk = 0;
+      for (int c2 = 0; c2 < nc2; ++c2) rk += beats(sv[c2], c2, vc, c) ? 1 : 0;
+      srank[c] = rk;
     }
     __syncthreads();
-    for (int c = tid; c < nc; c += blockDim.x) {
-      if (sel_rank[c] >= F) continue;
+    for (int c = tid; c < nc2; c += EXR_THREADS) {
+      if (srank[c] >= F) continue;
       int p = 0;
-      for (int c2 = 0; c2 < c; ++c2) p += sel_rank[c2] < F ? 1 : 0;
-      sel_pos[p] = c;
+      for (int c2 = 0; c2 < c; ++c2) p += srank[c2] < F ? 1 : 0;
+      spos[p] = c;
     }
   }
   __syncthreads();
   const int slot0 = t.row_base[s];
-  for (int j = tid; j < F; j += blockDim.x) {
-    const int u = base + sel_pos[j];
+  const int neff = __ldcg(t.n_eff + b);
+  for (int j = tid; j < F; j += EXR_THREADS) {
+    const int c = spos[j];
+    const int uu = base + c;
+    const int pi = c / kids;                        // the row that generated the child
     const int n2 = b * F + j;
     const int slot = slot0 + j;
-    const int srow = __ldcg(t.node_row + nb0 + u);
-    const unsigned long long m = __ldcg(t.slot_mask + static_cast<size_t>(b) * t.tree_rows + srow) |
-                                 (1ull << slot);
-    t.slot_mask[static_cast<size_t>(b) * t.tree_rows + slot] = m;
-    t.frontier[b * 64 + j] = u;
+    const unsigned long long mk = __ldcg(cur.mask + b * R + pi) | (1ull << slot);
+    t.slot_mask[static_cast<size_t>(b) * t.tree_rows + slot] = mk;
+    t.frontier[b * 64 + j] = uu;
     nxt.req[n2] = b;
     nxt.slot[n2] = slot;
-    nxt.pos[n2] = __ldcg(t.n_eff + b) + s;
-    nxt.tok[n2] = __ldcg(t.node_tok + nb0 + u);
-    nxt.feat[n2] = b * R + (srow - t.row_base[s - 1]);
-    nxt.node[n2] = u;
-    nxt.mask[n2] = m;
-    if (tr.frontier) tr.frontier[b * tr.f_max + j] = u;
+    nxt.pos[n2] = neff + s;
+    nxt.tok[n2] = __ldcg(scratch_tok + b * 256 + c);
+    nxt.feat[n2] = b * R + pi;
+    nxt.node[n2] = uu;
+    nxt.mask[n2] = mk;
+    nxt.v[n2] = sv[c];
+    if (tr.frontier) tr.frontier[b * tr.f_max + j] = uu;
   }
 }
 
@@ -209,16 +358,19 @@ __global__ void __launch_bounds__(RR_THREADS) rerank_kernel(const TreeArgs t, co
   const size_t nb0 = static_cast<size_t>(b) * t.max_nodes;
   const int G = t.node_base[t.depth] - 1;     // generated nodes: ids 1..G
   const int S = t.slots;
-  // kept flags (node c = tid + 1)
+  // kept flags (node c = tid + 1), ranked from values staged in shared memory
+  __shared__ float vals[RR_THREADS];
+  if (tid < G) vals[tid] = __ldcg(t.node_logv + nb0 + tid + 1);
+  __syncthreads();
   int kf = 0;
   if (tid < G) {
     const int c = tid + 1;
     if (t.tree_kind == 1) {
       kf = 1;
     } else {
-      const float vc = __ldcg(t.node_logv + nb0 + c);
+      const float vc = vals[tid];
       int rk = 0;
-      for (int c2 = 1; c2 <= G; ++c2) rk += beats(__ldcg(t.node_logv + nb0 + c2), c2, vc, c) ? 1 : 0;
+      for (int c2 = 1; c2 <= G; ++c2) rk += beats(vals[c2 - 1], c2, vc, c) ? 1 : 0;
       kf = rk < t.m;
     }
   }
@@ -267,13 +419,21 @@ __global__ void __launch_bounds__(RR_THREADS) rerank_kernel(const TreeArgs t, co
 }
 
 // ----------------------------------------------------- standalone merge
-__global__ void __launch_bounds__(EXP_WARPS * 32)
+constexpr size_t MERGE_SMEM_BUDGET = 180 * 1024;
+constexpr int MG_MAX_WARPS = 16;
+static int merge_warps(int G, int kp) {
+  const size_t per = sizeof(float2) * static_cast<size_t>(G) * kp;
+  int w = static_cast<int>(MERGE_SMEM_BUDGET / per);
+  return w < 1 ? 1 : (w > MG_MAX_WARPS ? MG_MAX_WARPS : w);
+}
+
+__global__ void __launch_bounds__(MG_MAX_WARPS * 32)
 lm_merge_kernel(const LmPartials lm, int N, int k, int* ids, float* logp, float* lse_out) {
   extern __shared__ float2 mg_smem[];
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = blockIdx.x * EXP_WARPS + warp;
+  const int n = blockIdx.x * (blockDim.x >> 5) + warp;
   if (n >= N) return;
   float2* cand = mg_smem + static_cast<size_t>(warp) * lm.G * k;
   float lse, v;
@@ -302,7 +462,8 @@ static cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStrea
 }
 
 cudaError_t tree_setup_attributes() {
-  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(expand_kernel));
+  cudaError_t e = cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(float2) * EXR_CAND));
   if (e != cudaSuccess) return e;
   return allow_max_smem(reinterpret_cast<const void*>(lm_merge_kernel));
 }
@@ -313,15 +474,17 @@ cudaError_t launch_tree_init(const TreeArgs& t, const RowMeta& rows0, cudaStream
   return cudaLaunchKernelEx(&cfg, tree_init_kernel, t, rows0);
 }
 
-static size_t merge_smem(int G, int kp) { return sizeof(float2) * EXP_WARPS * static_cast<size_t>(G) * kp; }
+static size_t merge_smem(int G, int kp) {
+  return sizeof(float2) * merge_warps(G, kp) * static_cast<size_t>(G) * kp;
+}
 
 cudaError_t launch_expand(const TreeArgs& t, int s, const LmPartials& lm, const RowMeta& cur,
                           const RowMeta& next, const ExpandTrace& tr, cudaStream_t st, bool pdl) {
   const int kp = t.kids[s - 1];
-  const size_t smem = merge_smem(lm.G, kp);
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(t.B), dim3(EXP_WARPS * 32), smem, st, pdl, attr);
-  return cudaLaunchKernelEx(&cfg, expand_kernel, t, s, lm, cur, next, tr, kp);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(t.B * t.rows[s - 1]), dim3(EXR_THREADS), sizeof(float2) * EXR_CAND, st,
+                                    pdl, attr);
+  return cudaLaunchKernelEx(&cfg, expand_kernel, t, s, lm, cur, next, tr, kp, t.exp_counters, t.exp_v, t.exp_tok);
 }
 
 cudaError_t launch_rerank(const TreeArgs& t, const OutArgs& o, cudaStream_t st, bool pdl) {
@@ -333,8 +496,8 @@ cudaError_t launch_rerank(const TreeArgs& t, const OutArgs& o, cudaStream_t st, 
 cudaError_t launch_lm_merge(const LmPartials& lm, int N, int k, int* ids, float* logp, float* lse,
                             cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg =
-      make_cfg(dim3((N + EXP_WARPS - 1) / EXP_WARPS), dim3(EXP_WARPS * 32), merge_smem(lm.G, k), st, pdl, attr);
+  const int w = merge_warps(lm.G, k);
+  cudaLaunchConfig_t cfg = make_cfg(dim3((N + w - 1) / w), dim3(w * 32), merge_smem(lm.G, k), st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, lm_merge_kernel, lm, N, k, ids, logp, lse);
 }
 

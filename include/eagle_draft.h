@@ -93,6 +93,8 @@ typedef struct {
 
 #define EAGLE_FLAG_NO_GRAPH 0x1   /* enqueue the kernels directly on every call */
 #define EAGLE_FLAG_NO_PDL   0x2   /* plain stream order between kernels */
+#define EAGLE_FLAG_GEMM_ONE_CTA 0x4 /* every GEMM takes a whole SM (default: the QKV, O, gate/up and
+                                       down GEMMs run two CTAs per SM so the next one starts early) */
 
 /* Weights, stored [out, in] row-major in `dtype` (the norm gains are always f32).
  * w_qkv stacks the query rows, then the key rows, then the value rows.
@@ -224,9 +226,10 @@ typedef enum {
   EAGLE_K_EXPAND = 9, EAGLE_K_RERANK = 10, EAGLE_K_MERGE = 11, EAGLE_K_COUNT = 12
 } eagle_kernel_kind_t;
 
-/* Profiling mode (enable != 0): every later call launches its kernels directly (no graph,
- * no programmatic dependent launch) with a CUDA event recorded on the call's stream
- * before and after each kernel.  eagle_draft_profile_read() synchronises, returns per
+/* Profiling mode (enable != 0): every later eagle_draft_tree call (without a trace)
+ * captures its kernels into a one-off CUDA graph, without programmatic dependent launch,
+ * with a CUDA event recorded before and after each kernel, and replays it on the call's
+ * stream (eagle_draft_lm_head_topk records its events directly on the stream).  eagle_draft_profile_read() synchronises, returns per
  * kind the summed kernel time in ms (host array ms[EAGLE_K_COUNT]) and the number of
  * launches (host array launches[EAGLE_K_COUNT]), and clears the records.  Disabling
  * returns to graph replay. */
