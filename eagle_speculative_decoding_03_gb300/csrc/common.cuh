@@ -279,6 +279,8 @@ struct GemmArgs {
   int tmem_cols;           // allocated TMEM columns
   int nbuf;                // accumulator buffers in TMEM (2 = epilogue overlaps next unit)
   int stages;
+  int csplit;              // 0: stream-K over (tile, K block) units; S >= 1: S CTAs per tile (a
+                           // cluster when S > 1) on consecutive K ranges, reduced through DSMEM
   BSrc b;
   EpiArgs e;
   float* part;             // split-K partial scratch [grid][2][nrb*npad][BM]

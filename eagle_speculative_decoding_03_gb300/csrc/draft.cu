@@ -60,11 +60,11 @@ struct eagle_draft {
   size_t ws_bytes = 0;
   float *h = nullptr, *y = nullptr, *a[2] = {nullptr, nullptr}, *q = nullptr, *o = nullptr, *gu = nullptr;
   float *ss_h = nullptr, *ss_y = nullptr, *g_root = nullptr, *tk = nullptr, *tv = nullptr;
-  float *rope_cos = nullptr, *rope_sin = nullptr, *part = nullptr, *att_part = nullptr;
+  float *rope_cos = nullptr, *rope_sin = nullptr, *part = nullptr;
   float *lm_max = nullptr, *lm_sum = nullptr, *lm_val = nullptr;
   // bf16 hi/lo operand copies [2 N_max][K] written by the producing epilogue (tensor-core path)
   uint16_t *xa_hl = nullptr, *o_hl = nullptr, *xm_hl = nullptr, *s_hl = nullptr, *a_hl = nullptr;
-  int *lm_id = nullptr, *counters = nullptr, *att_counters = nullptr;
+  int *lm_id = nullptr, *counters = nullptr;
   int *node_tok = nullptr, *node_parent = nullptr, *node_depth = nullptr, *node_row = nullptr;
   float* node_logv = nullptr;
   int *n_eff = nullptr, *frontier = nullptr, *exp_counters = nullptr, *exp_tok = nullptr;
@@ -184,7 +184,6 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   h->rope_cos = cv.take<float>(static_cast<size_t>(h->max_pos) * c.head_dim / 2);
   h->rope_sin = cv.take<float>(static_cast<size_t>(h->max_pos) * c.head_dim / 2);
   h->part = cv.take<float>(static_cast<size_t>(num_sms()) * 2 * 256 * BM);
-  h->att_part = cv.take<float>(static_cast<size_t>(B) * c.n_kv_heads * h->max_splits * h->qv_max * (c.head_dim + 4));
   const size_t lmn = static_cast<size_t>(h->lm_G) * n;
   const size_t lmt = static_cast<size_t>(ceil_div(c.vocab, BM)) * n;
   h->lm_max = cv.take<float>(lmt);
@@ -192,7 +191,6 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   h->lm_val = cv.take<float>(lmn * KMAX);
   h->lm_id = cv.take<int>(lmn * KMAX);
   h->counters = cv.take<int>(16384);
-  h->att_counters = cv.take<int>(static_cast<size_t>(B) * c.n_kv_heads);
   const size_t nn = static_cast<size_t>(B) * h->max_nodes;
   h->node_tok = cv.take<int>(nn);
   h->node_parent = cv.take<int>(nn);
@@ -626,8 +624,6 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       a.Hkv = c.n_kv_heads;
       a.hd = c.head_dim;
       a.max_splits = h->max_splits;
-      a.part = h->att_part;
-      a.counters = h->att_counters;
       a.out = h->o;
       a.out_hl = h->tc ? h->o_hl : nullptr;
       ProfScope ps(h, EAGLE_K_ATTN, st);

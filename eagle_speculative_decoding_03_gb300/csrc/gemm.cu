@@ -16,9 +16,12 @@
 #include "common.cuh"
 #include "internal.h"
 
+#include <cooperative_groups.h>
+
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 namespace eagle {
 
@@ -107,6 +110,7 @@ EAGLE_DEV void compute_rstd(const BSrc& b, int N, float* rstd, int tid, int nthr
 struct EpiScratch {
   float xch[16][BM];       // row-major exchange tile (rotary partners, LM-head transpose)
   float red[4][16];        // per-warp partial sums of squares
+  int meta[3][16];         // rows of the chunk: position, request, request-local slot
 };
 // Views of the epilogue's shared memory (the pointers themselves live in registers).
 struct EpiSmem {
@@ -133,8 +137,8 @@ EAGLE_DEV EpiSmem epi_views(void* scratch, void* lm, int N, int topk) {
 }
 
 // hi / lo rows of the operand copy the next GEMM loads with TMA
-EAGLE_DEV void write_hl(const EpiArgs& e, int n, int m, float val) {
-  if (e.hl_gamma) val *= __ldg(e.hl_gamma + m);
+EAGLE_DEV void write_hl(const EpiArgs& e, int n, int m, float val, float gamma = 1.f) {
+  val *= gamma;   // hl_gamma[m], loaded once by the caller
   uint16_t hi, lo;
   split_hilo(val, hi, lo);
   e.hl[static_cast<size_t>(2 * n) * e.hl_ld + m] = hi;
@@ -250,22 +254,67 @@ EAGLE_DEV void warp_topk_insert(float* lv, int* li, int k, const float* nv, int*
 
 // One 16-row chunk of accumulators: thread tl (0..127) holds feature m0 + tl of rows
 // n0 .. n0+15 in v[].  All 128 epilogue threads call this together.
-EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, const float* v, int tl) {
+// The global inputs of one 16-row chunk's epilogue, loaded ahead (all loads of a batch in
+// flight together): STORE: a[] = residuals; QKV: row metadata -> es.s->meta, a[] / b[] =
+// rotary cos / sin of this thread's feature.  Called by all 128 epilogue threads.
+EAGLE_DEV void epilogue_prefetch(const GemmArgs& g, EpiSmem& es, int mt, int n0, int tl, float* a, float* b) {
+  const EpiArgs& e = g.e;
+  const int m = mt * BM + tl;
+  const bool mvalid = m < g.M;
+  if (e.kind == EPI_STORE) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      a[i] = (e.resid && n0 + i < g.N && mvalid) ? __ldcg(e.resid + static_cast<size_t>(n0 + i) * e.ldr + m) : 0.f;
+    b[0] = e.hl && e.hl_gamma && mvalid ? __ldg(e.hl_gamma + m) : 1.f;
+  } else if (e.kind == EPI_QKV) {
+    const int hd = e.hd, half = hd >> 1;
+    const int head = m / hd, i = m - head * hd;
+    const bool rotate = head < e.Hq + e.Hkv;
+    if (tl < 16) {
+      const int n = n0 + tl;
+      es.s->meta[0][tl] = n < g.N ? __ldcg(e.row_pos + n) : 0;
+      es.s->meta[1][tl] = n < g.N ? __ldcg(e.row_req + n) : 0;
+      es.s->meta[2][tl] = n < g.N ? __ldcg(e.row_slot + n) : 0;
+    }
+    named_bar(1, 128);
+    const int j = i < half ? i : i - half;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const bool ok = n0 + r < g.N && mvalid && rotate;
+      const size_t o = static_cast<size_t>(es.s->meta[0][r]) * half + j;
+      a[r] = ok ? __ldg(e.rope_cos + o) : 1.f;
+      b[r] = ok ? __ldg(e.rope_sin + o) : 0.f;
+    }
+  }
+}
+
+// pre_a / pre_b (optional): this thread's inputs for the chunk, loaded earlier by
+// epilogue_prefetch (STORE: residuals; QKV: rotary cos / sin, with the row metadata
+// already in es.s->meta).
+EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, const float* v, int tl,
+                              const float* pre_a = nullptr, const float* pre_b = nullptr) {
   const EpiArgs& e = g.e;
   const int m = mt * BM + tl;
   const bool mvalid = m < g.M;
   const int warp_q = tl >> 5, lane = tl & 31;
   if (e.kind == EPI_STORE) {
+    // every residual load is issued before the first store (a store may alias a later
+    // load, which would otherwise serialise the round trips)
+    float rv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      rv[i] = pre_a ? pre_a[i]
+                    : (e.resid && n0 + i < g.N && mvalid) ? __ldcg(e.resid + static_cast<size_t>(n0 + i) * e.ldr + m) : 0.f;
+    const float gam = pre_b ? pre_b[0] : (e.hl && e.hl_gamma && mvalid ? __ldg(e.hl_gamma + m) : 1.f);
     float sq[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int n = n0 + i;
-      float val = v[i];
+      float val = v[i] + rv[i];
       sq[i] = 0.f;
       if (n < g.N && mvalid) {
-        if (e.resid) val += __ldcg(e.resid + static_cast<size_t>(n) * e.ldr + m);
         e.out[static_cast<size_t>(n) * e.ldo + m] = val;
-        if (e.hl) write_hl(e, n, m, val);
+        if (e.hl) write_hl(e, n, m, val, gam);
         sq[i] = val * val;
       }
     }
@@ -291,25 +340,34 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
       vn[r] = (e.nss && n0 + r < g.N) ? v[r] * es.rstd[n0 + r] : v[r];
       es.s->xch[r][tl] = vn[r];
     }
+    // row metadata (one load per row, shared), then the rotary table entries, all loaded
+    // before the first store
+    float rc[16], rsn[16];
+    if (pre_a) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        rc[r] = pre_a[r];
+        rsn[r] = pre_b[r];
+      }
+    } else {
+      epilogue_prefetch(g, es, mt, n0, tl, rc, rsn);
+    }
     named_bar(1, 128);
     const int partner = tl + (i < half ? half : -half);
-#pragma unroll 4
+#pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int n = n0 + r;
       if (n >= g.N || !mvalid) continue;
       float val = vn[r];
-      const int pos = __ldcg(e.row_pos + n);
       if (rotate) {
-        const int j = i < half ? i : i - half;
-        const float c = __ldg(e.rope_cos + static_cast<size_t>(pos) * half + j);
-        const float s = __ldg(e.rope_sin + static_cast<size_t>(pos) * half + j);
+        const float c = rc[r], s = rsn[r];
         const float p = es.s->xch[r][partner];
         val = i < half ? val * c - p * s : val * c + p * s;
       }
       if (head < e.Hq) {
         e.q[static_cast<size_t>(n) * e.Hq * hd + m] = val;
       } else {
-        const int b = __ldcg(e.row_req + n), slot = __ldcg(e.row_slot + n);
+        const int b = es.s->meta[1][r], slot = es.s->meta[2][r];
         const bool isk = head < e.Hq + e.Hkv;
         const int kvh = isk ? head - e.Hq : head - e.Hq - e.Hkv;
         float* dst = isk ? e.tk : e.tv;
@@ -324,6 +382,7 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
     named_bar(1, 128);
     if (tl < 64) {
       const int j = mt * (BM / 2) + tl;
+      const float gam = e.hl && e.hl_gamma ? __ldg(e.hl_gamma + j) : 1.f;
 #pragma unroll 4
       for (int r = 0; r < 16; ++r) {
         const int n = n0 + r;
@@ -335,7 +394,7 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
           }
           const float sv = silu_f(gt) * up;
           if (e.out) e.out[static_cast<size_t>(n) * e.ldo + j] = sv;
-          if (e.hl) write_hl(e, n, j, sv);
+          if (e.hl) write_hl(e, n, j, sv, gam);
         }
       }
     }
@@ -462,7 +521,7 @@ constexpr uint32_t TC_SMEM_OCC2 = 113 * 1024;   // two CTAs per SM
 // B tile rows are interleaved: row 2r = hi of GEMM row r, row 2r+1 = its lo part, so the
 // accumulator column 2r + 1 holds the low-order correction of column 2r.
 // NT = TC_THREADS (converter warps present, one CTA per SM) or 7 warps (operand by TMA only;
-// MINB = 2 lets the next kernel's CTA share the SM and start its weight stream early).
+// MINB = 1: the whole register file, MINB = 2: two CTAs per SM).
 template <int NT, int MINB>
 __global__ void __launch_bounds__(NT, MINB)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
@@ -487,7 +546,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
   const int KB = g.KB;
   const int npad = g.npad, nrb = g.nrb, np2 = 2 * npad;
   const Sched sc{static_cast<long long>(g.MT) * KB, static_cast<int>(gridDim.x)};
-  const long long u0 = sc.begin(blockIdx.x), u1 = sc.begin(blockIdx.x + 1);
+  // units [u0, u1): stream-K range, or (csplit) K range r of tile blockIdx.x / S
+  const int cs_t = g.csplit > 0 ? static_cast<int>(blockIdx.x) / g.csplit : 0;
+  const int cs_r = g.csplit > 0 ? static_cast<int>(blockIdx.x) - cs_t * g.csplit : 0;
+  const long long u0 = g.csplit > 0 ? static_cast<long long>(cs_t) * KB + static_cast<long long>(cs_r) * KB / g.csplit
+                                    : sc.begin(blockIdx.x);
+  const long long u1 = g.csplit > 0
+                           ? static_cast<long long>(cs_t) * KB + static_cast<long long>(cs_r + 1) * KB / g.csplit
+                           : sc.begin(blockIdx.x + 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < g.stages; ++s) {
@@ -782,6 +848,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
           for (int r = 0; r < 16; ++r) v[r] = c[2 * r] + c[2 * r + 1];
           if (complete) {
             epilogue_chunk(g, es, mt, n0, v, tl);
+          } else if (g.csplit > 1) {   // this rank's partial, in its (now idle) stage ring
+            float* cpart = reinterpret_cast<float*>(smem);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) cpart[static_cast<size_t>(n0 + r) * BM + tl] = v[r];
           } else {
 #pragma unroll
             for (int r = 0; r < 16; ++r) mypart[static_cast<size_t>(n0 + r) * BM + tl] = v[r];
@@ -791,7 +861,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
-      if (!complete) {
+      if (!complete && g.csplit == 0) {
         __threadfence();
         named_bar(1, 128);
         const int cf = sc.owner(static_cast<long long>(mt) * KB);
@@ -840,6 +910,51 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
       i += kb1 - kb0;
     }
     if (g.e.kind == EPI_LMHEAD) lmhead_flush(g, es, blockIdx.x, tl);
+  }
+
+  if (g.csplit > 1) {
+    // Every thread of every rank passes both cluster barriers (whatever its role did), so
+    // no rank can wait on one that left.  Rank 0 sums the ranks' partials in rank order.
+    cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+    const bool red = warp >= 2 && warp < 6 && cs_r == 0;
+    const bool pre_ok = red && g.N <= 16;   // one chunk of rows: its inputs load during the barrier
+    const int tl = (warp & 3) * 32 + lane;
+    EpiSmem es = epi_views(smem + L.epi_off, smem + L.lm_off, g.N, g.e.topk);
+    es.rstd = reinterpret_cast<float*>(smem + L.erstd_off);
+    float pre_a[16], pre_b[16];
+    if (pre_ok) epilogue_prefetch(g, es, cs_t, 0, tl, pre_a, pre_b);
+    cluster.sync();
+    if (red) {
+      for (int rb = 0; rb < nrb; ++rb) {
+        for (int c0 = 0; c0 < npad; c0 += 16) {
+          const int n0 = rb * npad + c0;
+          if (n0 >= g.N) break;
+          float v[16];
+#pragma unroll
+          for (int r = 0; r < 16; ++r) v[r] = 0.f;
+          for (int q0 = 0; q0 < g.csplit; q0 += 2) {   // loads of two ranks in flight together
+            float pv[2][16];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              if (q0 + u < g.csplit) {
+                const float* pq = cluster.map_shared_rank(reinterpret_cast<float*>(smem), q0 + u);
+#pragma unroll
+                for (int r = 0; r < 16; ++r) pv[u][r] = pq[static_cast<size_t>(n0 + r) * BM + tl];
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              if (q0 + u < g.csplit) {
+#pragma unroll
+                for (int r = 0; r < 16; ++r) v[r] += pv[u][r];
+              }
+          }
+          if (pre_ok) epilogue_chunk(g, es, cs_t, n0, v, tl, pre_a, pre_b);
+          else epilogue_chunk(g, es, cs_t, n0, v, tl);
+        }
+      }
+    }
+    cluster.sync();   // the partials stay in place until rank 0 has read them
   }
 
   tc_fence_before();
@@ -994,6 +1109,42 @@ cudaError_t allow_max_smem(const void* func, size_t* granted) {
   return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(m));
 }
 
+// Clusters of S CTAs of the one-CTA-per-SM kernel (full shared memory) the device holds
+// at once; cached per device and size.
+int gemm_active_clusters(int S) {
+  static std::mutex mu;
+  static int cache[16][9];
+  static bool init = false;
+  std::lock_guard<std::mutex> lk(mu);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 16 || S < 1 || S > 8) return 0;
+  if (!init) {
+    for (auto& row : cache)
+      for (int& c : row) c = -1;
+    init = true;
+  }
+  if (cache[dev][S] >= 0) return cache[dev][S];
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(S, 1, 1);
+  cfg.blockDim = dim3(TC_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = g_tc_smem_cap ? g_tc_smem_cap : 200 * 1024;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<TC_THREADS, 1>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[dev][S] = n;
+  return n;
+}
+
 // Fill the launch geometry of a GEMM over N rows.
 bool plan_gemm(GemmPlan& p, int N) {
   GemmArgs& g = p.args;
@@ -1016,11 +1167,35 @@ bool plan_gemm(GemmPlan& p, int N) {
   while (cols < g.nbuf * accum_cols) cols <<= 1;
   g.tmem_cols = cols;
   const long long total = static_cast<long long>(g.MT) * g.KB;
-  p.grid = static_cast<int>(std::min<long long>(num_sms(), total));
+  const int sms = num_sms();
+  p.grid = static_cast<int>(std::min<long long>(sms, total));
   p.grid_y = 1;
   const int topk = std::max(1, g.e.topk);
   const int lm_rows = g.e.kind == EPI_LMHEAD ? N : 0;
-  if (p.occ == 2 && (!g.b_tma || g.tmem_cols > 256)) p.occ = 1;
+  // Work split.  Few tiles (the small-N projections): S CTAs per tile in a cluster, each
+  // on 1/S of K, reduced on chip; enough tiles to fill the SMs: one tile per CTA;
+  // otherwise (the LM head, very wide layers) the stream-K schedule.
+  g.csplit = 0;
+  const size_t part_bytes = static_cast<size_t>(g.nrb) * g.npad * BM * sizeof(float);
+  if (g.e.kind != EPI_LMHEAD && !p.stream_k) {
+    int S = std::min(std::min(8, g.KB), sms / g.MT);
+    while (S >= 2 && gemm_active_clusters(S) < g.MT) --S;
+    if (S >= 2 && part_bytes <= 2 * static_cast<size_t>(A_STAGE_BYTES)) {
+      g.csplit = S;
+      p.occ = 1;
+    } else if (S < 2 && 4 * g.MT >= 3 * sms && g.MT <= sms * (g.b_tma ? 2 : 1)) {
+      g.csplit = 1;
+      p.occ = g.MT > sms ? 2 : 1;
+    }
+    if (g.csplit > 0) p.grid = g.MT * g.csplit;
+  }
+  if (p.occ == 2 && (!g.b_tma || g.tmem_cols > 256)) {
+    p.occ = 1;
+    if (g.csplit == 1 && g.MT > sms) {   // one tile per CTA needs two CTAs per SM here
+      g.csplit = 0;
+      p.grid = static_cast<int>(std::min<long long>(sms, total));
+    }
+  }
   uint32_t cap = static_cast<uint32_t>(g_tc_smem_cap ? g_tc_smem_cap : TC_MAX_SMEM);
   if (p.occ == 2) cap = std::min(cap, TC_SMEM_OCC2);
   int stages = 12;
@@ -1042,16 +1217,22 @@ cudaError_t gemm_setup_attributes() {
   if (e != cudaSuccess) return e;
   e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS_TMA, 2>));
   if (e != cudaSuccess) return e;
+  e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS_TMA, 1>));
+  if (e != cudaSuccess) return e;
   return allow_max_smem(reinterpret_cast<const void*>(gemm_simt_kernel), &g_simt_smem_cap);
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = p.tc && p.args.csplit > 1 ? p.args.csplit : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.tc && p.args.csplit > 1 ? 2 : 1;
   cfg.stream = st;
   cfg.dynamicSmemBytes = p.smem;
   if (p.tc) {
@@ -1059,6 +1240,10 @@ cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t st, bool pdl) {
     if (p.occ == 2) {
       cfg.blockDim = dim3(TC_THREADS_TMA, 1, 1);
       return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 2>, p.tm0, p.tm1, p.tmB, p.args);
+    }
+    if (p.args.b_tma) {   // no converter warps: the full register file for 7 warps
+      cfg.blockDim = dim3(TC_THREADS_TMA, 1, 1);
+      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 1>, p.tm0, p.tm1, p.tmB, p.args);
     }
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS, 1>, p.tm0, p.tm1, p.tmB, p.args);

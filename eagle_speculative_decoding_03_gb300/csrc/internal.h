@@ -20,6 +20,7 @@ struct GemmPlan {
   int grid = 0, grid_y = 1;
   size_t smem = 0;
   int occ = 1;                   // tc with TMA operand: 2 = two CTAs per SM (smaller ring)
+  bool stream_k = false;         // force the stream-K schedule (no per-tile CTA clusters)
 };
 
 // Allow `func` the device's opt-in maximum of dynamic shared memory (minus its static use).
@@ -28,6 +29,7 @@ size_t max_dyn_smem(const void* func);
 
 bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K, int box_rows = BM);
 int num_sms();
+int gemm_active_clusters(int S);
 bool plan_gemm(GemmPlan& p, int N);
 cudaError_t gemm_setup_attributes();
 cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t st, bool pdl);
@@ -47,9 +49,7 @@ struct AttnArgs {
   int tree_rows;            // request-local row capacity
   int tree_upto;            // rows that exist so far (through this depth)
   int B, Hq, Hkv, hd;
-  int max_splits;           // prefix splits + 1 (tree split)
-  float* part;              // [B][Hkv][max_splits][qv][hd + 2]
-  int* counters;            // [B][Hkv]
+  int max_splits;           // prefix chunks + 1 (tree chunk) of the longest request
   float* out;               // [N][Hq*hd]
   uint16_t* out_hl;         // [2N][Hq*hd] bf16 hi / lo rows of out (operand of the O projection)
 };

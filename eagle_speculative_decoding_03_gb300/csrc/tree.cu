@@ -173,13 +173,19 @@ __global__ void __launch_bounds__(EXR_THREADS)
 expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta cur, const RowMeta nxt,
               const ExpandTrace tr, const int kp, int* counters, float* scratch_v, int* scratch_tok) {
   extern __shared__ float2 cand[];                 // [EXR_CAND]
-  __shared__ float red_m[EXR_WARPS], red_s[EXR_WARPS], red_t[EXR_WARPS];
+  __shared__ float red_m[EXR_WARPS], red_s[EXR_WARPS];
+  __shared__ float2 heads[256];          // list heads: value, id bits (id -1: empty list)
+  __shared__ float thr_v;
+  __shared__ int thr_i;
   __shared__ float2 sel[KMAX];
   __shared__ int ncand;
   __shared__ float s_lse;
   __shared__ int s_last;
   __shared__ float sv[256];
   __shared__ int srank[256], spos[256];
+  __shared__ int s_u, s_slot, s_neff;
+  __shared__ float s_vu;
+  __shared__ unsigned long long s_pmask[64];
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -189,32 +195,55 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
   const int base = t.node_base[s - 1];
   const int G = lm.G;
 
-  // ---- log-sum-exp over the row's per-tile pairs, and the pruning threshold: the best
-  // kp-th entry over the complete CTA lists (the row's kp-th value cannot be lower)
+  // Metadata, loaded into registers together with the partials (one round trip): the
+  // row's node, value and slot, the prefix length, and the masks of the request's rows
+  // (parents of the next frontier, used by the request's last row to finish).
+  int r_u = 0, r_slot = 0, r_neff = 0;
+  float r_vu = 0.f;
+  unsigned long long r_mask = 0ull;
+  if (tid == 0) {
+    r_u = __ldcg(cur.node + n);
+    r_vu = __ldcg(cur.v + n);
+    r_slot = __ldcg(cur.slot + n);
+    r_neff = __ldcg(t.n_eff + b);
+  }
+  if (tid < R && s < t.depth) r_mask = __ldcg(cur.mask + b * R + tid);
+
+  // ---- log-sum-exp over the row's per-tile pairs (loads batched ahead of the arithmetic)
   float m = -INFINITY, sm = 0.f;
-  for (int t0 = tid; t0 < lm.T; t0 += EXR_THREADS) {
-    const float mt = __ldcg(lm.max + static_cast<size_t>(n) * lm.T + t0);
-    const float st = __ldcg(lm.sum + static_cast<size_t>(n) * lm.T + t0);
-    if (mt == -INFINITY) continue;
-    if (mt > m) {
-      sm = sm * expf(m - mt) + st;
-      m = mt;
-    } else {
-      sm += st * expf(mt - m);
+  const float* pm = lm.max + static_cast<size_t>(n) * lm.T;
+  const float* ps = lm.sum + static_cast<size_t>(n) * lm.T;
+  for (int t0 = tid; t0 < lm.T; t0 += 4 * EXR_THREADS) {
+    float mt[4], st[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int tt = t0 + j * EXR_THREADS;
+      mt[j] = tt < lm.T ? __ldcg(pm + tt) : -INFINITY;
+      st[j] = tt < lm.T ? __ldcg(ps + tt) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (mt[j] == -INFINITY) continue;
+      if (mt[j] > m) {
+        sm = sm * expf(m - mt[j]) + st[j];
+        m = mt[j];
+      } else {
+        sm += st[j] * expf(mt[j] - m);
+      }
     }
   }
-  float thr = -INFINITY;
+  // this thread's CTA list, whole (sorted best first; empty entries have id -1)
   float lv[KMAX];
   int li[KMAX];
   const size_t lbase = static_cast<size_t>(n) * G * kp;
-  if (tid < G) {   // this thread's CTA list, whole
+  if (tid < G) {
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
       if (j < kp) {
         lv[j] = __ldcg(lm.val + lbase + static_cast<size_t>(tid) * kp + j);
         li[j] = __ldcg(lm.id + lbase + static_cast<size_t>(tid) * kp + j);
-        if (j == kp - 1 && li[j] >= 0) thr = lv[j];
       }
+    heads[tid] = make_float2(lv[0], __int_as_float(li[0]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -223,34 +252,59 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
     const float M = fmaxf(m, om);
     sm = (m == -INFINITY ? 0.f : sm * expf(m - M)) + (om == -INFINITY ? 0.f : os * expf(om - M));
     m = M;
-    thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, o));
   }
   if (lane == 0) {
     red_m[warp] = m;
     red_s[warp] = sm;
-    red_t[warp] = thr;
   }
-  if (tid == 0) ncand = 0;
-  __syncthreads();
   if (tid == 0) {
-    float M = -INFINITY, S = 0.f, T = -INFINITY;
+    ncand = 0;
+    thr_v = -INFINITY;
+    thr_i = INT_MAX;
+    s_u = r_u;
+    s_vu = r_vu;
+    s_slot = r_slot;
+    s_neff = r_neff;
+  }
+  if (tid < R) s_pmask[tid] = r_mask;
+  __syncthreads();
+  // Pruning bound: the kids-th best list head h.  The kids best heads are distinct
+  // entries no worse than h, so every one of the row's top-kids entries is no worse
+  // than h (in the value-then-id order): only entries that h does not beat can be kept.
+  if (tid < G && li[0] >= 0) {   // rank of this list's head among the heads (branch-free)
+    const float v0 = lv[0];
+    const int i0 = li[0];
+    int rk = 0;
+#pragma unroll 8
+    for (int c2 = 0; c2 < G; ++c2) {
+      const float2 h = heads[c2];
+      const int hi = __float_as_int(h.y);
+      rk += (hi >= 0) & ((h.x > v0) | ((h.x == v0) & (hi < i0)));
+    }
+    if (rk == kids - 1) {
+      thr_v = v0;
+      thr_i = i0;
+    }
+  }
+  if (tid == 32) {
+    float M = -INFINITY, S = 0.f;
     for (int w = 0; w < EXR_WARPS; ++w) {
       const float mw = red_m[w], sw = red_s[w];
       const float MM = fmaxf(M, mw);
       S = (M == -INFINITY ? 0.f : S * expf(M - MM)) + (mw == -INFINITY ? 0.f : sw * expf(mw - MM));
       M = MM;
-      T = fmaxf(T, red_t[w]);
     }
     s_lse = M + logf(S);
-    red_t[0] = T;
   }
   __syncthreads();
-  thr = red_t[0];
-  // ---- candidates: list entries >= thr (each list is sorted best first)
+  // ---- candidates: list entries that the bound does not beat
   if (tid < G) {
+    const float tv = thr_v;
+    const int ti = thr_i;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
-      if (j < kp && li[j] >= 0 && lv[j] >= thr) cand[atomicAdd(&ncand, 1)] = make_float2(lv[j], __int_as_float(li[j]));
+      if (j < kp && li[j] >= 0 && !beats(tv, ti, lv[j], li[j]))
+        cand[atomicAdd(&ncand, 1)] = make_float2(lv[j], __int_as_float(li[j]));
   }
   __syncthreads();
   const int nc = ncand;
@@ -258,15 +312,17 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
     const float2 e = cand[c];
     const int id = __float_as_int(e.y);
     int rank = 0;
+#pragma unroll 8
     for (int c2 = 0; c2 < nc; ++c2) {
       const float2 f = cand[c2];
-      rank += beats(f.x, __float_as_int(f.y), e.x, id) ? 1 : 0;
+      const int fid = __float_as_int(f.y);
+      rank += (f.x > e.x) | ((f.x == e.x) & (fid < id));
     }
     if (rank < kids) sel[rank] = e;
   }
   __syncthreads();
   // ---- children in token-id order
-  const int u = __ldcg(cur.node + n);
+  const int u = s_u;
   if (tid < kids) {
     const float v = sel[tid].x;
     const int id = __float_as_int(sel[tid].y);
@@ -274,11 +330,11 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
     for (int j = 0; j < kids; ++j) rank += __float_as_int(sel[j].y) < id ? 1 : 0;
     const int c = i * kids + rank;
     const float lp = v - s_lse;
-    const float vc = __ldcg(cur.v + n) + lp;
+    const float vc = s_vu + lp;
     t.node_tok[nb0 + base + c] = id;
     t.node_parent[nb0 + base + c] = u;
     t.node_depth[nb0 + base + c] = s;
-    t.node_row[nb0 + base + c] = __ldcg(cur.slot + n);
+    t.node_row[nb0 + base + c] = s_slot;
     t.node_logv[nb0 + base + c] = vc;
     scratch_v[b * 256 + c] = vc;
     scratch_tok[b * 256 + c] = id;
@@ -300,35 +356,44 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
   if (tid == 0) counters[b] = 0;
   const int nc2 = R * kids;
   const int F = t.rows[s];
-  for (int c = tid; c < nc2; c += EXR_THREADS) sv[c] = __ldcg(scratch_v + b * 256 + c);
-  __syncthreads();
   if (t.tree_kind == 1) {  // static: every child, in generation order
-    for (int c = tid; c < nc2; c += EXR_THREADS) spos[c] = c;
+    for (int c = tid; c < nc2; c += EXR_THREADS) {
+      spos[c] = c;
+      sv[c] = __ldcg(scratch_v + b * 256 + c);
+    }
   } else {
+    // the F best children (value, then generation index), kept in generation order
+    for (int c = tid; c < nc2; c += EXR_THREADS) sv[c] = __ldcg(scratch_v + b * 256 + c);
+    __syncthreads();
     for (int c = tid; c < nc2; c += EXR_THREADS) {
       const float vc = sv[c];
       int rk = 0;
-      for (int c2 = 0; c2 < nc2; ++c2) rk += beats(sv[c2], c2, vc, c) ? 1 : 0;
+#pragma unroll 8
+      for (int c2 = 0; c2 < nc2; ++c2) {
+        const float w2 = sv[c2];
+        rk += (w2 > vc) | ((w2 == vc) & (c2 < c));
+      }
       srank[c] = rk;
     }
     __syncthreads();
     for (int c = tid; c < nc2; c += EXR_THREADS) {
       if (srank[c] >= F) continue;
       int p = 0;
-      for (int c2 = 0; c2 < c; ++c2) p += srank[c2] < F ? 1 : 0;
+#pragma unroll 8
+      for (int c2 = 0; c2 < c; ++c2) p += srank[c2] < F;
       spos[p] = c;
     }
   }
   __syncthreads();
   const int slot0 = t.row_base[s];
-  const int neff = __ldcg(t.n_eff + b);
+  const int neff = s_neff;
   for (int j = tid; j < F; j += EXR_THREADS) {
     const int c = spos[j];
     const int uu = base + c;
     const int pi = c / kids;                        // the row that generated the child
     const int n2 = b * F + j;
     const int slot = slot0 + j;
-    const unsigned long long mk = __ldcg(cur.mask + b * R + pi) | (1ull << slot);
+    const unsigned long long mk = s_pmask[pi] | (1ull << slot);
     t.slot_mask[static_cast<size_t>(b) * t.tree_rows + slot] = mk;
     t.frontier[b * 64 + j] = uu;
     nxt.req[n2] = b;
