@@ -47,6 +47,34 @@ def algorithmic_bytes(cfg, n_prefix_total: int, N_rows_per_depth):
     return weights * cfg.depth + kv * cfg.depth + emb + fc3, weights, kv
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one LM-head launch of the
+# headline workload (depth-2 launch, 10 rows), from the ncu capture summarised in
+# profiles/lm_head_gemm_eagle2_b1.md, and the hash of the kernel sources it was taken on:
+# reported only while they match.
+LM_TRAFFIC_BYTES = 1055.62e6
+LM_TRAFFIC_SOURCES = ("csrc/gemm.cu", "csrc/common.cuh", "csrc/internal.h")
+LM_TRAFFIC_SHA256 = "25cfe3afbc6265432c51395342784bdeb487d256e527fc31c21cf691e5568fa6"
+
+
+def lm_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in LM_TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "eagle_speculative_decoding_03_gb300", f), "rb") as fh:
+            h.update(fh.read())
+    return LM_TRAFFIC_BYTES if h.hexdigest() == LM_TRAFFIC_SHA256 else None
+
+
+def describe(name, cfg, B):
+    if cfg.tree == "static":
+        tree = f"EAGLE-1 static tree, branching {list(cfg.branching)}"
+    else:
+        tree = f"{'EAGLE-3' if cfg.feat == 'fused' else 'EAGLE-2'} dynamic tree k={cfg.k} depth={cfg.depth} m={cfg.m}"
+    pre = cfg.prefix[1] if cfg.prefix[0] == cfg.prefix[1] else f"U[{cfg.prefix[0]},{cfg.prefix[1]}]"
+    return (f"{name}: {tree}; head d={cfg.d}, {cfg.n_heads}q/{cfg.n_kv_heads}kv x {cfg.head_dim}, "
+            f"ff={cfg.d_ff}, |V|={cfg.vocab}, {cfg.dtype}; prefix n={pre}; B={B} per GPU")
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -239,6 +267,7 @@ def run_ours(args):
     lm_avg_ms = lm_ms / max(lm_n, 1)
     lm_bytes = (2 if cfg.dtype == "bf16" else 4) * cfg.vocab * cfg.d
     lm_gbs = lm_bytes / (lm_avg_ms * 1e-3) / 1e9
+    traffic = lm_traffic() if args.workload == "eagle2_b1" else None
     prof_total = sum(v[0] for v in prof.values())
     kernels = {k: {"ms_per_tree": v[0] / prof_trees, "share": v[0] / prof_total} for k, v in prof.items()}
 
@@ -314,19 +343,20 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "us_per_draft_step": ms * 1e3 / cfg.depth,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}: EAGLE-2 dynamic tree k={cfg.k} depth={cfg.depth} m={cfg.m}, "
-                               f"Llama-3-8B-shaped head (d={cfg.d}, {cfg.n_heads}q/{cfg.n_kv_heads}kv x "
-                               f"{cfg.head_dim}, ff={cfg.d_ff}, |V|={cfg.vocab}), prefix n={cfg.prefix[1]}, "
-                               f"B={B} per GPU",
+        "config": {"workload": describe(args.workload, cfg, B),
                    "global_batch": B * world, "seq_len": cfg.prefix[1], "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2: every tree streams the 1.55 GB of head weights from HBM",
+                   "l2": f"inputs larger than L2: every depth streams the {wbytes / 1e9:.2f} GB of head weights "
+                         f"from HBM" if wbytes > 129e6 else "weights fit in L2 (latency-bound shape)",
                    "nodes_per_tree": nodes_per_tree, "timing": "graph replay, CUDA events on the stream"},
         "hbm_frac_step": step_gbs / peak,
         "step_algorithmic_bytes": algo,
         "roofline": {"bound": "hbm", "kernel": "lm_head (gemm_tc_kernel, LM-head epilogue)",
                      "achieved": lm_gbs, "peak": peak, "unit": "GB/s", "frac": lm_gbs / peak,
                      "peak_source": peak_kind, "algorithmic_bytes_per_launch": lm_bytes,
-                     "avg_launch_ms": lm_avg_ms, "traffic": None},
+                     "avg_launch_ms": lm_avg_ms, "traffic": traffic,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the "
+                                       "depth-2 launch, profiles/lm_head_gemm_eagle2_b1.md"
+                                       if traffic else "kernel changed since the last capture"},
         "kernels": kernels,
         "gpu_launches": launches,
         "e2e": e2e,
