@@ -63,7 +63,7 @@ struct eagle_draft {
   float *rope_cos = nullptr, *rope_sin = nullptr, *part = nullptr;
   float *lm_max = nullptr, *lm_sum = nullptr, *lm_val = nullptr;
   // bf16 hi/lo operand copies [2 N_max][K] written by the producing epilogue (tensor-core path)
-  uint16_t *xa_hl = nullptr, *o_hl = nullptr, *xm_hl = nullptr, *s_hl = nullptr, *a_hl = nullptr;
+  uint16_t *xa_hl = nullptr, *o_hl = nullptr, *xm_hl = nullptr, *s_hl = nullptr, *a_hl = nullptr, *fc_hl = nullptr;
   int *lm_id = nullptr, *counters = nullptr;
   int *node_tok = nullptr, *node_parent = nullptr, *node_depth = nullptr, *node_row = nullptr;
   float* node_logv = nullptr;
@@ -85,7 +85,7 @@ struct eagle_draft {
 };
 
 static const char* kKernelNames[EAGLE_K_COUNT] = {"init", "fc3", "fc", "qkv_rope", "attention", "o_proj",
-                                                  "gate_up", "down", "lm_head", "expand", "rerank", "lm_merge"};
+                                                  "gate_up", "down", "lm_head", "expand", "rerank", "lm_merge", "fc_operand"};
 
 // Event pair around one launch (profiling mode only).
 struct ProfScope {
@@ -175,6 +175,7 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   h->xm_hl = cv.take<uint16_t>(static_cast<size_t>(2 * n) * d);
   h->s_hl = cv.take<uint16_t>(static_cast<size_t>(2 * n) * c.d_ff);
   h->a_hl = cv.take<uint16_t>(static_cast<size_t>(2 * n) * d);
+  h->fc_hl = cv.take<uint16_t>(static_cast<size_t>(2 * n) * 2 * d);
   h->ss_h = cv.take<float>(static_cast<size_t>(dt) * n);
   h->ss_y = cv.take<float>(static_cast<size_t>(dt) * n);
   h->g_root = cv.take<float>(static_cast<size_t>(B) * d);
@@ -336,7 +337,7 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
     delete h;
     return fail(EAGLE_ERR_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
   }
-  h->launches = 1 + (c.feat_kind == EAGLE_FEAT_FUSED ? 1 : 0) + 8 * c.depth + 1;
+  h->launches = 1 + (c.feat_kind == EAGLE_FEAT_FUSED ? 1 : 0) + (h->tc ? 9 : 8) * c.depth + 1;
   *out = h;
   return EAGLE_OK;
 }
@@ -554,15 +555,35 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
     // fc over [feat ; emb(tok)]
     {
       GemmPlan p = base_plan(h, h->tm_fc, nullptr, h->w.w_fc, nullptr, d, 2 * d, d);
-      BSrc& b = p.args.b;
-      b.mode = B_FC;
-      b.x = a_prev;
-      b.ldx = d;
-      b.split = d;
-      b.row_feat = cur.feat;
-      b.row_tok = cur.tok;
-      b.emb = h->w.embed;
-      b.emb_bf16 = h->tc ? 1 : 0;
+      if (h->tc) {
+        // the rows' operand copy (gather + hi/lo split) once, then a TMA operand like
+        // every other projection
+        FcOperandArgs fo;
+        fo.N = N;
+        fo.d = d;
+        fo.row_feat = cur.feat;
+        fo.row_tok = cur.tok;
+        fo.feat = s == 1 ? a_prev : nullptr;
+        fo.ldf = d;
+        fo.feat_hl = s == 1 ? nullptr : h->a_hl;
+        fo.emb = static_cast<const uint16_t*>(h->w.embed);
+        fo.out = h->fc_hl;
+        {
+          ProfScope ps(h, EAGLE_K_FC_OPERAND, st);
+          CU(launch_fc_operand(fo, st, pdl));
+        }
+        tma_operand(p, h->fc_hl, h->gemm_occ2);
+      } else {
+        BSrc& b = p.args.b;
+        b.mode = B_FC;
+        b.x = a_prev;
+        b.ldx = d;
+        b.split = d;
+        b.row_feat = cur.feat;
+        b.row_tok = cur.tok;
+        b.emb = h->w.embed;
+        b.emb_bf16 = 0;
+      }
       p.args.e = epi_store(h->h, d, nullptr, 0, h->ss_h, static_cast<int>(nmax));
       if (h->tc) write_operand(p.args.e, h->xa_hl, d, h->w.attn_norm);
       if ((r = run_gemm(h, p, N, st, EAGLE_K_FC)) != EAGLE_OK) return r;

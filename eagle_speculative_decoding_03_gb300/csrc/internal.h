@@ -129,6 +129,22 @@ struct ExpandTrace {
 
 cudaError_t tree_setup_attributes();
 cudaError_t launch_tree_init(const TreeArgs& t, const RowMeta& rows0, cudaStream_t st, bool pdl);
+
+// The fc GEMM's tensor-core operand for one depth: row n = [feature of row row_feat[n] ;
+// embedding of token row_tok[n]] as bf16 hi (row 2n) and lo (row 2n+1) parts, [2N][2d].
+// The feature comes from an fp32 matrix (the roots) or from the previous depth's operand
+// copy (already hi/lo); an embedding is exact in bf16 (lo = 0).
+struct FcOperandArgs {
+  int N, d;
+  const int* row_feat;
+  const int* row_tok;
+  const float* feat;          // [*][ldf] fp32, or null
+  int ldf;
+  const uint16_t* feat_hl;    // [2 *][d] hi / lo rows, or null
+  const uint16_t* emb;        // [V][d] bf16
+  uint16_t* out;              // [2N][2d]
+};
+cudaError_t launch_fc_operand(const FcOperandArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_expand(const TreeArgs& t, int s, const LmPartials& lm, const RowMeta& cur,
                           const RowMeta& next, const ExpandTrace& tr, cudaStream_t st, bool pdl);
 cudaError_t launch_rerank(const TreeArgs& t, const OutArgs& o, cudaStream_t st, bool pdl);

@@ -48,6 +48,47 @@ __global__ void tree_init_kernel(const TreeArgs t, const RowMeta r0) {
   r0.v[b] = 0.f;
 }
 
+// ------------------------------------------------------- fc operand copy
+// One item = 8 consecutive columns of one row: a feature chunk (copied hi/lo, or split
+// from fp32) or an embedding chunk (hi = the bf16 value, lo = 0).
+__global__ void __launch_bounds__(256) fc_operand_kernel(const FcOperandArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int chunks = a.d / 8;
+  const long long total = static_cast<long long>(a.N) * 2 * chunks;
+  const size_t ld = 2 * static_cast<size_t>(a.d);
+  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
+       it += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(it / (2 * chunks)), c = static_cast<int>(it - static_cast<long long>(n) * 2 * chunks);
+    uint4* hi = reinterpret_cast<uint4*>(a.out + 2 * static_cast<size_t>(n) * ld) + c;
+    uint4* lo = reinterpret_cast<uint4*>(a.out + (2 * static_cast<size_t>(n) + 1) * ld) + c;
+    if (c < chunks) {
+      const int f = __ldcg(a.row_feat + n);
+      if (a.feat_hl) {
+        const uint4 h = __ldcg(reinterpret_cast<const uint4*>(a.feat_hl + 2 * static_cast<size_t>(f) * a.d) + c);
+        const uint4 l = __ldcg(reinterpret_cast<const uint4*>(a.feat_hl + (2 * static_cast<size_t>(f) + 1) * a.d) + c);
+        *hi = h;
+        *lo = l;
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(a.feat + static_cast<size_t>(f) * a.ldf) + 2 * c;
+        const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        uint16_t hv[8], lv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split_hilo(xv[e], hv[e], lv[e]);
+        *hi = make_uint4(hv[0] | (uint32_t(hv[1]) << 16), hv[2] | (uint32_t(hv[3]) << 16), hv[4] | (uint32_t(hv[5]) << 16),
+                         hv[6] | (uint32_t(hv[7]) << 16));
+        *lo = make_uint4(lv[0] | (uint32_t(lv[1]) << 16), lv[2] | (uint32_t(lv[3]) << 16), lv[4] | (uint32_t(lv[5]) << 16),
+                         lv[6] | (uint32_t(lv[7]) << 16));
+      }
+    } else {
+      const int t = __ldcg(a.row_tok + n);
+      *hi = __ldg(reinterpret_cast<const uint4*>(a.emb + static_cast<size_t>(t) * a.d) + (c - chunks));
+      *lo = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
 // ---------------------------------------------- merge of LM-head partials
 constexpr int MERGE_MAX_G = 256;   // CTAs (lists) one warp can merge: 8 lists per lane
 
@@ -556,6 +597,15 @@ cudaError_t launch_rerank(const TreeArgs& t, const OutArgs& o, cudaStream_t st, 
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(t.B), dim3(RR_THREADS), 0, st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, rerank_kernel, t, o);
+}
+
+cudaError_t launch_fc_operand(const FcOperandArgs& a, cudaStream_t st, bool pdl) {
+  const long long items = static_cast<long long>(a.N) * 2 * (a.d / 8);
+  long long blocks = (items + 255) / 256;
+  if (blocks > 1216) blocks = 1216;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, fc_operand_kernel, a);
 }
 
 cudaError_t launch_lm_merge(const LmPartials& lm, int N, int k, int* ids, float* logp, float* lse,
