@@ -20,7 +20,7 @@ EAGLE_OK, EAGLE_ERR_INVALID_ARG, EAGLE_ERR_UNSUPPORTED, EAGLE_ERR_OOM, EAGLE_ERR
 DTYPE_F32, DTYPE_BF16 = 0, 1
 TREE_STATIC, TREE_DYNAMIC = 1, 2
 FEAT_F, FEAT_FUSED = 1, 3
-FLAG_NO_GRAPH, FLAG_NO_PDL, FLAG_GEMM_ONE_CTA = 1, 2, 4
+FLAG_NO_GRAPH, FLAG_NO_PDL, FLAG_GEMM_TWO_CTA = 1, 2, 4
 MAX_DEPTH = 16
 KERNEL_KINDS = 13
 DEVERR_TIMEOUT, DEVERR_PREFIX, DEVERR_TOKEN = 1, 2, 4

@@ -511,10 +511,9 @@ tree_attention_tc_kernel(const AttnArgs a) {
     }
     cp_async_commit();
   };
-#pragma unroll
-  for (int i = 0; i < TA_NST; ++i) issue(i);
   // one batch of loads in flight together: tree rows (if this CTA has the tree chunk),
-  // this warp's queries and its rows' ancestor masks
+  // this warp's queries and its rows' ancestor masks; issued before the ring's copies so
+  // that their latency overlaps the copy issue
   constexpr int PER = ATT_CHUNK * (TA_HD / 4) / ATT_THREADS;   // float4 of tree keys (and values) per thread
   float4 k4[PER], v4[PER];
   if (has_tree) {
@@ -550,6 +549,8 @@ tree_attention_tc_kernel(const AttnArgs a) {
     if (v0 < qv) w.mk0 = __ldcg(a.row_mask + row0 + v0 / gq);
     if (v1 < qv) w.mk1 = __ldcg(a.row_mask + row0 + v1 / gq);
   }
+#pragma unroll
+  for (int i = 0; i < TA_NST; ++i) issue(i);
   if (has_tree) {   // fp32 tree keys / values -> bf16 hi and lo tiles
 #pragma unroll
     for (int u = 0; u < PER; ++u) {

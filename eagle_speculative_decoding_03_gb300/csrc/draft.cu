@@ -49,7 +49,7 @@ struct eagle_draft {
   eagle_draft_config_t cfg;
   eagle_draft_weights_t w;
   bool tc = false;
-  bool use_graph = true, use_pdl = true, gemm_occ2 = true;
+  bool use_graph = true, use_pdl = true, gemm_occ2 = false;
   int D = 0, R = 0, gen = 0, S = 0, n_max = 0, k_max = 0, f_max = 0, max_nodes = 0;
   int rows[EAGLE_MAX_DEPTH], kids[EAGLE_MAX_DEPTH];
   int row_base[EAGLE_MAX_DEPTH + 1], node_base[EAGLE_MAX_DEPTH + 1];
@@ -233,7 +233,7 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
   h->tc = c.dtype == EAGLE_DTYPE_BF16;
   h->use_graph = !(c.flags & EAGLE_FLAG_NO_GRAPH);
   h->use_pdl = !(c.flags & EAGLE_FLAG_NO_PDL);
-  h->gemm_occ2 = !(c.flags & EAGLE_FLAG_GEMM_ONE_CTA);
+  h->gemm_occ2 = (c.flags & EAGLE_FLAG_GEMM_TWO_CTA) != 0;
   h->D = c.depth;
   // tree geometry
   int rb = 0, nb = 1, kmax = 0, fmax = 0, nmax_rows = 0;

@@ -1173,14 +1173,15 @@ bool plan_gemm(GemmPlan& p, int N) {
   const int topk = std::max(1, g.e.topk);
   const int lm_rows = g.e.kind == EPI_LMHEAD ? N : 0;
   // Work split.  Few tiles (the small-N projections): S CTAs per tile in a cluster, each
-  // on 1/S of K, reduced on chip; enough tiles to fill the SMs: one tile per CTA;
-  // otherwise (the LM head, very wide layers) the stream-K schedule.
+  // on 1/S of K, reduced on chip, when the clusters cover >= 80% of the SMs; enough tiles
+  // to fill the SMs: one tile per CTA; otherwise (the LM head, very wide layers, tile
+  // counts the clusters would leave SMs idle for) the stream-K schedule.
   g.csplit = 0;
   const size_t part_bytes = static_cast<size_t>(g.nrb) * g.npad * BM * sizeof(float);
   if (g.e.kind != EPI_LMHEAD && !p.stream_k) {
     int S = std::min(std::min(8, g.KB), sms / g.MT);
     while (S >= 2 && gemm_active_clusters(S) < g.MT) --S;
-    if (S >= 2 && part_bytes <= 2 * static_cast<size_t>(A_STAGE_BYTES)) {
+    if (S >= 2 && 5 * g.MT * S >= 4 * sms && part_bytes <= 2 * static_cast<size_t>(A_STAGE_BYTES)) {
       g.csplit = S;
       p.occ = 1;
     } else if (S < 2 && 4 * g.MT >= 3 * sms && g.MT <= sms * (g.b_tma ? 2 : 1)) {

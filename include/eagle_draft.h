@@ -93,8 +93,8 @@ typedef struct {
 
 #define EAGLE_FLAG_NO_GRAPH 0x1   /* enqueue the kernels directly on every call */
 #define EAGLE_FLAG_NO_PDL   0x2   /* plain stream order between kernels */
-#define EAGLE_FLAG_GEMM_ONE_CTA 0x4 /* every GEMM takes a whole SM (default: the QKV, O, gate/up and
-                                       down GEMMs run two CTAs per SM so the next one starts early) */
+#define EAGLE_FLAG_GEMM_TWO_CTA 0x4 /* stream-K GEMMs with a TMA operand run two CTAs per SM (a smaller
+                                       ring each) instead of one per SM with the full register file */
 
 /* Weights, stored [out, in] row-major in `dtype` (the norm gains are always f32).
  * w_qkv stacks the query rows, then the key rows, then the value rows.
