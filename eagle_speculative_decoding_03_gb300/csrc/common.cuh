@@ -24,6 +24,7 @@ constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;   // ~1 s at 2 GHz
 constexpr unsigned DEVERR_TIMEOUT = 0x1u;
 constexpr unsigned DEVERR_PREFIX = 0x2u;
 constexpr unsigned DEVERR_TOKEN = 0x4u;
+constexpr unsigned DEVERR_SELECT = 0x8u;
 
 // ---------------------------------------------------------- small helpers
 EAGLE_DEV uint32_t smem_u32(const void* p) {
@@ -54,6 +55,10 @@ EAGLE_DEV float warp_max(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
+
+// a value as the rankings see it: NaN ranks below everything, so a ranking stays a strict
+// order (exactly the requested number of winners) whatever the inputs hold
+EAGLE_DEV float rank_value(float v) { return v != v ? -INFINITY : v; }
 
 // total order used for every top-k of this library: larger value first, then smaller id
 EAGLE_DEV bool beats(float v, int id, float w, int wid) {

@@ -561,6 +561,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
         FcOperandArgs fo;
         fo.N = N;
         fo.d = d;
+        fo.vocab = c.vocab;
         fo.row_feat = cur.feat;
         fo.row_tok = cur.tok;
         fo.feat = s == 1 ? a_prev : nullptr;

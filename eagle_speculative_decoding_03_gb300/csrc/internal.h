@@ -135,7 +135,7 @@ cudaError_t launch_tree_init(const TreeArgs& t, const RowMeta& rows0, cudaStream
 // The feature comes from an fp32 matrix (the roots) or from the previous depth's operand
 // copy (already hi/lo); an embedding is exact in bf16 (lo = 0).
 struct FcOperandArgs {
-  int N, d;
+  int N, d, vocab;
   const int* row_feat;
   const int* row_tok;
   const float* feat;          // [*][ldf] fp32, or null

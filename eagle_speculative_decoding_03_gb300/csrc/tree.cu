@@ -82,7 +82,8 @@ __global__ void __launch_bounds__(256) fc_operand_kernel(const FcOperandArgs a) 
                          lv[6] | (uint32_t(lv[7]) << 16));
       }
     } else {
-      const int t = __ldcg(a.row_tok + n);
+      int t = __ldcg(a.row_tok + n);
+      t = (t < 0 || t >= a.vocab) ? 0 : t;   // never an address outside the table
       *hi = __ldg(reinterpret_cast<const uint4*>(a.emb + static_cast<size_t>(t) * a.d) + (c - chunks));
       *lo = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -298,6 +299,9 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
     red_m[warp] = m;
     red_s[warp] = sm;
   }
+  // a row with fewer than kids valid candidates (non-finite logits) keeps distinct
+  // out-of-range placeholders, caught below before they can index anything
+  if (tid < KMAX) sel[tid] = make_float2(-INFINITY, __int_as_float(-1 - tid));
   if (tid == 0) {
     ncand = 0;
     thr_v = -INFINITY;
@@ -366,9 +370,13 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
   const int u = s_u;
   if (tid < kids) {
     const float v = sel[tid].x;
-    const int id = __float_as_int(sel[tid].y);
+    int id = __float_as_int(sel[tid].y);
     int rank = 0;
     for (int j = 0; j < kids; ++j) rank += __float_as_int(sel[j].y) < id ? 1 : 0;
+    if (id < 0 || id >= t.vocab) {
+      atomicOr(t.err, DEVERR_SELECT);
+      id = 0;
+    }
     const int c = i * kids + rank;
     const float lp = v - s_lse;
     const float vc = s_vu + lp;
@@ -400,11 +408,11 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
   if (t.tree_kind == 1) {  // static: every child, in generation order
     for (int c = tid; c < nc2; c += EXR_THREADS) {
       spos[c] = c;
-      sv[c] = __ldcg(scratch_v + b * 256 + c);
+      sv[c] = rank_value(__ldcg(scratch_v + b * 256 + c));
     }
   } else {
     // the F best children (value, then generation index), kept in generation order
-    for (int c = tid; c < nc2; c += EXR_THREADS) sv[c] = __ldcg(scratch_v + b * 256 + c);
+    for (int c = tid; c < nc2; c += EXR_THREADS) sv[c] = rank_value(__ldcg(scratch_v + b * 256 + c));
     __syncthreads();
     for (int c = tid; c < nc2; c += EXR_THREADS) {
       const float vc = sv[c];
@@ -466,7 +474,7 @@ __global__ void __launch_bounds__(RR_THREADS) rerank_kernel(const TreeArgs t, co
   const int S = t.slots;
   // kept flags (node c = tid + 1), ranked from values staged in shared memory
   __shared__ float vals[RR_THREADS];
-  if (tid < G) vals[tid] = __ldcg(t.node_logv + nb0 + tid + 1);
+  if (tid < G) vals[tid] = rank_value(__ldcg(t.node_logv + nb0 + tid + 1));
   __syncthreads();
   int kf = 0;
   if (tid < G) {
@@ -490,7 +498,7 @@ __global__ void __launch_bounds__(RR_THREADS) rerank_kernel(const TreeArgs t, co
     __syncthreads();
   }
   if (tid == 0) slot_node[0] = 0;
-  if (tid < G && keep[tid]) slot_node[scan[tid]] = tid + 1;   // inclusive scan: slot = 1 + #kept before
+  if (tid < G && keep[tid] && scan[tid] < S) slot_node[scan[tid]] = tid + 1;   // inclusive scan: slot = 1 + #kept before
   __syncthreads();
   // parents as slots: binary search of the parent node among kept slots (sorted ids)
   if (tid < S) {

@@ -69,6 +69,8 @@ typedef enum { EAGLE_FEAT_F = 1, EAGLE_FEAT_FUSED = 3 } eagle_feat_kind_t;
 #define EAGLE_DEVERR_TIMEOUT     0x1u   /* a bounded wait inside a kernel ran out */
 #define EAGLE_DEVERR_PREFIX      0x2u   /* a request's prefix length was < 0 or > max_prefix */
 #define EAGLE_DEVERR_TOKEN       0x4u   /* a root token was outside [0, vocab) (treated as 0) */
+#define EAGLE_DEVERR_SELECT      0x8u   /* a row had fewer than k valid next-token candidates
+                                           (non-finite logits); the missing children get token 0 */
 
 typedef struct {
   int32_t d;            /* hidden size; d % 128 == 0 for bf16 weights */

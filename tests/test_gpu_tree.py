@@ -94,6 +94,23 @@ def test_out_of_range_root_token_is_reported(lib):
     assert ei.value.status == eb.EAGLE_ERR_DEVICE and "0x4" in str(ei.value)
 
 
+def test_non_finite_logits_are_reported_and_stay_in_bounds(lib):
+    # an LM head of NaNs: no row has a valid next-token candidate; the library flags it
+    # in the device error word and every emitted index stays inside its table
+    cfg = configs.get("small_dyn")
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    W["w_lm"] = np.full_like(W["w_lm"], 0x7FC0)          # bf16 quiet NaN
+    d = eb.EagleDraft(cfg, eb.device_weights(W))
+    out = {k: v.cpu().numpy() for k, v in d.tree(eb.device_inputs(I)).items()}
+    with pytest.raises(eb.EagleError) as ei:
+        d.check()
+    assert ei.value.status == eb.EAGLE_ERR_DEVICE and "0x8" in str(ei.value)
+    S = d.info["slots"]
+    assert ((out["tokens"] >= 0) & (out["tokens"] < cfg.vocab)).all()
+    assert ((out["parents"] >= -1) & (out["parents"] < S)).all()
+    assert set(np.unique(out["mask"])) <= {0, 1}
+
+
 def test_invalid_batch_rejected(lib):
     cfg = configs.get("small_dyn")
     W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
