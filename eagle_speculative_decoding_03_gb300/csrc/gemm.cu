@@ -108,7 +108,8 @@ EAGLE_DEV void compute_rstd(const BSrc& b, int N, float* rstd, int tid, int nthr
 // ==================================================================== epilogues
 // Shared-memory scratch of the 128 epilogue threads.
 struct EpiScratch {
-  float xch[16][BM];       // row-major exchange tile (rotary partners, LM-head transpose)
+  float xch[16][BM];       // row-major exchange tile (rotary partners, LM-head transpose;
+                           // STORE: the chunk's output rows before the vector stores)
   float red[4][16];        // per-warp partial sums of squares
   int meta[3][16];         // rows of the chunk: position, request, request-local slot
 };
@@ -121,11 +122,13 @@ struct EpiSmem {
   float* lv;               // [N][k] running top-k values (sorted)
   int* li;                 // [N][k] and their token ids
   float* rstd;             // [N] factored RMSNorm scale of each row (EPI_QKV / EPI_SWIGLU)
+  uint16_t* shl;            // STORE: [32][BM] operand-copy rows (hi, lo) before the vector stores
 };
 
 EAGLE_DEV EpiSmem epi_views(void* scratch, void* lm, int N, int topk) {
   EpiSmem es;
   es.s = reinterpret_cast<EpiScratch*>(scratch);
+  es.shl = reinterpret_cast<uint16_t*>(lm);   // STORE kind only (no LM-head lists then)
   float* f = reinterpret_cast<float*>(lm);
   es.st_max = f;
   es.st_sum = f + N;
@@ -307,15 +310,51 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
                     : (e.resid && n0 + i < g.N && mvalid) ? __ldcg(e.resid + static_cast<size_t>(n0 + i) * e.ldr + m) : 0.f;
     const float gam = pre_b ? pre_b[0] : (e.hl && e.hl_gamma && mvalid ? __ldg(e.hl_gamma + m) : 1.f);
     float sq[16];
+    // Rows are staged in shared memory and written with 16-byte vector stores of whole
+    // rows (a tile row is contiguous in out and in the operand copy): 8 stores per thread
+    // per chunk instead of 48 scalar ones.  Needs a full tile and 16-byte aligned rows.
+    const bool vec = g.M % BM == 0 && e.ldo % 4 == 0 && reinterpret_cast<uintptr_t>(e.out) % 16 == 0 &&
+                     (!e.hl || (e.hl_ld % 8 == 0 && reinterpret_cast<uintptr_t>(e.hl) % 16 == 0));
+    if (vec) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int n = n0 + i;
-      float val = v[i] + rv[i];
-      sq[i] = 0.f;
-      if (n < g.N && mvalid) {
-        e.out[static_cast<size_t>(n) * e.ldo + m] = val;
-        if (e.hl) write_hl(e, n, m, val, gam);
-        sq[i] = val * val;
+      for (int i = 0; i < 16; ++i) {
+        const float val = v[i] + rv[i];
+        es.s->xch[i][tl] = val;
+        sq[i] = n0 + i < g.N ? val * val : 0.f;
+        if (e.hl) {
+          uint16_t hi, lo;
+          split_hilo(val * gam, hi, lo);
+          es.shl[(2 * i) * BM + tl] = hi;
+          es.shl[(2 * i + 1) * BM + tl] = lo;
+        }
+      }
+      named_bar(1, 128);
+      const int rows = min(16, g.N - n0), m0 = mt * BM;
+      for (int idx = tl; idx < rows * (BM / 4); idx += 128) {   // out: 32 float4 per row
+        const int r = idx / (BM / 4), q = idx - r * (BM / 4);
+        *reinterpret_cast<float4*>(e.out + static_cast<size_t>(n0 + r) * e.ldo + m0 + 4 * q) =
+            *reinterpret_cast<const float4*>(&es.s->xch[r][4 * q]);
+      }
+      if (e.hl) {
+        for (int idx = tl; idx < 2 * rows * (BM / 8); idx += 128) {   // hi / lo rows: 16 uint4 per row
+          const int r = idx / (BM / 8), q = idx - r * (BM / 8);
+          const int n2 = 2 * n0 + r;   // row 2n = hi, 2n + 1 = lo
+          *reinterpret_cast<uint4*>(e.hl + static_cast<size_t>(n2) * e.hl_ld + m0 + 8 * q) =
+              *reinterpret_cast<const uint4*>(es.shl + r * BM + 8 * q);
+        }
+      }
+      named_bar(1, 128);   // the staging rows are read before the next chunk writes them
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int n = n0 + i;
+        float val = v[i] + rv[i];
+        sq[i] = 0.f;
+        if (n < g.N && mvalid) {
+          e.out[static_cast<size_t>(n) * e.ldo + m] = val;
+          if (e.hl) write_hl(e, n, m, val, gam);
+          sq[i] = val * val;
+        }
       }
     }
     if (e.ss) {
@@ -498,9 +537,13 @@ __host__ __device__ inline TcLayout tc_layout(int npad, int stages) {
   L.lm_off = L.erstd_off + sizeof(float) * 256;
   return L;
 }
-__host__ __device__ inline uint32_t tc_smem_bytes(int npad, int stages, int lm_rows, int topk) {
+// The region at lm_off holds the LM head's per-row lists, or (STORE epilogue) the
+// operand-copy staging rows.
+__host__ __device__ inline uint32_t tc_smem_bytes(int npad, int stages, int lm_rows, int topk, bool store) {
   TcLayout L = tc_layout(npad, stages);
-  return L.lm_off + static_cast<uint32_t>(lm_rows) * (3 + 2 * topk) * 4 + 1024;  // +1024: base alignment
+  uint32_t tail = static_cast<uint32_t>(lm_rows) * (3 + 2 * topk) * 4;
+  if (store && tail < 32 * BM * 2) tail = 32 * BM * 2;
+  return L.lm_off + tail + 1024;  // +1024: base alignment
 }
 
 EAGLE_DEV void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -1200,10 +1243,10 @@ bool plan_gemm(GemmPlan& p, int N) {
   uint32_t cap = static_cast<uint32_t>(g_tc_smem_cap ? g_tc_smem_cap : TC_MAX_SMEM);
   if (p.occ == 2) cap = std::min(cap, TC_SMEM_OCC2);
   int stages = 12;
-  while (stages >= 2 && tc_smem_bytes(g.npad, stages, lm_rows, topk) > cap) --stages;
+  while (stages >= 2 && tc_smem_bytes(g.npad, stages, lm_rows, topk, g.e.kind == EPI_STORE) > cap) --stages;
   if (stages < 2) return false;
   g.stages = stages;
-  p.smem = tc_smem_bytes(g.npad, stages, lm_rows, topk);
+  p.smem = tc_smem_bytes(g.npad, stages, lm_rows, topk, g.e.kind == EPI_STORE);
   if (g.b_tma) {
     // the operand copy holds 2 N rows (hi, lo); rows past them read as zero
     if (!p.b_hl || !make_act_map(&p.tmB, p.b_hl, 2 * N, g.K, 2 * g.npad)) return false;
