@@ -122,13 +122,13 @@ struct EpiSmem {
   float* lv;               // [N][k] running top-k values (sorted)
   int* li;                 // [N][k] and their token ids
   float* rstd;             // [N] factored RMSNorm scale of each row (EPI_QKV / EPI_SWIGLU)
-  uint16_t* shl;            // STORE: [32][BM] operand-copy rows (hi, lo) before the vector stores
+  uint16_t* shl;            // STORE / SWIGLU: [32][BM] operand-copy rows (hi, lo) before the vector stores
 };
 
 EAGLE_DEV EpiSmem epi_views(void* scratch, void* lm, int N, int topk) {
   EpiSmem es;
   es.s = reinterpret_cast<EpiScratch*>(scratch);
-  es.shl = reinterpret_cast<uint16_t*>(lm);   // STORE kind only (no LM-head lists then)
+  es.shl = reinterpret_cast<uint16_t*>(lm);   // STORE / SWIGLU only (no LM-head lists then)
   float* f = reinterpret_cast<float*>(lm);
   es.st_max = f;
   es.st_sum = f + N;
@@ -393,6 +393,39 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
     }
     named_bar(1, 128);
     const int partner = tl + (i < half ? half : -half);
+    if (hd == BM && g.M % BM == 0) {
+      // one head per tile: rotate, stage the rows, then 16-byte vector stores of whole
+      // head rows (q, or the request's tree K / V row)
+      float rv[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        rv[r] = vn[r];
+        if (rotate) {
+          const float p = es.s->xch[r][partner];
+          rv[r] = i < half ? vn[r] * rc[r] - p * rsn[r] : vn[r] * rc[r] + p * rsn[r];
+        }
+      }
+      named_bar(1, 128);
+#pragma unroll
+      for (int r = 0; r < 16; ++r) es.s->xch[r][tl] = rv[r];
+      named_bar(1, 128);
+      const int rows = min(16, g.N - n0);
+      for (int idx = tl; idx < rows * (BM / 4); idx += 128) {
+        const int r = idx / (BM / 4), q4 = idx - r * (BM / 4);
+        float* dst;
+        if (head < e.Hq) {
+          dst = e.q + static_cast<size_t>(n0 + r) * e.Hq * hd + static_cast<size_t>(head) * hd;
+        } else {
+          const int b = es.s->meta[1][r], slot = es.s->meta[2][r];
+          const bool isk = head < e.Hq + e.Hkv;
+          const int kvh = isk ? head - e.Hq : head - e.Hq - e.Hkv;
+          dst = (isk ? e.tk : e.tv) + ((static_cast<size_t>(b) * e.tree_rows + slot) * e.Hkv + kvh) * hd;
+        }
+        *reinterpret_cast<float4*>(dst + 4 * q4) = *reinterpret_cast<const float4*>(&es.s->xch[r][4 * q4]);
+      }
+      named_bar(1, 128);
+      return;
+    }
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int n = n0 + r;
@@ -419,6 +452,34 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
 #pragma unroll
     for (int r = 0; r < 16; ++r) es.s->xch[r][tl] = v[r];
     named_bar(1, 128);
+    if (!e.out && e.hl && e.hl_ld % 8 == 0 && reinterpret_cast<uintptr_t>(e.hl) % 16 == 0) {
+      // operand copy only: hi / lo rows staged, then 16-byte vector stores (64 columns)
+      if (tl < 64) {
+        const int j = mt * (BM / 2) + tl;
+        const float gam = e.hl_gamma ? __ldg(e.hl_gamma + j) : 1.f;
+#pragma unroll 4
+        for (int r = 0; r < 16; ++r) {
+          float gt = es.s->xch[r][tl], up = es.s->xch[r][tl + 64];
+          if (e.nss && n0 + r < g.N) {
+            gt *= es.rstd[n0 + r];
+            up *= es.rstd[n0 + r];
+          }
+          uint16_t hi, lo;
+          split_hilo(silu_f(gt) * up * gam, hi, lo);
+          es.shl[(2 * r) * BM + tl] = hi;
+          es.shl[(2 * r + 1) * BM + tl] = lo;
+        }
+      }
+      named_bar(1, 128);
+      const int rows = min(16, g.N - n0), j0 = mt * (BM / 2);
+      for (int idx = tl; idx < 2 * rows * (BM / 16); idx += 128) {   // 8 uint4 per 64-column row
+        const int r = idx / (BM / 16), q8 = idx - r * (BM / 16);
+        *reinterpret_cast<uint4*>(e.hl + static_cast<size_t>(2 * n0 + r) * e.hl_ld + j0 + 8 * q8) =
+            *reinterpret_cast<const uint4*>(es.shl + r * BM + 8 * q8);
+      }
+      named_bar(1, 128);
+      return;
+    }
     if (tl < 64) {
       const int j = mt * (BM / 2) + tl;
       const float gam = e.hl && e.hl_gamma ? __ldg(e.hl_gamma + j) : 1.f;
@@ -1243,10 +1304,11 @@ bool plan_gemm(GemmPlan& p, int N) {
   uint32_t cap = static_cast<uint32_t>(g_tc_smem_cap ? g_tc_smem_cap : TC_MAX_SMEM);
   if (p.occ == 2) cap = std::min(cap, TC_SMEM_OCC2);
   int stages = 12;
-  while (stages >= 2 && tc_smem_bytes(g.npad, stages, lm_rows, topk, g.e.kind == EPI_STORE) > cap) --stages;
+  const bool staged = g.e.kind == EPI_STORE || g.e.kind == EPI_SWIGLU;
+  while (stages >= 2 && tc_smem_bytes(g.npad, stages, lm_rows, topk, staged) > cap) --stages;
   if (stages < 2) return false;
   g.stages = stages;
-  p.smem = tc_smem_bytes(g.npad, stages, lm_rows, topk, g.e.kind == EPI_STORE);
+  p.smem = tc_smem_bytes(g.npad, stages, lm_rows, topk, staged);
   if (g.b_tma) {
     // the operand copy holds 2 N rows (hi, lo); rows past them read as zero
     if (!p.b_hl || !make_act_map(&p.tmB, p.b_hl, 2 * N, g.K, 2 * g.npad)) return false;
