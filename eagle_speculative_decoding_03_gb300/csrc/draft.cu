@@ -338,6 +338,8 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
     return fail(EAGLE_ERR_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
   }
   h->launches = 1 + (c.feat_kind == EAGLE_FEAT_FUSED ? 1 : 0) + (h->tc ? 9 : 8) * c.depth + 1;
+  if (h->tc)   // LM heads over more than 128 rows run as several launches (at max_batch)
+    for (int s = 0; s < h->D; ++s) h->launches += ceil_div(c.max_batch * h->rows[s], MAX_ROWS_PER_BLOCK) - 1;
   *out = h;
   return EAGLE_OK;
 }
@@ -450,9 +452,36 @@ static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t 
   return EAGLE_OK;
 }
 
+static LmPartials lm_partials(eagle_draft* h, int N);
+
 static eagle_status_t lm_head(eagle_draft* h, const float* a, const uint16_t* a_hl, int N, int topk,
                               cudaStream_t st) {
   const eagle_draft_config_t& c = h->cfg;
+  if (a_hl && N > MAX_ROWS_PER_BLOCK) {
+    // More rows than one TMEM accumulator pair holds: launches of <= 128 rows each, so the
+    // accumulators stay double-buffered (the top-k epilogue of one tile overlaps the next
+    // tile's MMAs); the partials of each launch land at its rows' offsets.
+    const int parts = ceil_div(N, MAX_ROWS_PER_BLOCK), per = ceil_div(N, parts);
+    const long long T = ceil_div(c.vocab, BM), G = lm_partials(h, N).G;
+    for (int r0 = 0; r0 < N; r0 += per) {
+      const int n = std::min(per, N - r0);
+      GemmPlan p = base_plan(h, h->tm_lm, nullptr, h->w.w_lm, nullptr, c.vocab, c.d, c.vocab);
+      p.args.b.mode = B_F32;
+      p.args.b.x = a + static_cast<size_t>(r0) * c.d;
+      p.args.b.ldx = c.d;
+      tma_operand(p, a_hl + 2 * static_cast<size_t>(r0) * c.d);
+      EpiArgs& e = p.args.e;
+      e.kind = EPI_LMHEAD;
+      e.lm_max = h->lm_max + r0 * T;
+      e.lm_sum = h->lm_sum + r0 * T;
+      e.lm_val = h->lm_val + r0 * G * topk;
+      e.lm_id = h->lm_id + r0 * G * topk;
+      e.topk = topk;
+      eagle_status_t r = run_gemm(h, p, n, st, EAGLE_K_LMHEAD);
+      if (r != EAGLE_OK) return r;
+    }
+    return EAGLE_OK;
+  }
   GemmPlan p = base_plan(h, h->tm_lm, nullptr, h->w.w_lm, nullptr, c.vocab, c.d, c.vocab);
   p.args.b.mode = B_F32;
   p.args.b.x = a;

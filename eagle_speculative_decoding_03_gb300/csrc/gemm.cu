@@ -1018,10 +1018,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
 
   if (g.csplit > 1) {
     // Every thread of every rank passes both cluster barriers (whatever its role did), so
-    // no rank can wait on one that left.  Rank 0 sums the ranks' partials in rank order.
+    // no rank can wait on one that left.  The 16-row chunks are dealt round-robin to the
+    // ranks; the rank of a chunk sums all ranks' partials of it in rank order.
     cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
-    const bool red = warp >= 2 && warp < 6 && cs_r == 0;
-    const bool pre_ok = red && g.N <= 16;   // one chunk of rows: its inputs load during the barrier
+    const bool red = warp >= 2 && warp < 6;
+    const bool pre_ok = red && cs_r == 0 && g.N <= 16;   // one chunk of rows: inputs load during the barrier
     const int tl = (warp & 3) * 32 + lane;
     EpiSmem es = epi_views(smem + L.epi_off, smem + L.lm_off, g.N, g.e.topk);
     es.rstd = reinterpret_cast<float*>(smem + L.erstd_off);
@@ -1029,10 +1030,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
     if (pre_ok) epilogue_prefetch(g, es, cs_t, 0, tl, pre_a, pre_b);
     cluster.sync();
     if (red) {
+      int ci = 0;   // chunk counter, for the round-robin deal
       for (int rb = 0; rb < nrb; ++rb) {
-        for (int c0 = 0; c0 < npad; c0 += 16) {
+        for (int c0 = 0; c0 < npad; c0 += 16, ++ci) {
           const int n0 = rb * npad + c0;
           if (n0 >= g.N) break;
+          if (ci % g.csplit != cs_r) continue;
           float v[16];
 #pragma unroll
           for (int r = 0; r < 16; ++r) v[r] = 0.f;
@@ -1058,7 +1061,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
         }
       }
     }
-    cluster.sync();   // the partials stay in place until rank 0 has read them
+    cluster.sync();   // the partials stay in place until every rank has read them
   }
 
   tc_fence_before();
@@ -1285,7 +1288,7 @@ bool plan_gemm(GemmPlan& p, int N) {
   if (g.e.kind != EPI_LMHEAD && !p.stream_k) {
     int S = std::min(std::min(8, g.KB), sms / g.MT);
     while (S >= 2 && gemm_active_clusters(S) < g.MT) --S;
-    if (S >= 2 && 5 * g.MT * S >= 4 * sms && part_bytes <= 2 * static_cast<size_t>(A_STAGE_BYTES)) {
+    if (S >= 2 && 5 * g.MT * S >= 4 * sms) {
       g.csplit = S;
       p.occ = 1;
     } else if (S < 2 && 4 * g.MT >= 3 * sms && g.MT <= sms * (g.b_tma ? 2 : 1)) {
@@ -1307,6 +1310,11 @@ bool plan_gemm(GemmPlan& p, int N) {
   const bool staged = g.e.kind == EPI_STORE || g.e.kind == EPI_SWIGLU;
   while (stages >= 2 && tc_smem_bytes(g.npad, stages, lm_rows, topk, staged) > cap) --stages;
   if (stages < 2) return false;
+  if (g.csplit > 1 && part_bytes > static_cast<size_t>(stages) * tc_layout(g.npad, stages).stage_bytes) {
+    // the partial tile does not fit the stage ring it is parked in: stream-K instead
+    g.csplit = 0;
+    p.grid = static_cast<int>(std::min<long long>(sms, total));
+  }
   g.stages = stages;
   p.smem = tc_smem_bytes(g.npad, stages, lm_rows, topk, staged);
   if (g.b_tma) {
