@@ -1288,7 +1288,9 @@ bool plan_gemm(GemmPlan& p, int N) {
   if (g.e.kind != EPI_LMHEAD && !p.stream_k) {
     int S = std::min(std::min(8, g.KB), sms / g.MT);
     while (S >= 2 && gemm_active_clusters(S) < g.MT) --S;
-    if (S >= 2 && 5 * g.MT * S >= 4 * sms) {
+    // (with more than one 16-row chunk the reduction tail, spread over the ranks, matters
+    // more than covering every SM with the weight stream)
+    if (S >= 2 && (5 * g.MT * S >= 4 * sms || (N > 16 && 2 * g.MT * S >= sms))) {
       g.csplit = S;
       p.occ = 1;
     } else if (S < 2 && 4 * g.MT >= 3 * sms && g.MT <= sms * (g.b_tma ? 2 : 1)) {
