@@ -733,7 +733,7 @@ cudaError_t attn_setup_attributes() {
 // clusters of `cs` CTAs the device holds at once (cached per kernel, size and smem)
 static int active_clusters(bool tc, int cs, size_t smem) {
   struct Entry { int dev, tc, cs; size_t smem; int n; };
-  static Entry cache[64];
+  static Entry cache[128];
   static int used = 0;
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
@@ -759,7 +759,7 @@ static int active_clusters(bool tc, int cs, size_t smem) {
     cudaGetLastError();
     n = 0;
   }
-  if (used < 64) cache[used++] = Entry{dev, tc ? 1 : 0, cs, smem, n};
+  if (used < 128) cache[used++] = Entry{dev, tc ? 1 : 0, cs, smem, n};
   return n;
 }
 
@@ -784,8 +784,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
   const int cmax = g_att_cluster ? g_att_cluster : 8;
   int best_cs = 0;
   long long best_cost = 0;
-  for (int cs = 1; cs <= cmax; cs *= 2) {
-    if (cs > 1 && cs / 2 >= a.max_splits) break;
+  for (int cs = 1; cs <= cmax; ++cs) {
+    if (cs > a.max_splits) break;
     const int nca = active_clusters(tc, cs, smem);
     if (nca <= 0) continue;
     const long long waves = (total + nca - 1) / nca;
