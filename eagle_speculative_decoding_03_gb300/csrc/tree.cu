@@ -216,15 +216,15 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
               const ExpandTrace tr, const int kp, int* counters, float* scratch_v, int* scratch_tok) {
   extern __shared__ float2 cand[];                 // [EXR_CAND]
   __shared__ float red_m[EXR_WARPS], red_s[EXR_WARPS];
-  __shared__ float2 heads[256];          // list heads: value, id bits (id -1: empty list)
-  __shared__ float thr_v;
-  __shared__ int thr_i;
+  __shared__ float wb_v[EXR_WARPS];
+  __shared__ int wb_i[EXR_WARPS];
   __shared__ float2 sel[KMAX];
   __shared__ int ncand;
   __shared__ float s_lse;
   __shared__ int s_last;
   __shared__ float sv[256];
   __shared__ int srank[256], spos[256];
+  __shared__ int wcount[EXR_WARPS];
   __shared__ int s_u, s_slot, s_neff;
   __shared__ float s_vu;
   __shared__ unsigned long long s_pmask[64];
@@ -285,7 +285,6 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
         lv[j] = __ldcg(lm.val + lbase + static_cast<size_t>(tid) * kp + j);
         li[j] = __ldcg(lm.id + lbase + static_cast<size_t>(tid) * kp + j);
       }
-    heads[tid] = make_float2(lv[0], __int_as_float(li[0]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -304,8 +303,6 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
   if (tid < KMAX) sel[tid] = make_float2(-INFINITY, __int_as_float(-1 - tid));
   if (tid == 0) {
     ncand = 0;
-    thr_v = -INFINITY;
-    thr_i = INT_MAX;
     s_u = r_u;
     s_vu = r_vu;
     s_slot = r_slot;
@@ -313,22 +310,35 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
   }
   if (tid < R) s_pmask[tid] = r_mask;
   __syncthreads();
-  // Pruning bound: the kids-th best list head h.  The kids best heads are distinct
-  // entries no worse than h, so every one of the row's top-kids entries is no worse
-  // than h (in the value-then-id order): only entries that h does not beat can be kept.
-  if (tid < G && li[0] >= 0) {   // rank of this list's head among the heads (branch-free)
-    const float v0 = lv[0];
-    const int i0 = li[0];
+  // Pruning bound: in each warp, the kids-th best of its lanes' list heads; then the best
+  // of those.  The kids best heads of any subset of the lists are distinct entries no
+  // worse than the subset's kids-th head, so each of the row's top-kids entries is no
+  // worse than the bound (value-then-id order): only entries the bound does not beat can
+  // be kept.  Ranks within a warp come from shuffles, not shared-memory loops.
+  {
+    float hv = -INFINITY;
+    int hid = INT_MAX;   // empty
+    if (tid < G && li[0] >= 0) {
+      hv = lv[0];
+      hid = li[0];
+    }
     int rk = 0;
 #pragma unroll 8
-    for (int c2 = 0; c2 < G; ++c2) {
-      const float2 h = heads[c2];
-      const int hi = __float_as_int(h.y);
-      rk += (hi >= 0) & ((h.x > v0) | ((h.x == v0) & (hi < i0)));
+    for (int o = 1; o < 32; ++o) {
+      const int src = (lane + o) & 31;
+      const float ov = __shfl_sync(0xffffffffu, hv, src);
+      const int oi = __shfl_sync(0xffffffffu, hid, src);
+      rk += (oi != INT_MAX) & ((ov > hv) | ((ov == hv) & (oi < hid)));
     }
-    if (rk == kids - 1) {
-      thr_v = v0;
-      thr_i = i0;
+    const int nv = __popc(__ballot_sync(0xffffffffu, hid != INT_MAX));
+    if (lane == 0) {
+      wb_v[warp] = -INFINITY;
+      wb_i[warp] = INT_MAX;
+    }
+    __syncwarp();
+    if (nv >= kids && hid != INT_MAX && rk == kids - 1) {
+      wb_v[warp] = hv;
+      wb_i[warp] = hid;
     }
   }
   if (tid == 32) {
@@ -344,8 +354,14 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
   __syncthreads();
   // ---- candidates: list entries that the bound does not beat
   if (tid < G) {
-    const float tv = thr_v;
-    const int ti = thr_i;
+    float tv = -INFINITY;
+    int ti = INT_MAX;
+#pragma unroll
+    for (int w = 0; w < EXR_WARPS; ++w)
+      if (wb_i[w] != INT_MAX && beats(wb_v[w], wb_i[w], tv, ti)) {
+        tv = wb_v[w];
+        ti = wb_i[w];
+      }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
       if (j < kp && li[j] >= 0 && !beats(tv, ti, lv[j], li[j]))
@@ -411,26 +427,63 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
       sv[c] = rank_value(__ldcg(scratch_v + b * 256 + c));
     }
   } else {
-    // the F best children (value, then generation index), kept in generation order
-    for (int c = tid; c < nc2; c += EXR_THREADS) sv[c] = rank_value(__ldcg(scratch_v + b * 256 + c));
-    __syncthreads();
-    for (int c = tid; c < nc2; c += EXR_THREADS) {
-      const float vc = sv[c];
+    // the F best children (value, then generation index), kept in generation order.
+    // nc2 <= 256 = one child per thread.  Bound: in each warp, the F-th best of its
+    // children; the best such bound.  Exact ranks only among the children the bound
+    // does not beat; positions in generation order from per-warp ballots.
+    const float vc = tid < nc2 ? rank_value(__ldcg(scratch_v + b * 256 + tid)) : -INFINITY;
+    const int idc = tid < nc2 ? tid : INT_MAX;
+    if (tid < nc2) sv[tid] = vc;
+    {
       int rk = 0;
 #pragma unroll 8
-      for (int c2 = 0; c2 < nc2; ++c2) {
-        const float w2 = sv[c2];
-        rk += (w2 > vc) | ((w2 == vc) & (c2 < c));
+      for (int o = 1; o < 32; ++o) {
+        const int src = (lane + o) & 31;
+        const float ov = __shfl_sync(0xffffffffu, vc, src);
+        const int oi = __shfl_sync(0xffffffffu, idc, src);
+        rk += (oi != INT_MAX) & ((ov > vc) | ((ov == vc) & (oi < idc)));
       }
-      srank[c] = rk;
+      const int nv = __popc(__ballot_sync(0xffffffffu, idc != INT_MAX));
+      if (lane == 0) {
+        wb_v[warp] = -INFINITY;
+        wb_i[warp] = INT_MAX;
+      }
+      __syncwarp();
+      if (nv >= F && idc != INT_MAX && rk == F - 1) {
+        wb_v[warp] = vc;
+        wb_i[warp] = idc;
+      }
     }
+    if (tid == 0) ncand = 0;
     __syncthreads();
-    for (int c = tid; c < nc2; c += EXR_THREADS) {
-      if (srank[c] >= F) continue;
-      int p = 0;
-#pragma unroll 8
-      for (int c2 = 0; c2 < c; ++c2) p += srank[c2] < F;
-      spos[p] = c;
+    float tv = -INFINITY;
+    int ti = INT_MAX;
+#pragma unroll
+    for (int w = 0; w < EXR_WARPS; ++w)
+      if (wb_i[w] != INT_MAX && beats(wb_v[w], wb_i[w], tv, ti)) {
+        tv = wb_v[w];
+        ti = wb_i[w];
+      }
+    if (idc != INT_MAX && !beats(tv, ti, vc, idc)) srank[atomicAdd(&ncand, 1)] = idc;   // candidate list
+    __syncthreads();
+    const int nc = ncand;
+    bool keep = false;
+    if (idc != INT_MAX && !beats(tv, ti, vc, idc)) {
+      int rk = 0;
+      for (int j = 0; j < nc; ++j) {
+        const int c2 = srank[j];
+        const float w2 = sv[c2];
+        rk += (w2 > vc) | ((w2 == vc) & (c2 < idc));
+      }
+      keep = rk < F;
+    }
+    const unsigned kb = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) wcount[warp] = __popc(kb);
+    __syncthreads();
+    if (keep) {
+      int p = __popc(kb & ((1u << lane) - 1u));
+      for (int w = 0; w < warp; ++w) p += wcount[w];
+      spos[p] = idc;
     }
   }
   __syncthreads();
