@@ -577,6 +577,27 @@ struct Sched {
   }
 };
 
+// Segment sg of a CTA's unit range [u0, u1) in processing order (false: no more).  With
+// `reorder`, the tiles the CTA shares with a neighbour come first (its last tile, then its
+// first) and its whole tiles last, so the cross-CTA fix-ups happen while the CTAs still
+// have work rather than at the end of the kernel.
+EAGLE_DEV bool range_segment(long long u0, long long u1, int KB, bool reorder, int sg, long long& b, long long& e) {
+  if (u1 <= u0) return false;
+  const long long ft = u0 / KB, lt = (u1 - 1) / KB;
+  if (!reorder || ft == lt) {
+    b = u0;
+    e = u1;
+    return sg == 0;
+  }
+  const bool hsplit = u0 % KB != 0, tsplit = u1 % KB != 0;
+  const long long mb = hsplit ? (ft + 1) * KB : u0, me = tsplit ? lt * KB : u1;
+  int k = 0;
+  if (tsplit && k++ == sg) { b = lt * KB; e = u1; return true; }
+  if (hsplit && k++ == sg) { b = u0; e = (ft + 1) * KB; return true; }
+  if (me > mb && k++ == sg) { b = mb; e = me; return true; }
+  return false;
+}
+
 // ============================================================ tcgen05 mainloop
 struct TcLayout {
   uint32_t stage_bytes, b_off;
@@ -626,7 +647,7 @@ constexpr uint32_t TC_SMEM_OCC2 = 113 * 1024;   // two CTAs per SM
 // accumulator column 2r + 1 holds the low-order correction of column 2r.
 // NT = TC_THREADS (converter warps present, one CTA per SM) or 7 warps (operand by TMA only;
 // MINB = 1: the whole register file, MINB = 2: two CTAs per SM).
-template <int NT, int MINB>
+template <int NT, int MINB, bool SEG>
 __global__ void __launch_bounds__(NT, MINB)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
@@ -658,6 +679,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
   const long long u1 = g.csplit > 0
                            ? static_cast<long long>(cs_t) * KB + static_cast<long long>(cs_r + 1) * KB / g.csplit
                            : sc.begin(blockIdx.x + 1);
+  const bool reorder = SEG && g.csplit == 0;   // (compiled out of the other instances)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < g.stages; ++s) {
@@ -695,27 +717,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (long long i = u0; i < u1 && ok;) {
-        const int mt = static_cast<int>(i / KB), kb0 = static_cast<int>(i % KB);
-        const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
-        const bool second = !g.a_pair && mt * BM >= g.m_split;
-        const CUtensorMap* tm = second ? &tm1 : &tm0;
-        const int mrow = g.a_pair ? mt * (BM / 2) : (second ? mt * BM - g.m_split : mt * BM);
-        for (int kb = kb0; kb < kb1 && ok; ++kb) {
-          for (int rb = 0; rb < nrb && ok; ++rb) {
-            if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
-            const uint32_t dst = sbase + stage * L.stage_bytes;
-            mbar_arrive_expect_tx(bar_full + 8 * stage, A_STAGE_BYTES);
-            if (g.a_pair) {  // rows 0-63 from map 0 (gate), rows 64-127 from map 1 (up)
-              tma_load_2d(dst, &tm0, kb * BK, mrow, bar_full + 8 * stage, pol);
-              tma_load_2d(dst + A_STAGE_BYTES / 2, &tm1, kb * BK, mrow, bar_full + 8 * stage, pol);
-            } else {
-              tma_load_2d(dst, tm, kb * BK, mrow, bar_full + 8 * stage, pol);
+      for (int sg = 0; ok; ++sg) {
+        long long s0, s1;
+        if (!range_segment(u0, u1, KB, reorder, sg, s0, s1)) break;
+        for (long long i = s0; i < s1 && ok;) {
+          const int mt = static_cast<int>(i / KB), kb0 = static_cast<int>(i % KB);
+          const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (s1 - i)));
+          const bool second = !g.a_pair && mt * BM >= g.m_split;
+          const CUtensorMap* tm = second ? &tm1 : &tm0;
+          const int mrow = g.a_pair ? mt * (BM / 2) : (second ? mt * BM - g.m_split : mt * BM);
+          for (int kb = kb0; kb < kb1 && ok; ++kb) {
+            for (int rb = 0; rb < nrb && ok; ++rb) {
+              if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
+              const uint32_t dst = sbase + stage * L.stage_bytes;
+              mbar_arrive_expect_tx(bar_full + 8 * stage, A_STAGE_BYTES);
+              if (g.a_pair) {  // rows 0-63 from map 0 (gate), rows 64-127 from map 1 (up)
+                tma_load_2d(dst, &tm0, kb * BK, mrow, bar_full + 8 * stage, pol);
+                tma_load_2d(dst + A_STAGE_BYTES / 2, &tm1, kb * BK, mrow, bar_full + 8 * stage, pol);
+              } else {
+                tma_load_2d(dst, tm, kb * BK, mrow, bar_full + 8 * stage, pol);
+              }
+              if (++stage == g.stages) { stage = 0; phase ^= 1; }
             }
-            if (++stage == g.stages) { stage = 0; phase ^= 1; }
           }
+          i += kb1 - kb0;
         }
-        i += kb1 - kb0;
       }
       if (!ok) {
         // let copies already issued land before the CTA releases its shared memory
@@ -732,30 +758,34 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
       uint32_t phase = 0;
       long long uc = 0;
       bool ok = true;
-      for (long long i = u0; i < u1 && ok; ++uc) {
-        const int kb0 = static_cast<int>(i % KB);
-        const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
-        const int ab = static_cast<int>(uc % g.nbuf);
-        const uint32_t ap = static_cast<uint32_t>((uc / g.nbuf) & 1);
-        if (!mbar_wait(bar_acce + 8 * ab, ap ^ 1, g.err, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        for (int kb = kb0; kb < kb1 && ok; ++kb) {
-          for (int rb = 0; rb < nrb; ++rb) {
-            if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t a_addr = sbase + stage * L.stage_bytes;
-            const uint32_t b_addr = a_addr + L.b_off;
-            const uint32_t d = tmem + static_cast<uint32_t>((ab * nrb + rb) * np2);
-#pragma unroll
-            for (int j = 0; j < BK / 16; ++j)
-              tc_mma_bf16(d, smem_desc_sw128(a_addr + 32 * j), smem_desc_sw128(b_addr + 32 * j), idesc,
-                          (kb > kb0 || j > 0) ? 1u : 0u);
-            tc_commit(bar_empty + 8 * stage);
-            if (++stage == g.stages) { stage = 0; phase ^= 1; }
+      for (int sg = 0; ok; ++sg) {
+        long long s0, s1;
+        if (!range_segment(u0, u1, KB, reorder, sg, s0, s1)) break;
+        for (long long i = s0; i < s1 && ok; ++uc) {
+          const int kb0 = static_cast<int>(i % KB);
+          const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (s1 - i)));
+          const int ab = static_cast<int>(uc % g.nbuf);
+          const uint32_t ap = static_cast<uint32_t>((uc / g.nbuf) & 1);
+          if (!mbar_wait(bar_acce + 8 * ab, ap ^ 1, g.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          for (int kb = kb0; kb < kb1 && ok; ++kb) {
+            for (int rb = 0; rb < nrb; ++rb) {
+              if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t a_addr = sbase + stage * L.stage_bytes;
+              const uint32_t b_addr = a_addr + L.b_off;
+              const uint32_t d = tmem + static_cast<uint32_t>((ab * nrb + rb) * np2);
+  #pragma unroll
+              for (int j = 0; j < BK / 16; ++j)
+                tc_mma_bf16(d, smem_desc_sw128(a_addr + 32 * j), smem_desc_sw128(b_addr + 32 * j), idesc,
+                            (kb > kb0 || j > 0) ? 1u : 0u);
+              tc_commit(bar_empty + 8 * stage);
+              if (++stage == g.stages) { stage = 0; phase ^= 1; }
+            }
           }
+          if (ok) tc_commit(bar_accf + 8 * ab);
+          i += kb1 - kb0;
         }
-        if (ok) tc_commit(bar_accf + 8 * ab);
-        i += kb1 - kb0;
       }
       if (!ok) {
         // let MMAs already issued finish before TMEM is released
@@ -775,19 +805,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (long long i = u0; i < u1 && ok;) {
-        const int kb0 = static_cast<int>(i % KB);
-        const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
-        for (int kb = kb0; kb < kb1 && ok; ++kb) {
-          for (int rb = 0; rb < nrb && ok; ++rb) {
-            if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
-            mbar_arrive_expect_tx(bar_full + 8 * stage, b_bytes);
-            tma_load_2d(sbase + stage * L.stage_bytes + L.b_off, &tmB, kb * BK, rb * np2, bar_full + 8 * stage,
-                        pol_b);
-            if (++stage == g.stages) { stage = 0; phase ^= 1; }
+      for (int sg = 0; ok; ++sg) {
+        long long s0, s1;
+        if (!range_segment(u0, u1, KB, reorder, sg, s0, s1)) break;
+        for (long long i = s0; i < s1 && ok;) {
+          const int kb0 = static_cast<int>(i % KB);
+          const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (s1 - i)));
+          for (int kb = kb0; kb < kb1 && ok; ++kb) {
+            for (int rb = 0; rb < nrb && ok; ++rb) {
+              if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
+              mbar_arrive_expect_tx(bar_full + 8 * stage, b_bytes);
+              tma_load_2d(sbase + stage * L.stage_bytes + L.b_off, &tmB, kb * BK, rb * np2, bar_full + 8 * stage,
+                          pol_b);
+              if (++stage == g.stages) { stage = 0; phase ^= 1; }
+            }
           }
+          i += kb1 - kb0;
         }
-        i += kb1 - kb0;
       }
       if (!ok) {
         const long long t0 = clock64();
@@ -808,40 +842,44 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (long long i = u0; i < u1 && ok;) {
-      const int kb0 = static_cast<int>(i % KB);
-      const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
-      for (int kb = kb0; kb < kb1 && ok; ++kb) {
-        const int k0 = kb * BK;
-        const bool bf = g.b.mode == B_BF16 || (g.b.mode == B_FC && k0 >= g.b.split);
-        const uint32_t rowbytes = bf ? 128u : 256u;
-        for (int rb = 0; rb < nrb; ++rb) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag));
-          if (!ok) break;
-          const int r0 = rb * npad;
-          const int rows = min(npad, g.N - r0);
-          const uint32_t bdst = sbase + stage * L.stage_bytes + L.b_off;
-          if (lane == 0) mbar_arrive_expect_tx(bar_bfull + 8 * stage, static_cast<uint32_t>(rows) * rowbytes);
-          __syncwarp();
-          for (int r = lane; r < rows; r += 32) {
-            const int n = r0 + r;
-            const void* src;
-            if (g.b.mode == B_FC) {
-              src = k0 < g.b.split
-                        ? static_cast<const void*>(g.b.x + static_cast<size_t>(s_feat[n]) * g.b.ldx + k0)
-                        : static_cast<const void*>(static_cast<const uint16_t*>(g.b.emb) +
-                                                   static_cast<size_t>(s_tok[n]) * g.b.split + (k0 - g.b.split));
-            } else if (g.b.mode == B_BF16) {
-              src = g.b.xb + static_cast<size_t>(n) * g.b.ldx + k0;
-            } else {
-              src = g.b.x + static_cast<size_t>(n) * g.b.ldx + k0;
+    for (int sg = 0; ok; ++sg) {
+      long long s0, s1;
+      if (!range_segment(u0, u1, KB, reorder, sg, s0, s1)) break;
+      for (long long i = s0; i < s1 && ok;) {
+        const int kb0 = static_cast<int>(i % KB);
+        const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (s1 - i)));
+        for (int kb = kb0; kb < kb1 && ok; ++kb) {
+          const int k0 = kb * BK;
+          const bool bf = g.b.mode == B_BF16 || (g.b.mode == B_FC && k0 >= g.b.split);
+          const uint32_t rowbytes = bf ? 128u : 256u;
+          for (int rb = 0; rb < nrb; ++rb) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag));
+            if (!ok) break;
+            const int r0 = rb * npad;
+            const int rows = min(npad, g.N - r0);
+            const uint32_t bdst = sbase + stage * L.stage_bytes + L.b_off;
+            if (lane == 0) mbar_arrive_expect_tx(bar_bfull + 8 * stage, static_cast<uint32_t>(rows) * rowbytes);
+            __syncwarp();
+            for (int r = lane; r < rows; r += 32) {
+              const int n = r0 + r;
+              const void* src;
+              if (g.b.mode == B_FC) {
+                src = k0 < g.b.split
+                          ? static_cast<const void*>(g.b.x + static_cast<size_t>(s_feat[n]) * g.b.ldx + k0)
+                          : static_cast<const void*>(static_cast<const uint16_t*>(g.b.emb) +
+                                                     static_cast<size_t>(s_tok[n]) * g.b.split + (k0 - g.b.split));
+              } else if (g.b.mode == B_BF16) {
+                src = g.b.xb + static_cast<size_t>(n) * g.b.ldx + k0;
+              } else {
+                src = g.b.x + static_cast<size_t>(n) * g.b.ldx + k0;
+              }
+              bulk_copy_g2s(bdst + 256u * r, src, rowbytes, bar_bfull + 8 * stage);
             }
-            bulk_copy_g2s(bdst + 256u * r, src, rowbytes, bar_bfull + 8 * stage);
+            if (++stage == g.stages) { stage = 0; phase ^= 1; }
           }
-          if (++stage == g.stages) { stage = 0; phase ^= 1; }
         }
+        i += kb1 - kb0;
       }
-      i += kb1 - kb0;
     }
     if (!ok) {
       const long long t0 = clock64();
@@ -861,58 +899,62 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
     bool ok = true;
     const uint32_t cbyte = (4u * lane) & 15u;
     const int chunk = lane >> 2;
-    for (long long i = u0; i < u1 && ok;) {
-      const int kb0 = static_cast<int>(i % KB);
-      const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
-      for (int kb = kb0; kb < kb1 && ok; ++kb) {
-        const int k0 = kb * BK;
-        const bool bf = g.b.mode == B_BF16 || (g.b.mode == B_FC && k0 >= g.b.split);
-        for (int rb = 0; rb < nrb; ++rb, ++it) {
-          if (it % TC_NCW == cw) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_bfull + 8 * stage, phase, g.err, abort_flag));
-            if (!ok) break;
-            float gm0 = 1.f, gm1 = 1.f;
-            if (g.b.mode == B_NORM) {
-              const float2 gg = __ldg(reinterpret_cast<const float2*>(g.b.gamma + k0) + lane);
-              gm0 = gg.x;
-              gm1 = gg.y;
-            }
-            const int r0 = rb * npad;
-            const int rows = min(npad, g.N - r0);
-            uint8_t* bs = smem + stage * L.stage_bytes + L.b_off;
-            for (int r = 0; r < rows; ++r) {
-              float x0, x1;
-              if (bf) {
-                const uint32_t w = *reinterpret_cast<const uint32_t*>(bs + 256 * r + 4 * lane);
-                x0 = __uint_as_float(w << 16);
-                x1 = __uint_as_float(w & 0xFFFF0000u);
-              } else {
-                const float2 f = *reinterpret_cast<const float2*>(bs + 256 * r + 8 * lane);
-                x0 = f.x;
-                x1 = f.y;
-              }
+    for (int sg = 0; ok; ++sg) {
+      long long s0, s1;
+      if (!range_segment(u0, u1, KB, reorder, sg, s0, s1)) break;
+      for (long long i = s0; i < s1 && ok;) {
+        const int kb0 = static_cast<int>(i % KB);
+        const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (s1 - i)));
+        for (int kb = kb0; kb < kb1 && ok; ++kb) {
+          const int k0 = kb * BK;
+          const bool bf = g.b.mode == B_BF16 || (g.b.mode == B_FC && k0 >= g.b.split);
+          for (int rb = 0; rb < nrb; ++rb, ++it) {
+            if (it % TC_NCW == cw) {
+              ok = __all_sync(0xffffffffu, mbar_wait(bar_bfull + 8 * stage, phase, g.err, abort_flag));
+              if (!ok) break;
+              float gm0 = 1.f, gm1 = 1.f;
               if (g.b.mode == B_NORM) {
-                const float rs = rstd[r0 + r];
-                x0 = x0 * rs * gm0;
-                x1 = x1 * rs * gm1;
+                const float2 gg = __ldg(reinterpret_cast<const float2*>(g.b.gamma + k0) + lane);
+                gm0 = gg.x;
+                gm1 = gg.y;
               }
-              uint16_t h0, l0, h1, l1;
-              split_hilo(x0, h0, l0);
-              split_hilo(x1, h1, l1);
-              __syncwarp();   // every lane has read row r before it is overwritten
-              *reinterpret_cast<uint32_t*>(bs + sw128_offset(2 * r, chunk) + cbyte) =
-                  static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
-              *reinterpret_cast<uint32_t*>(bs + sw128_offset(2 * r + 1, chunk) + cbyte) =
-                  static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+              const int r0 = rb * npad;
+              const int rows = min(npad, g.N - r0);
+              uint8_t* bs = smem + stage * L.stage_bytes + L.b_off;
+              for (int r = 0; r < rows; ++r) {
+                float x0, x1;
+                if (bf) {
+                  const uint32_t w = *reinterpret_cast<const uint32_t*>(bs + 256 * r + 4 * lane);
+                  x0 = __uint_as_float(w << 16);
+                  x1 = __uint_as_float(w & 0xFFFF0000u);
+                } else {
+                  const float2 f = *reinterpret_cast<const float2*>(bs + 256 * r + 8 * lane);
+                  x0 = f.x;
+                  x1 = f.y;
+                }
+                if (g.b.mode == B_NORM) {
+                  const float rs = rstd[r0 + r];
+                  x0 = x0 * rs * gm0;
+                  x1 = x1 * rs * gm1;
+                }
+                uint16_t h0, l0, h1, l1;
+                split_hilo(x0, h0, l0);
+                split_hilo(x1, h1, l1);
+                __syncwarp();   // every lane has read row r before it is overwritten
+                *reinterpret_cast<uint32_t*>(bs + sw128_offset(2 * r, chunk) + cbyte) =
+                    static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+                *reinterpret_cast<uint32_t*>(bs + sw128_offset(2 * r + 1, chunk) + cbyte) =
+                    static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_full + 8 * stage);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_full + 8 * stage);
+            if (++stage == g.stages) { stage = 0; phase ^= 1; }
           }
-          if (++stage == g.stages) { stage = 0; phase ^= 1; }
         }
+        i += kb1 - kb0;
       }
-      i += kb1 - kb0;
     }
   } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------ epilogue (warps 2-5)
@@ -927,91 +969,95 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
     const int rows_total = nrb * npad;
     long long uc = 0;
     bool ok = true;
-    for (long long i = u0; i < u1 && ok; ++uc) {
-      const int mt = static_cast<int>(i / KB), kb0 = static_cast<int>(i % KB);
-      const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (u1 - i)));
-      const int ab = static_cast<int>(uc % g.nbuf);
-      const uint32_t ap = static_cast<uint32_t>((uc / g.nbuf) & 1);
-      ok = epi_all(mbar_wait(bar_accf + 8 * ab, ap, g.err, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      const bool complete = kb0 == 0 && kb1 == KB;
-      const int slot = (i == u0) ? 0 : 1;   // the CTA's first unit or its last
-      float* mypart = g.part + (static_cast<size_t>(blockIdx.x) * 2 + slot) * rows_total * BM;
-      for (int rb = 0; rb < nrb; ++rb) {
-        for (int c0 = 0; c0 < npad; c0 += 16) {
-          const int n0 = rb * npad + c0;
-          if (n0 >= g.N) break;
-          const uint32_t col = static_cast<uint32_t>((ab * nrb + rb) * np2 + 2 * c0);
-          float c[32], v[16];
-          __syncwarp();
-          tmem_ld16(tmem + lane_base + col, c);
-          tmem_ld16(tmem + lane_base + col + 16, c + 16);
-          tmem_wait_ld();
-#pragma unroll
-          for (int r = 0; r < 16; ++r) v[r] = c[2 * r] + c[2 * r + 1];
-          if (complete) {
-            epilogue_chunk(g, es, mt, n0, v, tl);
-          } else if (g.csplit > 1) {   // this rank's partial, in its (now idle) stage ring
-            float* cpart = reinterpret_cast<float*>(smem);
-#pragma unroll
-            for (int r = 0; r < 16; ++r) cpart[static_cast<size_t>(n0 + r) * BM + tl] = v[r];
-          } else {
-#pragma unroll
-            for (int r = 0; r < 16; ++r) mypart[static_cast<size_t>(n0 + r) * BM + tl] = v[r];
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
-      if (!complete && g.csplit == 0) {
-        __threadfence();
-        named_bar(1, 128);
-        const int cf = sc.owner(static_cast<long long>(mt) * KB);
-        const int cl = sc.owner(static_cast<long long>(mt + 1) * KB - 1);
-        if (tl == 0) {
-          const int old = atomicAdd(g.counters + mt, 1);
-          *last_flag = (old == cl - cf);
-        }
-        named_bar(1, 128);
-        if (*last_flag) {
-          __threadfence();
-          if (tl == 0) g.counters[mt] = 0;
-          for (int rb = 0; rb < nrb; ++rb) {
-            for (int c0 = 0; c0 < npad; c0 += 16) {
-              const int n0 = rb * npad + c0;
-              if (n0 >= g.N) break;
-              // partials summed in CTA order; loads of up to 4 segments issued together
-              float v[16];
-#pragma unroll
-              for (int r = 0; r < 16; ++r) v[r] = 0.f;
-              for (int c0 = cf; c0 <= cl; c0 += 4) {
-                float pv[4][16];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  const int c = c0 + u;
-                  if (c <= cl) {
-                    const int sl = (sc.begin(c) / KB == mt) ? 0 : 1;
-                    const float* p = g.part + (static_cast<size_t>(c) * 2 + sl) * rows_total * BM;
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) pv[u][r] = __ldcg(p + static_cast<size_t>(n0 + r) * BM + tl);
-                  }
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                  if (c0 + u <= cl) {
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) v[r] += pv[u][r];
-                  }
-              }
+    for (int sg = 0; ok; ++sg) {
+      long long s0, s1;
+      if (!range_segment(u0, u1, KB, reorder, sg, s0, s1)) break;
+      for (long long i = s0; i < s1 && ok; ++uc) {
+        const int mt = static_cast<int>(i / KB), kb0 = static_cast<int>(i % KB);
+        const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (s1 - i)));
+        const int ab = static_cast<int>(uc % g.nbuf);
+        const uint32_t ap = static_cast<uint32_t>((uc / g.nbuf) & 1);
+        ok = epi_all(mbar_wait(bar_accf + 8 * ab, ap, g.err, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const bool complete = kb0 == 0 && kb1 == KB;
+        const int slot = (mt == u0 / KB) ? 0 : 1;   // the CTA's first tile or its last
+        float* mypart = g.part + (static_cast<size_t>(blockIdx.x) * 2 + slot) * rows_total * BM;
+        for (int rb = 0; rb < nrb; ++rb) {
+          for (int c0 = 0; c0 < npad; c0 += 16) {
+            const int n0 = rb * npad + c0;
+            if (n0 >= g.N) break;
+            const uint32_t col = static_cast<uint32_t>((ab * nrb + rb) * np2 + 2 * c0);
+            float c[32], v[16];
+            __syncwarp();
+            tmem_ld16(tmem + lane_base + col, c);
+            tmem_ld16(tmem + lane_base + col + 16, c + 16);
+            tmem_wait_ld();
+  #pragma unroll
+            for (int r = 0; r < 16; ++r) v[r] = c[2 * r] + c[2 * r + 1];
+            if (complete) {
               epilogue_chunk(g, es, mt, n0, v, tl);
+            } else if (g.csplit > 1) {   // this rank's partial, in its (now idle) stage ring
+              float* cpart = reinterpret_cast<float*>(smem);
+  #pragma unroll
+              for (int r = 0; r < 16; ++r) cpart[static_cast<size_t>(n0 + r) * BM + tl] = v[r];
+            } else {
+  #pragma unroll
+              for (int r = 0; r < 16; ++r) mypart[static_cast<size_t>(n0 + r) * BM + tl] = v[r];
             }
           }
         }
-        named_bar(1, 128);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
+        if (!complete && g.csplit == 0) {
+          __threadfence();
+          named_bar(1, 128);
+          const int cf = sc.owner(static_cast<long long>(mt) * KB);
+          const int cl = sc.owner(static_cast<long long>(mt + 1) * KB - 1);
+          if (tl == 0) {
+            const int old = atomicAdd(g.counters + mt, 1);
+            *last_flag = (old == cl - cf);
+          }
+          named_bar(1, 128);
+          if (*last_flag) {
+            __threadfence();
+            if (tl == 0) g.counters[mt] = 0;
+            for (int rb = 0; rb < nrb; ++rb) {
+              for (int c0 = 0; c0 < npad; c0 += 16) {
+                const int n0 = rb * npad + c0;
+                if (n0 >= g.N) break;
+                // partials summed in CTA order; loads of up to 4 segments issued together
+                float v[16];
+  #pragma unroll
+                for (int r = 0; r < 16; ++r) v[r] = 0.f;
+                for (int c0 = cf; c0 <= cl; c0 += 4) {
+                  float pv[4][16];
+  #pragma unroll
+                  for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + u;
+                    if (c <= cl) {
+                      const int sl = (sc.begin(c) / KB == mt) ? 0 : 1;
+                      const float* p = g.part + (static_cast<size_t>(c) * 2 + sl) * rows_total * BM;
+  #pragma unroll
+                      for (int r = 0; r < 16; ++r) pv[u][r] = __ldcg(p + static_cast<size_t>(n0 + r) * BM + tl);
+                    }
+                  }
+  #pragma unroll
+                  for (int u = 0; u < 4; ++u)
+                    if (c0 + u <= cl) {
+  #pragma unroll
+                      for (int r = 0; r < 16; ++r) v[r] += pv[u][r];
+                    }
+                }
+                epilogue_chunk(g, es, mt, n0, v, tl);
+              }
+            }
+          }
+          named_bar(1, 128);
+        }
+        i += kb1 - kb0;
       }
-      i += kb1 - kb0;
     }
     if (g.e.kind == EPI_LMHEAD) lmhead_flush(g, es, blockIdx.x, tl);
   }
@@ -1244,7 +1290,7 @@ int gemm_active_clusters(int S) {
   cfg.blockDim = dim3(TC_THREADS, 1, 1);
   cfg.dynamicSmemBytes = g_tc_smem_cap ? g_tc_smem_cap : 200 * 1024;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<TC_THREADS, 1>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<TC_THREADS, 1, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -1329,11 +1375,13 @@ bool plan_gemm(GemmPlan& p, int N) {
 }
 
 cudaError_t gemm_setup_attributes() {
-  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS, 1>), &g_tc_smem_cap);
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS, 1, false>), &g_tc_smem_cap);
   if (e != cudaSuccess) return e;
-  e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS_TMA, 2>));
+  e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS_TMA, 2, false>));
   if (e != cudaSuccess) return e;
-  e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS_TMA, 1>));
+  e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS_TMA, 1, false>));
+  if (e != cudaSuccess) return e;
+  e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS_TMA, 1, true>));
   if (e != cudaSuccess) return e;
   return allow_max_smem(reinterpret_cast<const void*>(gemm_simt_kernel), &g_simt_smem_cap);
 }
@@ -1355,14 +1403,16 @@ cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t st, bool pdl) {
     cfg.gridDim = dim3(p.grid, 1, 1);
     if (p.occ == 2) {
       cfg.blockDim = dim3(TC_THREADS_TMA, 1, 1);
-      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 2>, p.tm0, p.tm1, p.tmB, p.args);
+      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 2, false>, p.tm0, p.tm1, p.tmB, p.args);
     }
     if (p.args.b_tma) {   // no converter warps: the full register file for 7 warps
       cfg.blockDim = dim3(TC_THREADS_TMA, 1, 1);
-      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 1>, p.tm0, p.tm1, p.tmB, p.args);
+      if (p.args.e.kind == EPI_LMHEAD && p.args.N <= 16)   // stream-K with the split tiles first
+        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 1, true>, p.tm0, p.tm1, p.tmB, p.args);
+      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 1, false>, p.tm0, p.tm1, p.tmB, p.args);
     }
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS, 1>, p.tm0, p.tm1, p.tmB, p.args);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS, 1, false>, p.tm0, p.tm1, p.tmB, p.args);
   }
   cfg.gridDim = dim3(p.grid, p.grid_y, 1);
   cfg.blockDim = dim3(256, 1, 1);
