@@ -516,6 +516,11 @@ constexpr int RR_THREADS = 1024;
 __global__ void __launch_bounds__(RR_THREADS) rerank_kernel(const TreeArgs t, const OutArgs o) {
   __shared__ int keep[RR_THREADS];
   __shared__ int scan[RR_THREADS];
+  __shared__ float vals[RR_THREADS];        // node tid + 1: value as ranked
+  __shared__ int npar[RR_THREADS];          // node tid + 1: parent node
+  __shared__ int slot_of[RR_THREADS + 1];   // node -> kept slot (-1: not kept)
+  __shared__ int ntok[RR_THREADS + 1], ndep[RR_THREADS + 1];
+  __shared__ float nlogv[RR_THREADS + 1];
   __shared__ int slot_node[64];
   __shared__ int slot_par[64];
   __shared__ unsigned long long anc[64];
@@ -523,12 +528,23 @@ __global__ void __launch_bounds__(RR_THREADS) rerank_kernel(const TreeArgs t, co
   pdl_trigger();
   const int b = blockIdx.x, tid = threadIdx.x;
   const size_t nb0 = static_cast<size_t>(b) * t.max_nodes;
-  const int G = t.node_base[t.depth] - 1;     // generated nodes: ids 1..G
+  const int G = t.node_base[t.depth] - 1;     // generated nodes: ids 1..G (node 0: the root)
   const int S = t.slots;
-  // kept flags (node c = tid + 1), ranked from values staged in shared memory
-  __shared__ float vals[RR_THREADS];
-  if (tid < G) vals[tid] = rank_value(__ldcg(t.node_logv + nb0 + tid + 1));
+  // one batch of loads: every node's value, parent, token and depth, and the prefix length
+  for (int c = tid; c <= G; c += RR_THREADS) {   // G + 1 <= 1025 nodes
+    const float lv = __ldcg(t.node_logv + nb0 + c);
+    nlogv[c] = lv;
+    ntok[c] = __ldcg(t.node_tok + nb0 + c);
+    ndep[c] = __ldcg(t.node_depth + nb0 + c);
+    slot_of[c] = -1;
+    if (c >= 1) {
+      vals[c - 1] = rank_value(lv);
+      npar[c - 1] = __ldcg(t.node_parent + nb0 + c);
+    }
+  }
+  const int neff = __ldcg(t.n_eff + b);
   __syncthreads();
+  // kept flags (node c = tid + 1): static trees keep every node, dynamic ones the m best
   int kf = 0;
   if (tid < G) {
     const int c = tid + 1;
@@ -537,7 +553,11 @@ __global__ void __launch_bounds__(RR_THREADS) rerank_kernel(const TreeArgs t, co
     } else {
       const float vc = vals[tid];
       int rk = 0;
-      for (int c2 = 1; c2 <= G; ++c2) rk += beats(vals[c2 - 1], c2, vc, c) ? 1 : 0;
+#pragma unroll 8
+      for (int c2 = 1; c2 <= G; ++c2) {
+        const float w = vals[c2 - 1];
+        rk += (w > vc) | ((w == vc) & (c2 < c));
+      }
       kf = rk < t.m;
     }
   }
@@ -550,33 +570,33 @@ __global__ void __launch_bounds__(RR_THREADS) rerank_kernel(const TreeArgs t, co
     scan[tid] += add;
     __syncthreads();
   }
-  if (tid == 0) slot_node[0] = 0;
-  if (tid < G && keep[tid] && scan[tid] < S) slot_node[scan[tid]] = tid + 1;   // inclusive scan: slot = 1 + #kept before
+  if (tid == 0) {
+    slot_node[0] = 0;
+    slot_of[0] = 0;
+  }
+  if (tid < G && keep[tid] && scan[tid] < S) {   // inclusive scan: slot = 1 + #kept before
+    slot_node[scan[tid]] = tid + 1;
+    slot_of[tid + 1] = scan[tid];
+  }
   __syncthreads();
-  // parents as slots: binary search of the parent node among kept slots (sorted ids)
+  // emitted slots in generation order; parents as slots (a kept node's parent is kept:
+  // V never increases along a path and a parent precedes its children in the tie order)
   if (tid < S) {
     const int c = slot_node[tid];
-    int ps = -1;
-    if (tid > 0) {
-      const int p = __ldcg(t.node_parent + nb0 + c);
-      int lo = 0, hi = S - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (slot_node[mid] < p) lo = mid + 1; else hi = mid;
-      }
-      ps = slot_node[lo] == p ? lo : -1;
-    }
+    const int ps = tid > 0 ? slot_of[npar[c - 1]] : -1;
     slot_par[tid] = ps;
     const size_t ob = static_cast<size_t>(b) * S + tid;
-    o.tokens[ob] = __ldcg(t.node_tok + nb0 + c);
+    o.tokens[ob] = ntok[c];
     o.parents[ob] = ps;
-    o.positions[ob] = __ldcg(t.n_eff + b) + __ldcg(t.node_depth + nb0 + c);
-    o.logv[ob] = __ldcg(t.node_logv + nb0 + c);
+    o.positions[ob] = neff + ndep[c];
+    o.logv[ob] = nlogv[c];
     if (o.final_nodes) o.final_nodes[ob] = c;
   }
   __syncthreads();
-  if (tid == 0) {
-    for (int i = 0; i < S; ++i) anc[i] = (i == 0 || slot_par[i] < 0 ? 0ull : anc[slot_par[i]]) | (1ull << i);
+  if (tid < S) {   // ancestor-or-self bits: walk the slot's parent chain
+    unsigned long long a = 0ull;
+    for (int j = tid, step = 0; j >= 0 && step < 64; j = slot_par[j], ++step) a |= 1ull << j;
+    anc[tid] = a;
   }
   __syncthreads();
   for (int idx = tid; idx < S * S; idx += RR_THREADS) {
