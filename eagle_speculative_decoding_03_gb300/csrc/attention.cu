@@ -484,9 +484,10 @@ tree_attention_tc_kernel(const AttnArgs a) {
   float* lst = mst + 4 * TA_MAX_QV;
   const uint32_t ring_u = smem_u32(ring), tree_u = smem_u32(trees);
 
-  pdl_wait();
-  pdl_trigger();
-  const int nb = __ldcg(a.n_eff + b);
+  // The prefix keys and values are inputs of the draft step that none of its kernels
+  // write, so the ring's first stages are issued before the wait on the previous kernel;
+  // the prefix length is clamped here the way the roots kernel clamps (and reports) it.
+  const int nb = min(max(__ldg(a.cu_seqlens + b + 1) - __ldg(a.cu_seqlens + b), 0), a.max_prefix);
   const int npre = (nb + ATT_CHUNK - 1) / ATT_CHUNK;
   const int row0 = b * a.rows_per_req;
   const size_t kv_ld = static_cast<size_t>(a.Hkv) * TA_HD;
@@ -511,9 +512,12 @@ tree_attention_tc_kernel(const AttnArgs a) {
     }
     cp_async_commit();
   };
+#pragma unroll
+  for (int i = 0; i < TA_NST; ++i) issue(i);
+  pdl_wait();
+  pdl_trigger();
   // one batch of loads in flight together: tree rows (if this CTA has the tree chunk),
-  // this warp's queries and its rows' ancestor masks; issued before the ring's copies so
-  // that their latency overlaps the copy issue
+  // this warp's queries and its rows' ancestor masks (all written by the previous kernels)
   constexpr int PER = ATT_CHUNK * (TA_HD / 4) / ATT_THREADS;   // float4 of tree keys (and values) per thread
   float4 k4[PER], v4[PER];
   if (has_tree) {
@@ -549,8 +553,6 @@ tree_attention_tc_kernel(const AttnArgs a) {
     if (v0 < qv) w.mk0 = __ldcg(a.row_mask + row0 + v0 / gq);
     if (v1 < qv) w.mk1 = __ldcg(a.row_mask + row0 + v1 / gq);
   }
-#pragma unroll
-  for (int i = 0; i < TA_NST; ++i) issue(i);
   if (has_tree) {   // fp32 tree keys / values -> bf16 hi and lo tiles
 #pragma unroll
     for (int u = 0; u < PER; ++u) {

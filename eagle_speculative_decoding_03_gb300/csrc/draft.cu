@@ -664,6 +664,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       a.cache_bf16 = h->tc ? 1 : 0;
       a.cu_seqlens = in->cu_seqlens;
       a.n_eff = h->n_eff;
+      a.max_prefix = c.max_prefix;
       a.tk = h->tk;
       a.tv = h->tv;
       a.row_mask = cur.mask;

@@ -754,6 +754,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(BM, np2);
+      // Stage 0's operand descriptors; a stage or a 16-wide K step only moves the start
+      // address field (bits 0-13, in 16-byte units, far from carrying), so the loop adds.
+      const uint64_t adesc0 = smem_desc_sw128(sbase), bdesc0 = smem_desc_sw128(sbase + L.b_off);
+      const uint64_t dstep = L.stage_bytes >> 4;
       int stage = 0;
       uint32_t phase = 0;
       long long uc = 0;
@@ -772,13 +776,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
             for (int rb = 0; rb < nrb; ++rb) {
               if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag)) { ok = false; break; }
               tc_fence_after();
-              const uint32_t a_addr = sbase + stage * L.stage_bytes;
-              const uint32_t b_addr = a_addr + L.b_off;
               const uint32_t d = tmem + static_cast<uint32_t>((ab * nrb + rb) * np2);
+              const uint64_t ad = adesc0 + stage * dstep, bd = bdesc0 + stage * dstep;
   #pragma unroll
-              for (int j = 0; j < BK / 16; ++j)
-                tc_mma_bf16(d, smem_desc_sw128(a_addr + 32 * j), smem_desc_sw128(b_addr + 32 * j), idesc,
-                            (kb > kb0 || j > 0) ? 1u : 0u);
+              for (int j = 0; j < BK / 16; ++j)   // 16 bf16 of K = 32 bytes = 2 descriptor units
+                tc_mma_bf16(d, ad + 2 * j, bd + 2 * j, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
               tc_commit(bar_empty + 8 * stage);
               if (++stage == g.stages) { stage = 0; phase ^= 1; }
             }
@@ -1334,9 +1336,14 @@ bool plan_gemm(GemmPlan& p, int N) {
   if (g.e.kind != EPI_LMHEAD && !p.stream_k) {
     int S = std::min(std::min(8, g.KB), sms / g.MT);
     while (S >= 2 && gemm_active_clusters(S) < g.MT) --S;
-    // (with more than one 16-row chunk the reduction tail, spread over the ranks, matters
-    // more than covering every SM with the weight stream)
-    if (S >= 2 && (5 * g.MT * S >= 4 * sms || (N > 16 && 2 * g.MT * S >= sms))) {
+    // Long K (fc's 2d, the FFN's d_ff) with one row block stays on stream-K: its CTAs start
+    // on each SM as the previous kernel's CTAs retire, while a cluster waits for S free SMs
+    // at once, and the on-chip reduction saves little against so long a weight stream.  With
+    // two or more row blocks the stream-K partial tiles double and the accumulator loses its
+    // second buffer, so the clusters win there.  (With more than one 16-row chunk the
+    // reduction tail, spread over the ranks, matters more than covering every SM with the
+    // weight stream.)
+    if (S >= 2 && (g.K < 8192 || g.nrb > 1) && (5 * g.MT * S >= 4 * sms || (N > 16 && 2 * g.MT * S >= sms))) {
       g.csplit = S;
       p.occ = 1;
     } else if (S < 2 && 4 * g.MT >= 3 * sms && g.MT <= sms * (g.b_tma ? 2 : 1)) {

@@ -42,6 +42,7 @@ struct AttnArgs {
   int cache_bf16;
   const int* cu_seqlens;    // [B+1]
   const int* n_eff;         // [B] validated prefix lengths
+  int max_prefix;           // cu_seqlens lengths are clamped to [0, max_prefix]
   const float* tk;          // [B][tree_rows][Hkv][hd] rotated keys of tree rows
   const float* tv;
   const unsigned long long* row_mask;  // [N] ancestor-or-self bits over request-local rows

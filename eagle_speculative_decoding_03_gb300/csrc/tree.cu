@@ -52,8 +52,11 @@ __global__ void tree_init_kernel(const TreeArgs t, const RowMeta r0) {
 // One item = 8 consecutive columns of one row: a feature chunk (copied hi/lo, or split
 // from fp32) or an embedding chunk (hi = the bf16 value, lo = 0).
 __global__ void __launch_bounds__(256) fc_operand_kernel(const FcOperandArgs a) {
-  pdl_wait();
+  // Trigger first: the fc GEMM that follows launches now and streams its weights while
+  // this kernel still waits for the frontier; it reads this kernel's rows only after its
+  // own wait.
   pdl_trigger();
+  pdl_wait();
   const int chunks = a.d / 8;
   const long long total = static_cast<long long>(a.N) * 2 * chunks;
   const size_t ld = 2 * static_cast<size_t>(a.d);
@@ -683,7 +686,9 @@ cudaError_t launch_rerank(const TreeArgs& t, const OutArgs& o, cudaStream_t st, 
 cudaError_t launch_fc_operand(const FcOperandArgs& a, cudaStream_t st, bool pdl) {
   const long long items = static_cast<long long>(a.N) * 2 * (a.d / 8);
   long long blocks = (items + 255) / 256;
-  if (blocks > 1216) blocks = 1216;
+  // at most two CTAs per SM: all of them fit beside the LM head's CTAs at once, so they
+  // all reach the trigger while the LM head runs
+  if (blocks > 2 * num_sms()) blocks = 2 * num_sms();
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, fc_operand_kernel, a);
