@@ -686,9 +686,7 @@ cudaError_t launch_rerank(const TreeArgs& t, const OutArgs& o, cudaStream_t st, 
 cudaError_t launch_fc_operand(const FcOperandArgs& a, cudaStream_t st, bool pdl) {
   const long long items = static_cast<long long>(a.N) * 2 * (a.d / 8);
   long long blocks = (items + 255) / 256;
-  // at most two CTAs per SM: all of them fit beside the LM head's CTAs at once, so they
-  // all reach the trigger while the LM head runs
-  if (blocks > 2 * num_sms()) blocks = 2 * num_sms();
+  if (blocks > 1216) blocks = 1216;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, fc_operand_kernel, a);
