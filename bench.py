@@ -196,6 +196,22 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------------- replicas (one per rank)
+def max_over_ranks(ms, dist, device="cuda"):
+    """The slowest rank's time, on every rank (one all-reduce; the identity on one rank)."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_rank, ms):
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------- our arm
 def time_trees(d, dI, out, stream, steps, warmup, dist, clock_id=None):
     import torch
@@ -215,11 +231,7 @@ def time_trees(d, dI, out, stream, steps, warmup, dist, clock_id=None):
     if dist:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
-    ms = e0.elapsed_time(e1) / steps
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, dist)
     d.check()
     return ms, clocks
 
@@ -249,7 +261,7 @@ def run_ours(args):
 
     # ---- device-timed tree (graph replay, inputs resident in HBM)
     ms, clocks = time_trees(d, dI, out, stream, args.steps, args.warmup, dist, gpu_uuid(local))
-    value = world * nodes_per_tree / (ms * 1e-3)
+    value = job_throughput(world, nodes_per_tree, ms)
     n_prefix = int(I["cu_seqlens"][-1])
     rows = [B * cfg.rows_at(s) for s in range(1, cfg.depth + 1)]
     algo, wbytes, kvbytes = algorithmic_bytes(cfg, n_prefix, rows)
@@ -297,12 +309,8 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * nodes_per_tree / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist)
+    e2e = {"value": job_throughput(world, nodes_per_tree, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     # ---- the same head at B=32 (batched serving), sharing the weights
@@ -322,7 +330,7 @@ def run_ours(args):
             d4.tree(dI4, out=out4, stream=stream)
         p4 = d4.profile_read()
         d4.profile(False)
-        b32 = {"workload": "eagle2_b32", "value": world * c4.B * c4.kept_per_request() / (ms4 * 1e-3),
+        b32 = {"workload": "eagle2_b32", "value": job_throughput(world, c4.B * c4.kept_per_request(), ms4),
                "unit": UNIT, "ms_per_step": ms4, "us_per_draft_step": ms4 * 1e3 / c4.depth,
                "hbm_frac_step": algo4 / (ms4 * 1e-3) / 1e9 / peak,
                "kernels_ms_per_tree": {k: v[0] / 3 for k, v in p4.items()}}
