@@ -119,6 +119,12 @@ SMALL = {
         name="small_fused", d=512, n_heads=8, n_kv_heads=2, head_dim=128, d_ff=1024, vocab=3072,
         rms_eps=1e-6, rope_theta=5e5, dtype="bf16", tree="dynamic", depth=4, k=5, m=12,
         feat="fused", B=2, prefix=(200, 200), seed=2003, gamma_jitter=0.1),
+    # the largest tree the boundary takes: k = 16, 16 rows x 16 children = 256 candidates per
+    # request at each depth, 49 rows per request (one 64-bit row mask), m + 1 = 64 slots
+    "small_max": DraftConfig(
+        name="small_max", d=256, n_heads=2, n_kv_heads=1, head_dim=128, d_ff=640, vocab=2048,
+        rms_eps=1e-6, rope_theta=1e4, dtype="bf16", tree="dynamic", depth=4, k=16, m=63,
+        B=2, prefix=(1, 90), seed=2005, gamma_jitter=0.1),
     "small_f32": DraftConfig(
         name="small_f32", d=192, n_heads=3, n_kv_heads=1, head_dim=64, d_ff=400, vocab=700,
         rms_eps=1e-6, rope_theta=1e4, dtype="f32", tree="dynamic", depth=3, k=3, m=7,
