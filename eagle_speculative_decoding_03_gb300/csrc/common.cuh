@@ -284,6 +284,8 @@ struct GemmArgs {
   int tmem_cols;           // allocated TMEM columns
   int nbuf;                // accumulator buffers in TMEM (2 = epilogue overlaps next unit)
   int stages;
+  int kpair;               // 1: two consecutive K blocks per pipeline stage (TMA operand only),
+                           // so one barrier round trip and one issue loop pass cover 8 MMAs
   int csplit;              // 0: stream-K over (tile, K block) units; S >= 1: S CTAs per tile (a
                            // cluster when S > 1) on consecutive K ranges, reduced through DSMEM
   BSrc b;

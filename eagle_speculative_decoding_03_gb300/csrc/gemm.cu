@@ -606,10 +606,12 @@ struct TcLayout {
 
 // Shared memory of gemm_tc_kernel: [stages x (A tile 16 KB | B tile npad*256 B)] |
 // mbarriers | misc words | gathered row indices | epilogue scratch | rstd | LM-head lists.
-__host__ __device__ inline TcLayout tc_layout(int npad, int stages) {
+// With kpair a stage holds two K blocks: [A(kb) | A(kb+1) | B(kb) | B(kb+1)].
+__host__ __device__ inline TcLayout tc_layout(int npad, int stages, int kpair = 0) {
   TcLayout L;
-  L.b_off = A_STAGE_BYTES;
-  L.stage_bytes = A_STAGE_BYTES + npad * 256;
+  const uint32_t kp = kpair ? 2u : 1u;
+  L.b_off = kp * A_STAGE_BYTES;
+  L.stage_bytes = kp * (A_STAGE_BYTES + npad * 256);
   L.bar_off = L.stage_bytes * stages;
   L.misc_off = L.bar_off + (3 * stages + 4) * 8;
   L.idx_off = (L.misc_off + 64 + 15) & ~15u;
@@ -621,8 +623,9 @@ __host__ __device__ inline TcLayout tc_layout(int npad, int stages) {
 }
 // The region at lm_off holds the LM head's per-row lists, or (STORE epilogue) the
 // operand-copy staging rows.
-__host__ __device__ inline uint32_t tc_smem_bytes(int npad, int stages, int lm_rows, int topk, bool store) {
-  TcLayout L = tc_layout(npad, stages);
+__host__ __device__ inline uint32_t tc_smem_bytes(int npad, int stages, int lm_rows, int topk, bool store,
+                                                  int kpair = 0) {
+  TcLayout L = tc_layout(npad, stages, kpair);
   uint32_t tail = static_cast<uint32_t>(lm_rows) * (3 + 2 * topk) * 4;
   if (store && tail < 32 * BM * 2) tail = 32 * BM * 2;
   return L.lm_off + tail + 1024;  // +1024: base alignment
@@ -653,7 +656,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
                const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const TcLayout L = tc_layout(g.npad, g.stages);
+  const TcLayout L = tc_layout(g.npad, g.stages, g.kpair);
+  const int KP = g.kpair ? 2 : 1;   // K blocks per stage
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + L.bar_off;
   const uint32_t bar_empty = bar_full + 8 * g.stages;
@@ -726,19 +730,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
           const bool second = !g.a_pair && mt * BM >= g.m_split;
           const CUtensorMap* tm = second ? &tm1 : &tm0;
           const int mrow = g.a_pair ? mt * (BM / 2) : (second ? mt * BM - g.m_split : mt * BM);
-          for (int kb = kb0; kb < kb1 && ok; ++kb) {
+          for (int kb = kb0; kb < kb1 && ok;) {
+            const int nk = min(KP, kb1 - kb);   // K blocks of this stage
             for (int rb = 0; rb < nrb && ok; ++rb) {
               if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
               const uint32_t dst = sbase + stage * L.stage_bytes;
-              mbar_arrive_expect_tx(bar_full + 8 * stage, A_STAGE_BYTES);
-              if (g.a_pair) {  // rows 0-63 from map 0 (gate), rows 64-127 from map 1 (up)
-                tma_load_2d(dst, &tm0, kb * BK, mrow, bar_full + 8 * stage, pol);
-                tma_load_2d(dst + A_STAGE_BYTES / 2, &tm1, kb * BK, mrow, bar_full + 8 * stage, pol);
-              } else {
-                tma_load_2d(dst, tm, kb * BK, mrow, bar_full + 8 * stage, pol);
+              mbar_arrive_expect_tx(bar_full + 8 * stage, nk * A_STAGE_BYTES);
+              for (int u = 0; u < nk; ++u) {
+                const uint32_t du = dst + u * A_STAGE_BYTES;
+                if (g.a_pair) {  // rows 0-63 from map 0 (gate), rows 64-127 from map 1 (up)
+                  tma_load_2d(du, &tm0, (kb + u) * BK, mrow, bar_full + 8 * stage, pol);
+                  tma_load_2d(du + A_STAGE_BYTES / 2, &tm1, (kb + u) * BK, mrow, bar_full + 8 * stage, pol);
+                } else {
+                  tma_load_2d(du, tm, (kb + u) * BK, mrow, bar_full + 8 * stage, pol);
+                }
               }
               if (++stage == g.stages) { stage = 0; phase ^= 1; }
             }
+            kb += nk;
           }
           i += kb1 - kb0;
         }
@@ -758,6 +767,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
       // address field (bits 0-13, in 16-byte units, far from carrying), so the loop adds.
       const uint64_t adesc0 = smem_desc_sw128(sbase), bdesc0 = smem_desc_sw128(sbase + L.b_off);
       const uint64_t dstep = L.stage_bytes >> 4;
+      const uint64_t astep2 = A_STAGE_BYTES >> 4, bstep2 = (static_cast<uint32_t>(npad) * 256u) >> 4;
       int stage = 0;
       uint32_t phase = 0;
       long long uc = 0;
@@ -772,7 +782,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
           const uint32_t ap = static_cast<uint32_t>((uc / g.nbuf) & 1);
           if (!mbar_wait(bar_acce + 8 * ab, ap ^ 1, g.err, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          for (int kb = kb0; kb < kb1 && ok; ++kb) {
+          for (int kb = kb0; kb < kb1 && ok;) {
+            const int nk = min(KP, kb1 - kb);
             for (int rb = 0; rb < nrb; ++rb) {
               if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag)) { ok = false; break; }
               tc_fence_after();
@@ -781,9 +792,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
   #pragma unroll
               for (int j = 0; j < BK / 16; ++j)   // 16 bf16 of K = 32 bytes = 2 descriptor units
                 tc_mma_bf16(d, ad + 2 * j, bd + 2 * j, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
+              if (nk == 2) {   // the stage's second K block
+  #pragma unroll
+                for (int j = 0; j < BK / 16; ++j)
+                  tc_mma_bf16(d, ad + astep2 + 2 * j, bd + bstep2 + 2 * j, idesc, 1u);
+              }
               tc_commit(bar_empty + 8 * stage);
               if (++stage == g.stages) { stage = 0; phase ^= 1; }
             }
+            kb += nk;
           }
           if (ok) tc_commit(bar_accf + 8 * ab);
           i += kb1 - kb0;
@@ -813,14 +830,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
         for (long long i = s0; i < s1 && ok;) {
           const int kb0 = static_cast<int>(i % KB);
           const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (s1 - i)));
-          for (int kb = kb0; kb < kb1 && ok; ++kb) {
+          for (int kb = kb0; kb < kb1 && ok;) {
+            const int nk = min(KP, kb1 - kb);
             for (int rb = 0; rb < nrb && ok; ++rb) {
               if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
-              mbar_arrive_expect_tx(bar_full + 8 * stage, b_bytes);
-              tma_load_2d(sbase + stage * L.stage_bytes + L.b_off, &tmB, kb * BK, rb * np2, bar_full + 8 * stage,
-                          pol_b);
+              mbar_arrive_expect_tx(bar_full + 8 * stage, nk * b_bytes);
+              for (int u = 0; u < nk; ++u)
+                tma_load_2d(sbase + stage * L.stage_bytes + L.b_off + u * b_bytes, &tmB, (kb + u) * BK, rb * np2,
+                            bar_full + 8 * stage, pol_b);
               if (++stage == g.stages) { stage = 0; phase ^= 1; }
             }
+            kb += nk;
           }
           i += kb1 - kb0;
         }
@@ -1361,17 +1381,21 @@ bool plan_gemm(GemmPlan& p, int N) {
   }
   uint32_t cap = static_cast<uint32_t>(g_tc_smem_cap ? g_tc_smem_cap : TC_MAX_SMEM);
   if (p.occ == 2) cap = std::min(cap, TC_SMEM_OCC2);
+  // Few rows (one 16-row block): the MMA issuer's per-stage work (barrier wait, commit,
+  // loop) rather than the tensor core bounds its rate, so a stage carries two K blocks.
+  g.kpair = g.b_tma && g.npad <= 16 ? 1 : 0;
   int stages = 12;
   const bool staged = g.e.kind == EPI_STORE || g.e.kind == EPI_SWIGLU;
-  while (stages >= 2 && tc_smem_bytes(g.npad, stages, lm_rows, topk, staged) > cap) --stages;
+  while (stages >= 2 && tc_smem_bytes(g.npad, stages, lm_rows, topk, staged, g.kpair) > cap) --stages;
   if (stages < 2) return false;
-  if (g.csplit > 1 && part_bytes > static_cast<size_t>(stages) * tc_layout(g.npad, stages).stage_bytes) {
+  if (g.csplit > 1 &&
+      part_bytes > static_cast<size_t>(stages) * tc_layout(g.npad, stages, g.kpair).stage_bytes) {
     // the partial tile does not fit the stage ring it is parked in: stream-K instead
     g.csplit = 0;
     p.grid = static_cast<int>(std::min<long long>(sms, total));
   }
   g.stages = stages;
-  p.smem = tc_smem_bytes(g.npad, stages, lm_rows, topk, staged);
+  p.smem = tc_smem_bytes(g.npad, stages, lm_rows, topk, staged, g.kpair);
   if (g.b_tma) {
     // the operand copy holds 2 N rows (hi, lo); rows past them read as zero
     if (!p.b_hl || !make_act_map(&p.tmB, p.b_hl, 2 * N, g.K, 2 * g.npad)) return false;
