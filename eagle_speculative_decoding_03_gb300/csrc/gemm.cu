@@ -782,25 +782,39 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
           const uint32_t ap = static_cast<uint32_t>((uc / g.nbuf) & 1);
           if (!mbar_wait(bar_acce + 8 * ab, ap ^ 1, g.err, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          for (int kb = kb0; kb < kb1 && ok;) {
-            const int nk = min(KP, kb1 - kb);
-            for (int rb = 0; rb < nrb; ++rb) {
+          // (the one-block loop is kept apart: this thread's per-stage work bounds the rate)
+          if (KP == 1) {
+            for (int kb = kb0; kb < kb1 && ok; ++kb) {
+              for (int rb = 0; rb < nrb; ++rb) {
+                if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>((ab * nrb + rb) * np2);
+                const uint64_t ad = adesc0 + stage * dstep, bd = bdesc0 + stage * dstep;
+  #pragma unroll
+                for (int j = 0; j < BK / 16; ++j)   // 16 bf16 of K = 32 bytes = 2 descriptor units
+                  tc_mma_bf16(d, ad + 2 * j, bd + 2 * j, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
+                tc_commit(bar_empty + 8 * stage);
+                if (++stage == g.stages) { stage = 0; phase ^= 1; }
+              }
+            }
+          } else {   // one 16-row block (nrb == 1), two K blocks per stage
+            const uint32_t d = tmem + static_cast<uint32_t>(ab * np2);
+            for (int kb = kb0; kb < kb1 && ok;) {
               if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag)) { ok = false; break; }
               tc_fence_after();
-              const uint32_t d = tmem + static_cast<uint32_t>((ab * nrb + rb) * np2);
               const uint64_t ad = adesc0 + stage * dstep, bd = bdesc0 + stage * dstep;
   #pragma unroll
-              for (int j = 0; j < BK / 16; ++j)   // 16 bf16 of K = 32 bytes = 2 descriptor units
+              for (int j = 0; j < BK / 16; ++j)
                 tc_mma_bf16(d, ad + 2 * j, bd + 2 * j, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
-              if (nk == 2) {   // the stage's second K block
+              if (kb + 1 < kb1) {   // the stage's second K block
   #pragma unroll
                 for (int j = 0; j < BK / 16; ++j)
                   tc_mma_bf16(d, ad + astep2 + 2 * j, bd + bstep2 + 2 * j, idesc, 1u);
               }
               tc_commit(bar_empty + 8 * stage);
               if (++stage == g.stages) { stage = 0; phase ^= 1; }
+              kb += 2;
             }
-            kb += nk;
           }
           if (ok) tc_commit(bar_accf + 8 * ab);
           i += kb1 - kb0;
