@@ -131,3 +131,39 @@ def oracle_cfg(cfg: DraftConfig) -> dict:
                 d_ff=cfg.d_ff, vocab=cfg.vocab, rms_eps=cfg.rms_eps, rope_theta=cfg.rope_theta,
                 tree=cfg.tree, depth=cfg.depth, k=cfg.k, m=cfg.m,
                 branching=tuple(cfg.branching), feat=cfg.feat)
+
+
+# ------------------------------------------------- verification side (synthetic target)
+def make_target(cfg: DraftConfig) -> dict:
+    """One synthetic target decoder layer for the tree-verification pass.
+
+    The same head shapes as the draft layer, its own weights, and a final RMSNorm gain.
+    The target's frozen embedding and LM head are the draft's (``make_weights``): the
+    draft reuses the target's tables.
+    """
+    d, ff, s, dt = cfg.d, cfg.d_ff, cfg.seed, cfg.dtype
+
+    def gain(key):
+        if cfg.gamma_jitter:
+            return normal((d,), (s, key), cfg.gamma_jitter, "f32", 1.0)
+        return np.ones(d, np.float32)
+
+    return {
+        "attn_norm": gain(40),
+        "w_qkv": normal((cfg.qkv_dim, d), (s, 41), (1.0 / d) ** 0.5, dt),
+        "w_o": normal((d, cfg.attn_dim), (s, 42), (1.0 / cfg.attn_dim) ** 0.5, dt),
+        "mlp_norm": gain(43),
+        "w_gate": normal((ff, d), (s, 44), (1.0 / d) ** 0.5, dt),
+        "w_up": normal((ff, d), (s, 45), (1.0 / d) ** 0.5, dt),
+        "w_down": normal((d, ff), (s, 46), (1.0 / ff) ** 0.5, dt),
+        "final_norm": gain(47),
+    }
+
+
+def make_target_cache(cfg: DraftConfig, inp: dict, seed_offset: int = 0) -> dict:
+    """The target layer's verified-prefix KV cache, packed like the draft's (same
+    ``cu_seqlens``), post-RoPE, N(0,1)."""
+    s = cfg.seed + 7919 * seed_offset
+    shape = (int(inp["cu_seqlens"][-1]), cfg.n_kv_heads, cfg.head_dim)
+    return {"k_cache": normal(shape, (s, 48), 1.0, cfg.dtype),
+            "v_cache": normal(shape, (s, 49), 1.0, cfg.dtype)}
