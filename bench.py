@@ -48,9 +48,9 @@ def algorithmic_bytes(cfg, n_prefix_total: int, N_rows_per_depth):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one LM-head launch of the
-# headline workload (depth-2 launch, 10 rows), from the ncu capture summarised in
-# profiles/lm_head_gemm_eagle2_b1.md, and the hash of the kernel sources it was taken on:
-# reported only while they match.
+# headline workload, from an ncu capture of its depth-2 launch (10 rows; the summary sits
+# with the other ncu summaries under profiles/), and the hash of the kernel sources it was
+# taken on: reported only while they match.
 LM_TRAFFIC_BYTES = 1055.90e6
 LM_TRAFFIC_SOURCES = ("csrc/gemm.cu", "csrc/common.cuh", "csrc/internal.h")
 LM_TRAFFIC_SHA256 = "27295b5e8c480d0b303bf2c18aa18219a55fd904c3d1e6b805c12e8183a450ce"
@@ -363,7 +363,7 @@ def run_ours(args):
                      "peak_source": peak_kind, "algorithmic_bytes_per_launch": lm_bytes,
                      "avg_launch_ms": lm_avg_ms, "traffic": traffic,
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the "
-                                       "depth-2 launch, profiles/lm_head_gemm_eagle2_b1.md"
+                                       "depth-2 launch of this workload (ncu, full size)"
                                        if traffic else "kernel changed since the last capture"},
         "kernels": kernels,
         "gpu_launches": launches,
