@@ -137,6 +137,84 @@ def _chain_reference(cfg, W, I):
     return toks, np.array(logv), feats
 
 
+def _chain_along_path(cfg, W, I, b, tokens):
+    """The written recurrence run causally along one token path of request b:
+    step j feeds [feature of step j-1 ; emb(tokens[j])] (the root feature at j = 0:
+    f, or EAGLE-3's FC([l;m;h])) through fc and the layer at position n_b + j, with
+    plain causal attention over [prefix of b, steps 0..j].  torch float64 library
+    routines only; nothing is shared with the oracle but the upcast.  Returns the
+    per-step h, rotated q, attention output, layer output a and log-sum-exp."""
+    T = lambda a: torch.from_numpy(O.as_f64(a))
+    d, Hq, Hkv, hd = cfg.d, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+    lo, hi = int(I["cu_seqlens"][b]), int(I["cu_seqlens"][b + 1])
+    n = hi - lo
+    Ks, Vs = T(I["k_cache"][lo:hi]), T(I["v_cache"][lo:hi])
+    f = T(I["root_feat"][b])
+    if cfg.feat == "fused":
+        f = T(W["w_fc3"]) @ f
+    inv = cfg.rope_theta ** (-torch.arange(hd // 2, dtype=torch.float64) * 2 / hd)
+
+    def rot(x, pos):
+        z = torch.complex(x[..., :hd // 2], x[..., hd // 2:]) * torch.polar(torch.ones_like(inv), pos * inv)
+        return torch.cat([z.real, z.imag], -1)
+
+    out = []
+    for j, t in enumerate(tokens):
+        pos = n + j
+        h = torch.cat([f, T(W["embed"][int(t)])]) @ T(W["w_fc"]).T
+        x = F.rms_norm(h, (d,), T(W["attn_norm"]), cfg.rms_eps)
+        qkv = x @ T(W["w_qkv"]).T
+        q = rot(qkv[:Hq * hd].view(Hq, hd), pos)
+        k = rot(qkv[Hq * hd:(Hq + Hkv) * hd].view(1, Hkv, hd), pos)
+        v = qkv[(Hq + Hkv) * hd:].view(1, Hkv, hd)
+        Ks, Vs = torch.cat([Ks, k]), torch.cat([Vs, v])
+        rep = Hq // Hkv
+        att = F.scaled_dot_product_attention(
+            q[:, None], Ks.permute(1, 0, 2).repeat_interleave(rep, 0),
+            Vs.permute(1, 0, 2).repeat_interleave(rep, 0))[:, 0].reshape(-1)
+        y = h + att @ T(W["w_o"]).T
+        z = F.rms_norm(y, (d,), T(W["mlp_norm"]), cfg.rms_eps)
+        a = y + (F.silu(z @ T(W["w_gate"]).T) * (z @ T(W["w_up"]).T)) @ T(W["w_down"]).T
+        lse = torch.logsumexp(a @ T(W["w_lm"]).T, -1)
+        out.append(dict(h=h.numpy(), q=q.numpy(), attn=att.numpy(), a=a.numpy(), lse=float(lse)))
+        f = a
+    return out
+
+
+def _assert_rows_follow_their_paths(cfg, W, I, res):
+    """Every tree row equals the causal chain re-run along its own root-to-node path."""
+    checked = 0
+    for s, tr in enumerate(res["trace"], 1):
+        for i, (b, u, rid) in enumerate(tr["rows"]):
+            req = res["reqs"][b]
+            path = (req.tok[0],) + req.path(u)           # the root token, then the path to u
+            assert len(path) == s
+            last = _chain_along_path(cfg, W, I, b, path)[-1]
+            for key in ("h", "q", "attn", "a"):
+                got = tr[key][i].reshape(-1)
+                np.testing.assert_allclose(got, last[key].reshape(-1), rtol=1e-11, atol=1e-11,
+                                           err_msg=f"{cfg.name} depth {s} row {i} {key}")
+            np.testing.assert_allclose(tr["lse"][i], last["lse"], rtol=1e-12, atol=1e-11)
+            checked += 1
+    return checked
+
+
+@pytest.mark.parametrize("name", ["small_dyn", "small_static", "small_fused", "tiny16"])
+def test_every_tree_row_equals_the_chain_along_its_path(name, small_runs):
+    """Ancestor-only tree attention ('Tree attention in one verification pass'): a row of
+    a branching tree sees the prefix and its ancestors' KV only, so it must equal the
+    plain recurrence ('The recurrence, written out') run causally along its own path.
+    A sibling or cousin leaking into a row's KV, or a row reading the wrong source row's
+    ancestors, breaks this."""
+    if name == "tiny16":
+        cfg = TINY
+        W, I, res = _run(cfg)
+    else:
+        cfg = configs.get(name)
+        W, I, res = small_runs[name]
+    assert _assert_rows_follow_their_paths(cfg, W, I, res) == sum(len(t["rows"]) for t in res["trace"])
+
+
 def test_chain_recurrence_k1():
     cfg = configs.get("tiny_chain")
     W, I, res = _run(cfg)
