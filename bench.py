@@ -141,54 +141,94 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
-def oracle_step_sample(cfg, W, I):
-    """One draft step of the oracle at full width (the rows of depth 2 of every request:
-    fc, decoder layer over the prefix + own KV, LM head, log-softmax, top-k).  Returns
-    seconds."""
-    from oracle import eagle_oracle as O
-    ocfg = synth.oracle_cfg(cfg)
-    R = cfg.rows_at(2) if cfg.depth > 1 else 1
-    N = cfg.B * R
-    rng = np.random.default_rng(0)
-    cu = np.asarray(I["cu_seqlens"], np.int64)
-    feats = rng.standard_normal((N, cfg.d)) * synth.FEATURE_RMS
-    toks = rng.integers(0, cfg.vocab, N)
-    pos = np.array([cu[i // R + 1] - cu[i // R] + 1 for i in range(N)])
-    Kc, Vc = O.as_f64(I["k_cache"]), O.as_f64(I["v_cache"])
+class OracleStep:
+    """One draft step of the float64 oracle on the workload's real depth-2 rows.
 
-    def attend(i, k_i, v_i):
-        b = i // R
-        return (np.concatenate([Kc[cu[b]:cu[b + 1]], k_i[None]]),
-                np.concatenate([Vc[cu[b]:cu[b + 1]], v_i[None]]))
+    Set-up (untimed): the oracle's own depth-1 expansion of every request (the root row),
+    which fixes the depth-2 frontier, its tokens, the parent row's output feature and the
+    root row's K/V.  ``run()`` then times the oracle's fc + decoder layer + LM head +
+    log-softmax + top-k over those rows, attending to the prefix, the root row and
+    themselves exactly as the tree step does.  Returns seconds."""
 
-    t0 = time.perf_counter()
-    x_in = np.concatenate([feats, O.as_f64(W["embed"][toks])], axis=1)
-    out = O.decoder_rows(ocfg, W, x_in, pos, attend)
-    for i in range(N):
-        O.top_k(out["logp"][i], cfg.children_at(2))
-    return time.perf_counter() - t0
+    def __init__(self, cfg, W, I):
+        from oracle import eagle_oracle as O
+        self.O, self.cfg, self.W = O, cfg, W
+        ocfg = synth.oracle_cfg(cfg)
+        self.ocfg = ocfg
+        res = O.draft_tree(dict(ocfg, depth=1, m=min(ocfg["m"], cfg.children_at(1))), W, I)
+        cu = np.asarray(I["cu_seqlens"], np.int64)
+        self.Kc, self.Vc = O.as_f64(I["k_cache"]), O.as_f64(I["v_cache"])
+        feats, toks, pos, meta = [], [], [], []
+        for b, r in enumerate(res["reqs"]):
+            root_row = r.rows[0]
+            kids = [g for g in range(1, len(r.tok)) if r.depth[g] == 1]
+            if cfg.tree == "dynamic":
+                vals = np.array([r.logv[g] for g in kids])
+                sel, _ = O.top_k(vals, min(cfg.k, len(kids)), np.array(kids))
+                kids = sorted(np.array(kids)[sel].tolist())
+            for g in kids:
+                feats.append(root_row["a"])
+                toks.append(r.tok[g])
+                pos.append(r.n + 1)
+                meta.append((b, root_row["k"], root_row["v"], int(cu[b]), int(cu[b + 1])))
+        self.x_feat = np.stack(feats)
+        self.toks = np.asarray(toks)
+        self.pos = np.asarray(pos)
+        self.meta = meta
+        self.rows = len(toks)
+
+    def run(self) -> float:
+        O, meta = self.O, self.meta
+
+        def attend(i, k_i, v_i):
+            _, k0, v0, lo, hi = meta[i]
+            return (np.concatenate([self.Kc[lo:hi], k0[None], k_i[None]]),
+                    np.concatenate([self.Vc[lo:hi], v0[None], v_i[None]]))
+
+        t0 = time.perf_counter()
+        x_in = np.concatenate([self.x_feat, O.as_f64(self.W["embed"][self.toks])], axis=1)
+        out = O.decoder_rows(self.ocfg, self.W, x_in, self.pos, attend)
+        for i in range(self.rows):
+            O.top_k(out["logp"][i], self.cfg.children_at(2))
+        return time.perf_counter() - t0
+
+
+def config_block(name, cfg, B, world, wbytes):
+    """The ``config`` object both arms print (the same workload string and keys)."""
+    return {"workload": describe(name, cfg, B),
+            "global_batch": B * world, "seq_len": cfg.prefix[1], "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2: every depth streams the {wbytes / 1e9:.2f} GB of head weights "
+                  f"from HBM" if wbytes > 129e6 else "weights fit in L2 (latency-bound shape)",
+            "nodes_per_tree": B * cfg.kept_per_request()}
 
 
 # ------------------------------------------------------------- reference arm
 def run_reference(args):
+    """The float64 oracle timed on the host cores, one draft step (1/depth of a tree) per
+    bench step; rank 0 only.  ``ms_per_step`` is the measured draft-step time itself."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     cfg = configs.get(args.workload)
     W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    st = OracleStep(cfg, W, I)
     for _ in range(args.warmup):
-        oracle_step_sample(cfg, W, I)
-    ts = [oracle_step_sample(cfg, W, I) for _ in range(args.steps)]
+        st.run()
+    ts = [st.run() for _ in range(args.steps)]
     t = float(np.mean(ts))
     nodes_per_step = cfg.B * cfg.kept_per_request() / cfg.depth
     value = nodes_per_step / t
-    sample = (f"one draft step of the float64 oracle at full width ({cfg.B * cfg.rows_at(2)} rows: fc, decoder "
-              f"layer, LM head, top-k); nodes/s = (B*m/depth) / step time")
+    _, wbytes, _ = algorithmic_bytes(cfg, int(I["cu_seqlens"][-1]), [cfg.B])
+    sample = (f"one draft step of the float64 oracle on the oracle's own depth-2 rows ({st.rows} rows: fc, "
+              f"decoder layer, LM head, log-softmax, top-k); a bench step is that draft step, which stands for "
+              f"B*m/depth = {nodes_per_step:g} tree nodes")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 * cfg.depth,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "step_basis": "one draft step (1/depth of a tree)", "nodes_per_step": nodes_per_step,
             "us_per_draft_step": t * 1e6, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "global_batch": cfg.B, "seq_len": cfg.prefix[1]},
+            "config": config_block(args.workload, cfg, cfg.B, world, wbytes),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -339,10 +379,11 @@ def run_ours(args):
     # ---- CPU baseline: the float64 oracle on host cores (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        t = oracle_step_sample(cfg, W, I)
+        st = OracleStep(cfg, W, I)
+        t = st.run()
         v = (B * cfg.kept_per_request() / cfg.depth) / t
         cpu = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"one draft step of the float64 oracle at full width ({B * cfg.rows_at(2)} rows), "
+               "sample": f"one draft step of the float64 oracle on its own depth-2 rows ({st.rows} rows), "
                          f"{t:.1f} s; nodes/s = (B*m/depth) / step time"}
 
     launches = d.info["launches_per_tree"] * args.steps
@@ -351,11 +392,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "us_per_draft_step": ms * 1e3 / cfg.depth,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": describe(args.workload, cfg, B),
-                   "global_batch": B * world, "seq_len": cfg.prefix[1], "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: every depth streams the {wbytes / 1e9:.2f} GB of head weights "
-                         f"from HBM" if wbytes > 129e6 else "weights fit in L2 (latency-bound shape)",
-                   "nodes_per_tree": nodes_per_tree, "timing": "graph replay, CUDA events on the stream"},
+        "config": config_block(args.workload, cfg, B, world, wbytes),
+        "timing": "graph replay, CUDA events on the stream",
         "hbm_frac_step": step_gbs / peak,
         "step_algorithmic_bytes": algo,
         "roofline": {"bound": "hbm", "kernel": "lm_head (gemm_tc_kernel, LM-head epilogue)",

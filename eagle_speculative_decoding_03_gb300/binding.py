@@ -151,8 +151,16 @@ def device_inputs(I: dict, device="cuda"):
 
 def lm_head_topk_noalloc(w_lm, a, k: int, stream=None):
     """LM-head top-k without a handle and without any device allocation inside the
-    library (for callers that cannot allocate); outputs are allocated here by torch."""
+    library (for callers that cannot allocate); outputs are allocated here by torch.
+    The library reads w_lm as bf16 and a as float32: other dtypes are rejected here.
+    If a kernel of the call gave up, every row comes back as id -1 and NaN logp / lse."""
     import torch
+    if w_lm.dtype not in (torch.bfloat16, torch.int16) or w_lm.dim() != 2:
+        raise EagleError(EAGLE_ERR_INVALID_ARG, "noalloc: w_lm must be a 2-D bf16 tensor (or its int16 bits)")
+    if a.dtype != torch.float32 or a.dim() != 2 or a.shape[1] != w_lm.shape[1]:
+        raise EagleError(EAGLE_ERR_INVALID_ARG, "noalloc: a must be float32 [N, d] with d = w_lm.shape[1]")
+    if not (w_lm.is_contiguous() and a.is_contiguous()):
+        raise EagleError(EAGLE_ERR_INVALID_ARG, "noalloc: w_lm and a must be contiguous")
     N, d = int(a.shape[0]), int(a.shape[1])
     ids = torch.empty((N, k), dtype=torch.int32, device=a.device)
     logp = torch.empty((N, k), dtype=torch.float32, device=a.device)

@@ -499,6 +499,7 @@ static eagle_status_t lm_head(eagle_draft* h, const float* a, const uint16_t* a_
 
 static LmPartials lm_partials(eagle_draft* h, int N) {
   LmPartials lm;
+  lm.poison_if = nullptr;   // the handle reports kernel-side problems through eagle_draft_check
   lm.max = h->lm_max;
   lm.sum = h->lm_sum;
   lm.val = h->lm_val;

@@ -1269,14 +1269,23 @@ bool make_act_map(CUtensorMap* tm, const void* hl, int rows, int K, int box_rows
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int g_num_sms = 0;
+// SM count of the current device, cached per device ordinal (GPUs of one host may differ).
+constexpr int MAX_DEVICES = 64;
+static int g_num_sms[MAX_DEVICES] = {};
 int num_sms() {
-  if (!g_num_sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= MAX_DEVICES) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
   }
-  return g_num_sms;
+  if (!g_num_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
 }
 
 constexpr int TC_MAX_SMEM = 232448;
@@ -1302,12 +1311,12 @@ cudaError_t allow_max_smem(const void* func, size_t* granted) {
 // at once; cached per device and size.
 int gemm_active_clusters(int S) {
   static std::mutex mu;
-  static int cache[16][9];
+  static int cache[MAX_DEVICES][9];
   static bool init = false;
   std::lock_guard<std::mutex> lk(mu);
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 16 || S < 1 || S > 8) return 0;
+  if (dev < 0 || dev >= MAX_DEVICES || S < 1 || S > 8) return 0;
   if (!init) {
     for (auto& row : cache)
       for (int& c : row) c = -1;

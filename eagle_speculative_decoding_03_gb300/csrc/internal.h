@@ -108,6 +108,8 @@ struct LmPartials {
   int* id;                  // [N][G][k]
   int G;                    // CTAs that wrote top-k partials
   int T;                    // vocabulary tiles
+  const unsigned* poison_if;  // standalone merge: when this device word is non-zero (a kernel of
+                              // the call gave up), every output row is poisoned instead of merged
 };
 
 struct OutArgs {

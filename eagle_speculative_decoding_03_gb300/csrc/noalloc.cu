@@ -13,6 +13,13 @@
 // exits.  All calls share it and it keeps the last call's contents: a call clears what
 // must start at zero (the split-K arrival counters and the error word), and two calls
 // whose kernels overlap on the GPU (different streams or host threads) race on it.
+//
+// Errors inside the kernels: there is no handle to carry a device error word to the host,
+// so the call reports through its outputs.  If a bounded wait in the LM-head kernel runs
+// out, the tiles it never reached would leave the previous call's partials in the array;
+// the merge kernel then writes id -1 and NaN log-probability / log-sum-exp for every row
+// rather than merging them.  A row whose logits are not finite gets id -1 for each of the
+// k places it could not fill.
 #include "../../include/eagle_draft.h"
 #include "common.cuh"
 #include "internal.h"
@@ -133,6 +140,7 @@ extern "C" eagle_status_t eagle_lm_head_topk_noalloc(const void* w_lm, int32_t v
   lm.id = g.e.lm_id;
   lm.G = p.grid;
   lm.T = vocab / BM;
+  lm.poison_if = g.err;   // a wait that ran out leaves stale partials: poison the outputs instead
   if (launch_lm_merge(lm, N, k, ids, logp, lse, cs, false) != cudaSuccess)
     return na_fail(EAGLE_ERR_CUDA, "noalloc: merge kernel launch failed");
   return EAGLE_OK;

@@ -625,6 +625,15 @@ lm_merge_kernel(const LmPartials lm, int N, int k, int* ids, float* logp, float*
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * (blockDim.x >> 5) + warp;
   if (n >= N) return;
+  if (lm.poison_if && __ldcg(lm.poison_if) != 0u) {
+    // the LM-head kernel gave up part-way: its partials are incomplete, so no row is merged
+    if (lane < k) {
+      ids[static_cast<size_t>(n) * k + lane] = -1;
+      logp[static_cast<size_t>(n) * k + lane] = __int_as_float(0x7fc00000);
+    }
+    if (lane == 0) lse_out[n] = __int_as_float(0x7fc00000);
+    return;
+  }
   float2* cand = mg_smem + static_cast<size_t>(warp) * lm.G * k;
   float lse, v;
   int id;

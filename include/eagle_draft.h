@@ -215,7 +215,11 @@ EAGLE_API eagle_status_t eagle_draft_lm_head_topk(eagle_draft_t* handle, const f
  * The first call on a device looks up the array's device address and sets the kernels'
  * shared-memory limits (make that first call before any stream capture).  Every call
  * shares the array and clears the parts that must start at zero; calls whose kernels
- * overlap on the GPU (other streams, other threads) race on it and give wrong results. */
+ * overlap on the GPU (other streams, other threads) race on it and give wrong results.
+ * Kernel-side errors: with no handle to hold a device error word, they show in the
+ * outputs.  If a bounded wait inside the LM-head kernel runs out, every row of the call
+ * comes back as id -1 with NaN logp and lse; a row with fewer than k finite logits gets
+ * id -1 in the places it could not fill. */
 EAGLE_API eagle_status_t eagle_lm_head_topk_noalloc(const void* w_lm, int32_t vocab, int32_t d,
                                                     const float* a, int32_t N, int32_t k,
                                                     int32_t* ids, float* logp, float* lse,

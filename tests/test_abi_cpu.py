@@ -86,3 +86,16 @@ def test_struct_layout_matches_header():
     assert C.sizeof(eb.Weights) == 11 * 8
     assert C.sizeof(eb.Inputs) == 6 * 8
     assert C.sizeof(eb.Info) == 8 * 4 + 8
+
+
+def test_noalloc_binding_rejects_wrong_dtypes(lib):
+    """The allocation-free LM-head entry point reads w_lm as bf16 and a as float32; the
+    binding rejects anything else before the call (no GPU needed to see it)."""
+    import torch
+    w32 = torch.zeros((256, 128), dtype=torch.float32)
+    w16 = torch.zeros((256, 128), dtype=torch.bfloat16)
+    a32 = torch.zeros((2, 128), dtype=torch.float32)
+    for w, a in ((w32, a32), (w16, a32.double()), (w16, torch.zeros((2, 64), dtype=torch.float32))):
+        with pytest.raises(eb.EagleError) as ei:
+            eb.lm_head_topk_noalloc(w, a, 2)
+        assert ei.value.status == eb.EAGLE_ERR_INVALID_ARG

@@ -95,3 +95,25 @@ def test_reference_arm_line_keeps_the_contract(monkeypatch):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+@pytest.mark.parametrize("name", ["small_dyn", "small_static", "small_fused"])
+def test_reference_step_times_the_oracles_own_depth2_rows(name):
+    """The reference arm's timed draft step is the oracle's own depth-2 step: same rows,
+    tokens, features and attention (its layer outputs equal the whole-tree oracle's)."""
+    from oracle import eagle_oracle as O
+    cfg = configs.get(name)
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    st = bench.OracleStep(cfg, W, I)
+    assert st.rows == cfg.B * cfg.rows_at(2)
+    full = O.draft_tree(synth.oracle_cfg(cfg), W, I)["trace"][1]
+
+    def attend(i, k_i, v_i):
+        _, k0, v0, lo, hi = st.meta[i]
+        return (np.concatenate([st.Kc[lo:hi], k0[None], k_i[None]]),
+                np.concatenate([st.Vc[lo:hi], v0[None], v_i[None]]))
+
+    x_in = np.concatenate([st.x_feat, O.as_f64(W["embed"][st.toks])], axis=1)
+    out = O.decoder_rows(st.ocfg, W, x_in, st.pos, attend)
+    np.testing.assert_allclose(out["a"], full["a"], rtol=1e-12, atol=1e-12)
+    assert st.run() > 0

@@ -3,7 +3,9 @@ the benchmark times (graph replay with programmatic dependent launch).
 
 The oracle follows every request of a call independently, so for the batched workloads
 it checks a sample of requests (the shortest and the longest prefix, and one between)
-against the same rows of the full-batch GPU run.  Tolerances are those of the small
+against the same rows of the full-batch GPU run, and then every request teacher-forced:
+at each depth the oracle runs the layer on the GPU's own inputs and takes the LM head,
+children, frontier and rerank from the GPU's layer output.  Tolerances are those of the small
 parity tests: structure exact except near-ties below 1e-3 in log probability, features
 2e-2 relative, path values 1e-2 absolute."""
 import numpy as np
@@ -48,4 +50,12 @@ def test_tree_parity_full_size(lib, name, n_req):
     rep = parity.compare(synth.oracle_cfg(cfg), W, sI, sout, str_, d.info["slots"])
     print(name, reqs, {k: f"{v:.2e}" for k, v in rep["stats"].items()}, "forced:", rep["forced"])
     assert rep["ok"], rep["errors"]
+    if cfg.B > 1:
+        # every request (past the first 128-row LM-head chunk too), depth by depth on the
+        # GPU's own inputs: layer outputs, LM-head decisions, frontier, rerank and emit
+        rep = parity.compare_teacher_forced(synth.oracle_cfg(cfg), W, I, out, tr, d.info["slots"])
+        print(name, "all", rep["requests"], "requests (teacher-forced)",
+              {k: f"{v:.2e}" for k, v in rep["stats"].items()}, "forced:", len(rep["forced"]))
+        assert rep["ok"], rep["errors"]
+        assert rep["requests"] == cfg.B
     d.close()

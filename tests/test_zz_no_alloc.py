@@ -57,6 +57,28 @@ def test_noalloc_matches_handle_entry_point_twice(lib, name, N, k):
     handle.close()
 
 
+@pytest.mark.slow
+def test_noalloc_llama3_vocab_matches_handle_entry_point_twice(lib):
+    """The Llama-3-8B-shaped LM head (|V| = 128256, d = 4096: 1002 vocabulary tiles over the
+    full SM grid), N = 16 rows, k = 16: the largest launch the array is laid out for."""
+    base = configs.get("eagle2_b1")
+    cfg = base.with_(d_ff=128, n_heads=1, n_kv_heads=1, k=16, m=16, depth=2)   # only the LM head matters
+    W = synth.make_weights(cfg)
+    dW = eb.device_weights(W)
+    N, k = 16, 16
+    a_np = (np.random.default_rng(11).standard_normal((N, cfg.d)) * synth.FEATURE_RMS).astype(np.float32)
+    a = torch.from_numpy(a_np).cuda()
+    lp_ref, _ = O.log_softmax(O.linear(a_np, W["w_lm"]))
+    handle = eb.EagleDraft(cfg, dW, max_batch=1, max_prefix=16)
+    ref = handle.lm_head_topk(a, k)
+    handle.check()
+    for _ in range(2):
+        got = eb.lm_head_topk_noalloc(dW["w_lm"], a, k)
+        torch.cuda.synchronize()
+        _same_result(ref, got, lp_ref, k)
+    handle.close()
+
+
 def test_noalloc_allocates_nothing(lib):
     cfg = configs.get("small_dyn")
     dW = eb.device_weights(synth.make_weights(cfg))
