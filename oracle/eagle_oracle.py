@@ -221,7 +221,7 @@ def _choose(values, k, keys, forced, tol, log, what):
 
 
 def expand_tree(cfg: dict, n_prefix, root_tok, step, force: dict | None = None,
-                tol: float = MARGIN_TOL):
+                tol: float = MARGIN_TOL, seeds=None):
     """Static or EAGLE-2 dynamic tree expansion, independent of the network.
 
     ``step(s, reqs, rows)`` runs the draft model on the rows of depth s and returns
@@ -234,7 +234,14 @@ def expand_tree(cfg: dict, n_prefix, root_tok, step, force: dict | None = None,
     ``force["frontier"][s]`` [B, F] node ids, ``force["final"]`` [B, m] node ids.
     A forced choice is adopted only when it is a valid top-k up to ``tol``; otherwise
     the oracle keeps its own and records a mismatch.
+
+    ``seeds`` (optional, one 64-bit seed per request) switches to sampled drafting
+    ("EAGLE-1 - autoregressive feature drafting", zackli.ai: the draft samples its next
+    token from p-hat): a row's children are k tokens drawn without replacement from its
+    distribution, the top-k of log p + Gumbel noise (``oracle.sampling``), kept in draw
+    order; path values still add the unperturbed log-probabilities.
     """
+    from . import sampling
     D = cfg["depth"]
     static = cfg["tree"] == "static"
     reqs = [_Req(n, t) for n, t in zip(n_prefix, root_tok)]
@@ -256,9 +263,13 @@ def expand_tree(cfg: dict, n_prefix, root_tok, step, force: dict | None = None,
         for i, (b, u, rid) in enumerate(rows):
             r = reqs[b]
             forced = None if force is None else force["children"][s][i]
-            sel, margin = _choose(logp[i], kids, None, forced, tol, log, ("children", s, i))
+            key = logp[i]
+            if seeds is not None:           # draw order: largest perturbed value first
+                key = logp[i] + sampling.gumbel(len(logp[i]), r.frontier.index(u), s, int(seeds[b]))
+            sel, margin = _choose(key, kids, None, forced, tol, log, ("children", s, i))
             log["margins"].append(("children", s, i, margin))
-            sel = np.sort(sel)
+            if seeds is None:
+                sel = np.sort(sel)
             children.append(sel)
             child_logp.append(logp[i][sel])
             for t in sel:
@@ -370,7 +381,7 @@ def draft_tree(cfg: dict, W: dict, inp: dict, force: dict | None = None,
         logp = out.pop("logp")
         return logp, out
 
-    res = expand_tree(cfg, cu[1:] - cu[:-1], inp["root_tok"], step, force, tol)
+    res = expand_tree(cfg, cu[1:] - cu[:-1], inp["root_tok"], step, force, tol, inp.get("seeds"))
     res["root_feat"] = root_feat
     return res
 
