@@ -42,7 +42,8 @@ class Weights(C.Structure):
 
 class Inputs(C.Structure):
     _fields_ = [("B", C.c_int32), ("root_feat", C.c_void_p), ("root_tok", C.c_void_p),
-                ("k_cache", C.c_void_p), ("v_cache", C.c_void_p), ("cu_seqlens", C.c_void_p)]
+                ("k_cache", C.c_void_p), ("v_cache", C.c_void_p), ("cu_seqlens", C.c_void_p),
+                ("seeds", C.c_void_p)]
 
 
 class Outputs(C.Structure):
@@ -62,6 +63,31 @@ class Info(C.Structure):
                 ("n_max", C.c_int32), ("k_max", C.c_int32), ("f_max", C.c_int32),
                 ("launches_per_tree", C.c_int32), ("tensor_core_gemm", C.c_int32),
                 ("workspace_bytes", C.c_int64)]
+
+
+class VerifyConfig(C.Structure):
+    _fields_ = [("d", C.c_int32), ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("d_ff", C.c_int32), ("vocab", C.c_int32),
+                ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("dtype", C.c_int32),
+                ("max_batch", C.c_int32), ("max_slots", C.c_int32), ("max_prefix", C.c_int32),
+                ("flags", C.c_int32)]
+
+
+class VerifyWeights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("embed", "attn_norm", "w_qkv", "w_o", "mlp_norm", "w_gate",
+                                         "w_up", "w_down", "final_norm", "w_lm")]
+
+
+class VerifyInputs(C.Structure):
+    _fields_ = [("B", C.c_int32), ("S", C.c_int32)] + \
+        [(n, C.c_void_p) for n in ("tokens", "positions", "mask", "parents", "k_cache", "v_cache", "cu_seqlens")]
+
+
+VERIFY_OUTPUTS = ("top_id", "top_logp", "lse", "hidden", "accept_len", "accept_slots", "correction")
+
+
+class VerifyOutputs(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in VERIFY_OUTPUTS]
 
 
 _lib = None
@@ -97,6 +123,14 @@ def load(path: str = LIB_PATH):
     lib.eagle_draft_kernel_name.restype = C.c_char_p
     lib.eagle_lm_head_topk_noalloc.argtypes = [P, C.c_int32, C.c_int32, P, C.c_int32, C.c_int32, P, P, P, P]
     lib.eagle_lm_head_topk_noalloc.restype = C.c_int
+    lib.eagle_verify_create.argtypes = [C.POINTER(VerifyConfig), C.POINTER(VerifyWeights), C.POINTER(P)]
+    lib.eagle_verify_create.restype = C.c_int
+    lib.eagle_verify_tree.argtypes = [P, C.POINTER(VerifyInputs), C.POINTER(VerifyOutputs), P]
+    lib.eagle_verify_tree.restype = C.c_int
+    lib.eagle_verify_check.argtypes = [P, C.POINTER(C.c_uint32)]
+    lib.eagle_verify_check.restype = C.c_int
+    lib.eagle_verify_destroy.argtypes = [P]
+    lib.eagle_verify_destroy.restype = None
     lib.eagle_draft_last_error.argtypes = []
     lib.eagle_draft_last_error.restype = C.c_char_p
     _lib = lib
@@ -136,11 +170,12 @@ def _ptr(t) -> int | None:
 
 
 def device_weights(W: dict, device="cuda"):
-    """numpy weights (bf16 as uint16 bits) -> device tensors (bf16 kept as int16 bits)."""
+    """numpy weights (bf16 as uint16 bits) -> device tensors (bf16 kept as int16 bits;
+    uint64 seeds kept as int64 bits)."""
     import torch
     out = {}
     for k, v in W.items():
-        arr = v.view(np.int16) if v.dtype == np.uint16 else v
+        arr = v.view(np.int16) if v.dtype == np.uint16 else v.view(np.int64) if v.dtype == np.uint64 else v
         out[k] = torch.from_numpy(np.ascontiguousarray(arr)).to(device)
     return out
 
@@ -230,7 +265,7 @@ class EagleDraft:
         out = self.alloc_outputs(B, dI["root_tok"].device) if out is None else out
         inp = Inputs(B=B, root_feat=_ptr(dI["root_feat"]), root_tok=_ptr(dI["root_tok"]),
                      k_cache=_ptr(dI["k_cache"]), v_cache=_ptr(dI["v_cache"]),
-                     cu_seqlens=_ptr(dI["cu_seqlens"]))
+                     cu_seqlens=_ptr(dI["cu_seqlens"]), seeds=_ptr(dI.get("seeds")))
         o = Outputs(**{n: _ptr(out[n]) for n, _ in Outputs._fields_})
         tr = None if trace is None else C.byref(Trace(**{n: _ptr(trace.get(n)) for n in TRACE_FIELDS}))
         st = None if stream is None else stream.cuda_stream
@@ -262,6 +297,70 @@ class EagleDraft:
         """Synchronise; raise on a device error word or CUDA error."""
         w = C.c_uint32(0)
         st = load().eagle_draft_check(self.h, C.byref(w))
+        if st != EAGLE_OK:
+            raise EagleError(st, load().eagle_draft_last_error().decode())
+        return w.value
+
+
+class EagleVerify:
+    """Handle of the target's verification pass over emitted trees (bf16 target layer)."""
+
+    def __init__(self, cfg: DraftConfig, dWt: dict, dW: dict, max_batch: int, max_slots: int,
+                 max_prefix: int | None = None, flags: int = 0):
+        lib = load()
+        self.cfg = cfg
+        self._keep = (dWt, dW)
+        c = VerifyConfig(d=cfg.d, n_heads=cfg.n_heads, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,
+                         d_ff=cfg.d_ff, vocab=cfg.vocab, rms_eps=cfg.rms_eps, rope_theta=cfg.rope_theta,
+                         dtype=DTYPE_BF16 if cfg.dtype == "bf16" else DTYPE_F32, max_batch=max_batch,
+                         max_slots=max_slots, max_prefix=cfg.prefix[1] if max_prefix is None else max_prefix,
+                         flags=flags)
+        w = VerifyWeights(embed=_ptr(dW["embed"]), w_lm=_ptr(dW["w_lm"]),
+                          **{n: _ptr(dWt[n]) for n in ("attn_norm", "w_qkv", "w_o", "mlp_norm", "w_gate",
+                                                       "w_up", "w_down", "final_norm")})
+        h = C.c_void_p()
+        _check(lib.eagle_verify_create(C.byref(c), C.byref(w), C.byref(h)))
+        self.h = h
+
+    def close(self):
+        if getattr(self, "h", None):
+            load().eagle_verify_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def verify(self, tree: dict, cache: dict, cu_seqlens, accept: bool = True, hidden: bool = False,
+               stream=None) -> dict:
+        """tree: device tensors tokens / positions / parents [B,S] int32 and mask [B,S,S] uint8
+        (as eagle_draft_tree emits them); cache: the target's k_cache / v_cache."""
+        import torch
+        B, S = (int(x) for x in tree["tokens"].shape)
+        dev = tree["tokens"].device
+        out = {"top_id": torch.empty((B, S), dtype=torch.int32, device=dev),
+               "top_logp": torch.empty((B, S), dtype=torch.float32, device=dev),
+               "lse": torch.empty((B, S), dtype=torch.float32, device=dev)}
+        if hidden:
+            out["hidden"] = torch.empty((B, S, self.cfg.d), dtype=torch.float32, device=dev)
+        if accept:
+            out["accept_len"] = torch.empty((B,), dtype=torch.int32, device=dev)
+            out["accept_slots"] = torch.empty((B, S), dtype=torch.int32, device=dev)
+            out["correction"] = torch.empty((B,), dtype=torch.int32, device=dev)
+        inp = VerifyInputs(B=B, S=S, tokens=_ptr(tree["tokens"]), positions=_ptr(tree["positions"]),
+                           mask=_ptr(tree["mask"]), parents=_ptr(tree.get("parents")),
+                           k_cache=_ptr(cache["k_cache"]), v_cache=_ptr(cache["v_cache"]),
+                           cu_seqlens=_ptr(cu_seqlens))
+        o = VerifyOutputs(**{n: _ptr(out.get(n)) for n in VERIFY_OUTPUTS})
+        st = None if stream is None else stream.cuda_stream
+        _check(load().eagle_verify_tree(self.h, C.byref(inp), C.byref(o), st))
+        return out
+
+    def check(self) -> int:
+        w = C.c_uint32(0)
+        st = load().eagle_verify_check(self.h, C.byref(w))
         if st != EAGLE_OK:
             raise EagleError(st, load().eagle_draft_last_error().decode())
         return w.value

@@ -17,6 +17,7 @@
 #include "internal.h"
 
 #include <cooperative_groups.h>
+#include <algorithm>
 #include <mutex>
 namespace cg = cooperative_groups;
 
@@ -470,10 +471,16 @@ tree_attention_tc_kernel(const AttnArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
-  const int kvh = blockIdx.y, b = blockIdx.z;
+  // blockIdx.z = request * row groups + group: a request's rows may be split into groups
+  // of rows_per_group (each its own cluster, each reading the whole prefix) so that no CTA
+  // holds more than TA_MAX_QV query vectors
+  const int G = a.row_groups > 1 ? a.row_groups : 1;
+  const int kvh = blockIdx.y, b = blockIdx.z / G, grp = blockIdx.z - (blockIdx.z / G) * G;
+  const int rpg = G > 1 ? a.rows_per_group : a.rows_per_req;
+  const int rfirst = grp * rpg;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
   const int gq = a.Hq / a.Hkv;
-  const int qv = a.rows_per_req * gq;
+  const int qv = max(0, min(rpg, a.rows_per_req - rfirst)) * gq;
   const int WM = (qv + 15) >> 4, SROW = WM * 16;
   const int KS = ta_key_splits(WM);
   const int mt = warp / KS, ks = warp - mt * KS;
@@ -489,7 +496,7 @@ tree_attention_tc_kernel(const AttnArgs a) {
   // the prefix length is clamped here the way the roots kernel clamps (and reports) it.
   const int nb = min(max(__ldg(a.cu_seqlens + b + 1) - __ldg(a.cu_seqlens + b), 0), a.max_prefix);
   const int npre = (nb + ATT_CHUNK - 1) / ATT_CHUNK;
-  const int row0 = b * a.rows_per_req;
+  const int row0 = b * a.rows_per_req + rfirst;
   const size_t kv_ld = static_cast<size_t>(a.Hkv) * TA_HD;
   const size_t base = (static_cast<size_t>(__ldg(a.cu_seqlens + b)) * a.Hkv + kvh) * TA_HD;
   const uint16_t* kc = static_cast<const uint16_t*>(a.k_cache) + base;
@@ -708,9 +715,15 @@ tree_attention_tc_kernel(const AttnArgs a) {
   cluster.sync();
 }
 
-static bool use_tc(const AttnArgs& a) {
-  return a.cache_bf16 && a.hd == TA_HD && a.rows_per_req * (a.Hq / a.Hkv) <= TA_MAX_QV;
+static int rows_per_cta(const AttnArgs& a) {
+  return a.row_groups > 1 ? std::min(a.rows_per_group, a.rows_per_req) : a.rows_per_req;
 }
+
+static bool use_tc(const AttnArgs& a) {
+  return a.cache_bf16 && a.hd == TA_HD && rows_per_cta(a) * (a.Hq / a.Hkv) <= TA_MAX_QV;
+}
+
+int attn_rows_per_group(int Hq, int Hkv) { return TA_MAX_QV / (Hq / Hkv); }
 
 static int g_att_cluster = 0;
 
@@ -767,7 +780,11 @@ static int active_clusters(bool tc, int cs, size_t smem) {
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
   const bool tc = use_tc(a);
-  const int qv = a.rows_per_req * (a.Hq / a.Hkv);
+  const int G = a.row_groups > 1 ? a.row_groups : 1;
+  if (G > 1 && (!tc || static_cast<long long>(G) * a.rows_per_group < a.rows_per_req ||
+                static_cast<long long>(G - 1) * a.rows_per_group >= a.rows_per_req))
+    return cudaErrorInvalidValue;   // groups only on the tensor-core path, each with >= 1 row
+  const int qv = rows_per_cta(a) * (a.Hq / a.Hkv);
   const size_t smem = tc ? TA_SMEM : attn_smem_bytes(qv, a.hd);
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -782,7 +799,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
   // Cluster size: each CTA of a cluster of cs takes ceil(chunks / cs) chunks, and the
   // (request, kv head) clusters run in waves of as many as the device holds at once.
   // Estimated time ~ waves x (chunks per CTA + fixed cost of a CTA, ~4 chunks).
-  const int total = a.Hkv * a.B;
+  const int total = a.Hkv * a.B * G;
   const int cmax = g_att_cluster ? g_att_cluster : 8;
   int best_cs = 0;
   long long best_cost = 0;
@@ -801,7 +818,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
   attr[1].val.clusterDim.x = best_cs;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(best_cs, a.Hkv, a.B);
+  cfg.gridDim = dim3(best_cs, a.Hkv, a.B * G);
   if (tc) return cudaLaunchKernelEx(&cfg, tree_attention_tc_kernel, a);
   return cudaLaunchKernelEx(&cfg, tree_attention_kernel, a);
 }

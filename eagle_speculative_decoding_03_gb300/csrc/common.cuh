@@ -65,6 +65,42 @@ EAGLE_DEV bool beats(float v, int id, float w, int wid) {
   return v > w || (v == w && id < wid);
 }
 
+// ------------------------------------------------ counter-based random numbers
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+// as 1, 2, 3", SC 2011): each round multiplies counter words 0 and 2 by the two round
+// constants, XORs the high halves of the products with the other two words and the key,
+// and permutes; the key advances by the two Weyl constants between rounds.
+EAGLE_DEV uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+// Gumbel noise -log(-log U) of a 32-bit word x, U = (x + 1/2) / 2^32: -log U is taken
+// from U itself below 1/2 and as -log1p(-(1 - U)) above, 1 - U = (2^32 - 1 - x + 1/2) / 2^32
+// formed from the exact integer, so that neither end loses its precision.
+EAGLE_DEV float gumbel_of_word(uint32_t x) {
+  const float e = x < 0x80000000u ? -logf((static_cast<float>(x) + 0.5f) * 2.3283064365386963e-10f)
+                                  : -log1pf(-(static_cast<float>(0xFFFFFFFFu - x) + 0.5f) * 2.3283064365386963e-10f);
+  return -logf(e);
+}
+// The Gumbel noise of token t of row i at depth s under a request's 64-bit seed: word
+// (t mod 128) / 32 of Philox(counter = (32 (t / 128) + t mod 32, i, s, 0), key = seed).
+EAGLE_DEV float token_gumbel(int t, int i, int s, unsigned long long seed) {
+  const uint4 w = philox4x32_10(make_uint4(32u * static_cast<uint32_t>(t >> 7) + (t & 31), static_cast<uint32_t>(i),
+                                           static_cast<uint32_t>(s), 0u),
+                                static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  const int j = (t & 127) >> 5;
+  return gumbel_of_word(j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w);
+}
+
 // named barrier among `nthreads` threads (id 1.. ; 0 is __syncthreads)
 EAGLE_DEV void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -261,6 +297,11 @@ struct EpiArgs {
   float* lm_val;           // [N][grid][k]  (each row's CTA lists contiguous)
   int* lm_id;              // [N][grid][k]
   int topk;
+  // sampled drafting (EPI_LMHEAD, seeds != null): the top-k is taken over logit + Gumbel
+  // noise of (request, frontier slot, depth) = (row / sample_rows, row % sample_rows,
+  // sample_depth), row = sample_row0 + the launch's row; the log-sum-exp stays unperturbed
+  const unsigned long long* seeds;
+  int sample_rows, sample_depth, sample_row0;
   // operand copy for the next GEMM (EPI_STORE, EPI_SWIGLU):
   // hl[2 row][m] = hi, hl[2 row + 1][m] = lo of value * hl_gamma[m] (hl_gamma may be null)
   uint16_t* hl;

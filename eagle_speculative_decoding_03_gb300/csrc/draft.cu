@@ -388,61 +388,7 @@ extern "C" eagle_status_t eagle_draft_check(eagle_draft_t* h, uint32_t* word) {
 // ------------------------------------------------------------- GEMM setup
 static GemmPlan base_plan(eagle_draft* h, const CUtensorMap& tm0, const CUtensorMap* tm1, const void* w0,
                           const void* w1, int M, int K, int m_split) {
-  GemmPlan p;
-  p.tc = h->tc;
-  if (p.tc) {
-    p.tm0 = tm0;
-    p.tm1 = tm1 ? *tm1 : tm0;
-  } else {
-    p.w0f = static_cast<const float*>(w0);
-    p.w1f = static_cast<const float*>(w1 ? w1 : w0);
-  }
-  GemmArgs& g = p.args;
-  memset(&g, 0, sizeof(g));
-  g.M = M;
-  g.K = K;
-  g.m_split = m_split;
-  g.part = h->part;
-  g.counters = h->counters;
-  g.err = h->err;
-  return p;
-}
-
-static EpiArgs epi_store(float* out, int ldo, const float* resid, int ldr, float* ss, int ss_ld) {
-  EpiArgs e;
-  memset(&e, 0, sizeof(e));
-  e.kind = EPI_STORE;
-  e.out = out;
-  e.ldo = ldo;
-  e.resid = resid;
-  e.ldr = ldr;
-  e.ss = ss;
-  e.ss_ld = ss_ld;
-  return e;
-}
-
-// Operand tile loaded by TMA from a bf16 hi/lo copy written by the producing kernel.
-static void tma_operand(GemmPlan& p, const uint16_t* hl, bool shared_sm = false) {
-  p.args.b.mode = B_TMA;
-  p.args.b_tma = 1;
-  p.b_hl = hl;
-  p.occ = shared_sm ? 2 : 1;
-}
-
-// The producing epilogue also writes the next GEMM's operand copy (value * gamma).
-static void write_operand(EpiArgs& e, uint16_t* hl, int ld, const float* gamma) {
-  e.hl = hl;
-  e.hl_ld = ld;
-  e.hl_gamma = gamma;
-}
-
-// The consumer applies the RMSNorm row scale in its epilogue.
-static void factored_norm(EpiArgs& e, const float* ss, int tiles, int ld, int d, float eps) {
-  e.nss = ss;
-  e.nss_tiles = tiles;
-  e.nss_ld = ld;
-  e.nss_d = d;
-  e.nss_eps = eps;
+  return gemm_plan(h->tc, tm0, tm1, w0, w1, M, K, m_split, h->part, h->counters, h->err);
 }
 
 static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t st, int kind) {
@@ -454,8 +400,21 @@ static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t 
 
 static LmPartials lm_partials(eagle_draft* h, int N);
 
+// Sampled drafting of the LM head's top-k: per-request seeds, rows per request and depth.
+struct SampleArgs {
+  const unsigned long long* seeds = nullptr;
+  int rows = 1, depth = 0;
+};
+
+static void set_sampling(EpiArgs& e, const SampleArgs& sa, int row0) {
+  e.seeds = sa.seeds;
+  e.sample_rows = sa.rows;
+  e.sample_depth = sa.depth;
+  e.sample_row0 = row0;
+}
+
 static eagle_status_t lm_head(eagle_draft* h, const float* a, const uint16_t* a_hl, int N, int topk,
-                              cudaStream_t st) {
+                              cudaStream_t st, const SampleArgs& sa = SampleArgs()) {
   const eagle_draft_config_t& c = h->cfg;
   if (a_hl && N > MAX_ROWS_PER_BLOCK) {
     // More rows than one TMEM accumulator pair holds: launches of <= 128 rows each, so the
@@ -477,6 +436,7 @@ static eagle_status_t lm_head(eagle_draft* h, const float* a, const uint16_t* a_
       e.lm_val = h->lm_val + r0 * G * topk;
       e.lm_id = h->lm_id + r0 * G * topk;
       e.topk = topk;
+      set_sampling(e, sa, r0);
       eagle_status_t r = run_gemm(h, p, n, st, EAGLE_K_LMHEAD);
       if (r != EAGLE_OK) return r;
     }
@@ -494,6 +454,7 @@ static eagle_status_t lm_head(eagle_draft* h, const float* a, const uint16_t* a_
   e.lm_val = h->lm_val;
   e.lm_id = h->lm_id;
   e.topk = topk;
+  set_sampling(e, sa, 0);
   return run_gemm(h, p, N, st, EAGLE_K_LMHEAD);
 }
 
@@ -539,6 +500,7 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
   t.vocab = c.vocab;
   t.root_tok = in->root_tok;
   t.cu_seqlens = in->cu_seqlens;
+  t.seeds = reinterpret_cast<const unsigned long long*>(in->seeds);
   t.node_tok = h->node_tok;
   t.node_parent = h->node_parent;
   t.node_depth = h->node_depth;
@@ -738,7 +700,11 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       if ((r = run_gemm(h, p, N, st, EAGLE_K_DOWN)) != EAGLE_OK) return r;
     }
     // frozen LM head: online log-sum-exp + top-k partials
-    if ((r = lm_head(h, a_cur, h->tc ? h->a_hl : nullptr, N, h->kids[s - 1], st)) != EAGLE_OK) return r;
+    SampleArgs sa;
+    sa.seeds = t.seeds;
+    sa.rows = rows;
+    sa.depth = s;
+    if ((r = lm_head(h, a_cur, h->tc ? h->a_hl : nullptr, N, h->kids[s - 1], st, sa)) != EAGLE_OK) return r;
     // children, values, next frontier
     {
       ExpandTrace tr;
@@ -816,7 +782,7 @@ extern "C" eagle_status_t eagle_draft_tree(eagle_draft_t* h, const eagle_draft_i
   }
   if (trc || !h->use_graph) return enqueue_tree(h, in, out, trc, st);
   std::vector<const void*> key = {reinterpret_cast<const void*>(static_cast<intptr_t>(in->B)), in->root_feat,
-                                  in->root_tok, in->k_cache, in->v_cache, in->cu_seqlens, out->tokens,
+                                  in->root_tok, in->k_cache, in->v_cache, in->cu_seqlens, in->seeds, out->tokens,
                                   out->parents, out->positions, out->logv, out->mask};
   if (!h->graph || key != h->graph_key) {
     if (h->graph) {

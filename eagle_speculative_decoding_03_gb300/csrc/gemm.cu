@@ -500,8 +500,10 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
     }
     named_bar(1, 128);
   } else {  // EPI_LMHEAD
+    // (with a factored RMSNorm of the operand, e.g. a final norm before the LM head, the
+    // row scale is applied here)
 #pragma unroll
-    for (int r = 0; r < 16; ++r) es.s->xch[r][tl] = v[r];
+    for (int r = 0; r < 16; ++r) es.s->xch[r][tl] = (e.nss && n0 + r < g.N) ? v[r] * es.rstd[n0 + r] : v[r];
     named_bar(1, 128);
     const int k = e.topk;
     for (int r = warp_q; r < 16; r += 4) {
@@ -527,7 +529,20 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
         e.lm_max[static_cast<size_t>(n) * g.MT + mt] = tmax;
         e.lm_sum[static_cast<size_t>(n) * g.MT + mt] = s;
       }
-      // top-k
+      // top-k (sampled drafting: of logit + Gumbel noise; one Philox call gives the lane's
+      // four tokens, t = tile * 128 + lane + 32 j -> word j of counter 32 tile + lane)
+      if (e.seeds) {
+        const int gr = e.sample_row0 + n;
+        const int b = gr / e.sample_rows, i = gr - b * e.sample_rows;
+        const unsigned long long sd = __ldg(e.seeds + b);
+        const uint4 w = philox4x32_10(make_uint4(32u * static_cast<uint32_t>(mt) + lane, static_cast<uint32_t>(i),
+                                                 static_cast<uint32_t>(e.sample_depth), 0u),
+                                      static_cast<uint32_t>(sd), static_cast<uint32_t>(sd >> 32));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (id[j] != INT_MAX) val[j] += gumbel_of_word(ws[j]);
+      }
       const int cnt = es.st_cnt[n];
       float* lv = es.lv + static_cast<size_t>(n) * k;
       int* li = es.li + static_cast<size_t>(n) * k;
@@ -1341,6 +1356,41 @@ int gemm_active_clusters(int S) {
   }
   cache[dev][S] = n;
   return n;
+}
+
+GemmPlan gemm_plan(bool tc, const CUtensorMap& tm0, const CUtensorMap* tm1, const void* w0, const void* w1,
+                   int M, int K, int m_split, float* part, int* counters, unsigned* err) {
+  GemmPlan p;
+  p.tc = tc;
+  if (tc) {
+    p.tm0 = tm0;
+    p.tm1 = tm1 ? *tm1 : tm0;
+  } else {
+    p.w0f = static_cast<const float*>(w0);
+    p.w1f = static_cast<const float*>(w1 ? w1 : w0);
+  }
+  GemmArgs& g = p.args;
+  memset(&g, 0, sizeof(g));
+  g.M = M;
+  g.K = K;
+  g.m_split = m_split;
+  g.part = part;
+  g.counters = counters;
+  g.err = err;
+  return p;
+}
+
+EpiArgs epi_store(float* out, int ldo, const float* resid, int ldr, float* ss, int ss_ld) {
+  EpiArgs e;
+  memset(&e, 0, sizeof(e));
+  e.kind = EPI_STORE;
+  e.out = out;
+  e.ldo = ldo;
+  e.resid = resid;
+  e.ldr = ldr;
+  e.ss = ss;
+  e.ss_ld = ss_ld;
+  return e;
 }
 
 // Fill the launch geometry of a GEMM over N rows.

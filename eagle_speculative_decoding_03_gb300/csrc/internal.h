@@ -28,6 +28,34 @@ cudaError_t allow_max_smem(const void* func, size_t* granted = nullptr);
 size_t max_dyn_smem(const void* func);
 
 bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K, int box_rows = BM);
+
+// A GEMM over weights [M][K] (rows [0, m_split) from map / pointer 0, the rest from 1),
+// with the caller's split-K scratch, arrival counters and device error word.
+GemmPlan gemm_plan(bool tc, const CUtensorMap& tm0, const CUtensorMap* tm1, const void* w0, const void* w1,
+                   int M, int K, int m_split, float* part, int* counters, unsigned* err);
+// EPI_STORE epilogue: out = acc (+ resid); per-tile sums of squares into ss (nullable).
+EpiArgs epi_store(float* out, int ldo, const float* resid, int ldr, float* ss, int ss_ld);
+// Operand tile loaded by TMA from a bf16 hi/lo copy written by the producing kernel.
+inline void tma_operand(GemmPlan& p, const uint16_t* hl, bool shared_sm = false) {
+  p.args.b.mode = B_TMA;
+  p.args.b_tma = 1;
+  p.b_hl = hl;
+  p.occ = shared_sm ? 2 : 1;
+}
+// The producing epilogue also writes the next GEMM's operand copy (value * gamma).
+inline void write_operand(EpiArgs& e, uint16_t* hl, int ld, const float* gamma) {
+  e.hl = hl;
+  e.hl_ld = ld;
+  e.hl_gamma = gamma;
+}
+// The consumer applies the RMSNorm row scale in its epilogue (per-tile sums of squares).
+inline void factored_norm(EpiArgs& e, const float* ss, int tiles, int ld, int d, float eps) {
+  e.nss = ss;
+  e.nss_tiles = tiles;
+  e.nss_ld = ld;
+  e.nss_d = d;
+  e.nss_eps = eps;
+}
 int num_sms();
 int gemm_active_clusters(int S);
 bool plan_gemm(GemmPlan& p, int N);
@@ -51,6 +79,8 @@ struct AttnArgs {
   int tree_upto;            // rows that exist so far (through this depth)
   int B, Hq, Hkv, hd;
   int max_splits;           // prefix chunks + 1 (tree chunk) of the longest request
+  int row_groups;           // > 1: a request's rows run as this many groups of rows_per_group
+  int rows_per_group;       // (tensor-core kernel only; 0 / 1 = one group)
   float* out;               // [N][Hq*hd]
   uint16_t* out_hl;         // [2N][Hq*hd] bf16 hi / lo rows of out (operand of the O projection)
 };
@@ -58,6 +88,8 @@ size_t attn_smem_bytes(int qv, int hd);
 size_t attn_merge_capacity(int qv, int hd);
 cudaError_t attn_setup_attributes();
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl);
+// Largest rows_per_group the tensor-core kernel takes for Hq / Hkv query heads per KV head.
+int attn_rows_per_group(int Hq, int Hkv);
 
 // --------------------------------------------------------- tree kernels
 struct TreeArgs {
@@ -73,6 +105,7 @@ struct TreeArgs {
   // inputs
   const int* root_tok;
   const int* cu_seqlens;
+  const unsigned long long* seeds;   // [B] sampled drafting, or null (greedy top-k)
   // node table [B][max_nodes]
   int* node_tok;
   int* node_parent;

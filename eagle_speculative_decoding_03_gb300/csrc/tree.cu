@@ -385,13 +385,20 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
     if (rank < kids) sel[rank] = e;
   }
   __syncthreads();
-  // ---- children in token-id order
+  // ---- children in token-id order (greedy) or draw order (sampled)
   const int u = s_u;
   if (tid < kids) {
-    const float v = sel[tid].x;
+    float v = sel[tid].x;
     int id = __float_as_int(sel[tid].y);
     int rank = 0;
-    for (int j = 0; j < kids; ++j) rank += __float_as_int(sel[j].y) < id ? 1 : 0;
+    if (t.seeds) {
+      // sampled drafting: sel holds logit + Gumbel noise in draw order; the children keep
+      // that order and their log-probabilities drop the noise again
+      rank = tid;
+      if (id >= 0 && id < t.vocab) v -= token_gumbel(id, i, s, __ldg(t.seeds + b));
+    } else {
+      for (int j = 0; j < kids; ++j) rank += __float_as_int(sel[j].y) < id ? 1 : 0;
+    }
     if (id < 0 || id >= t.vocab) {
       atomicOr(t.err, DEVERR_SELECT);
       id = 0;

@@ -125,12 +125,22 @@ typedef struct {
   const void*    k_cache;    /* `dtype` [sum n_b, Hkv, hd] */
   const void*    v_cache;    /* `dtype` [sum n_b, Hkv, hd] */
   const int32_t* cu_seqlens; /* [B + 1], cu_seqlens[0] = 0, n_b = cu_seqlens[b+1] - cu_seqlens[b] */
+  const uint64_t* seeds;     /* [B] or NULL.  NULL: greedy drafting (each node's k most likely tokens).
+                                Set: sampled drafting ("EAGLE-1 - autoregressive feature drafting",
+                                zackli.ai: the draft samples t-hat ~ p-hat): a node's k children are k
+                                tokens drawn without replacement from the draft's distribution, the top-k
+                                of log p + Gumbel noise.  The noise of token t of frontier slot i at depth s
+                                of request b is -log(-log U), U = (x + 1/2) / 2^32 with x word
+                                (t mod 128) / 32 of Philox4x32-10(counter = (32 (t / 128) + t mod 32, i, s,
+                                0), key = seeds[b] as (low, high) 32-bit words).  Children are then kept in
+                                draw order (largest perturbed value first) instead of token order; path
+                                values add the unperturbed log-probabilities. */
 } eagle_draft_inputs_t;
 
 /* Outputs (device).  S = kept + 1 slots per request (eagle_draft_info_t.slots):
  * slot 0 is the root (token root_tok, parent -1, position n_b, logv 0); slots 1.. are the
- * kept nodes in generation order (depth, then the parent's frontier slot, then token id),
- * so a parent always precedes its children. */
+ * kept nodes in generation order (depth, then the parent's frontier slot, then token id -
+ * draw order when sampling), so a parent always precedes its children. */
 typedef struct {
   int32_t* tokens;     /* [B, S] */
   int32_t* parents;    /* [B, S] parent slot, -1 for the root */
@@ -149,7 +159,7 @@ typedef struct {
   float*   y;           /* [depth][N_max][d]       after O-proj + residual */
   float*   a;           /* [depth][N_max][d]       layer output (next feature f' / latent a) */
   float*   lse;         /* [depth][N_max]          log-sum-exp of the row's logits */
-  int32_t* children;    /* [depth][N_max][k_max]   children token ids (ascending) */
+  int32_t* children;    /* [depth][N_max][k_max]   children token ids (ascending; draw order when sampling) */
   float*   child_logp;  /* [depth][N_max][k_max]   their log-probabilities */
   int32_t* frontier;    /* [depth][max_batch][f_max] node ids expanded at the next depth */
   int32_t* final_nodes; /* [max_batch][S]          node id of every emitted slot */
@@ -254,6 +264,89 @@ EAGLE_API eagle_status_t eagle_draft_check(eagle_draft_t* handle, uint32_t* word
 
 /* Frees the workspace and the handle.  NULL is accepted. */
 EAGLE_API void eagle_draft_destroy(eagle_draft_t* handle);
+
+/* ------------------------------------------------------------------------------------
+ * Verification side: the target's one pass over an emitted tree ("Tree attention in one
+ * verification pass", aicassindra.com tm_eagle_deep) and greedy acceptance ("How
+ * speculative decoding works", kaushalya.io, steps "target verification" / "output of the
+ * round"; "Acceptance length under a tree", aicassindra.com).
+ *
+ * The target is one Llama-style decoder layer (RMSNorm, QKV, rotary, grouped-query
+ * attention, O, RMSNorm, SwiGLU MLP) with its own weights, between the frozen embedding
+ * and the frozen LM head, with a final RMSNorm before the LM head.  Every slot of the
+ * tree is one row: token tokens[b][i] at position positions[b][i], attending to the
+ * request's whole verified prefix (the target's own post-RoPE cache) and to the slots j
+ * with mask[b][i][j] = 1 (its ancestors and itself).  The result per slot is the target's
+ * most likely next token after that slot's path (ties to the lower id), its
+ * log-probability and the log-sum-exp of the logits.  No [slots x |V|] logits are stored.
+ * bf16 weights and cache, head_dim 128 only.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  int32_t d, n_heads, n_kv_heads, head_dim, d_ff, vocab;  /* as in eagle_draft_config_t */
+  float   rms_eps, rope_theta;
+  int32_t dtype;        /* EAGLE_DTYPE_BF16 */
+  int32_t max_batch;    /* largest B a call may pass */
+  int32_t max_slots;    /* largest S (slots per request, root included); <= 64, max_batch * max_slots <= 256 */
+  int32_t max_prefix;   /* largest prefix length n_b; positions must be < max_prefix + max_slots + 1 */
+  int32_t flags;        /* EAGLE_FLAG_NO_PDL or 0 */
+} eagle_verify_config_t;
+
+/* Target weights (device, bf16 [out, in] row-major; gains f32), borrowed for the handle's
+ * lifetime.  embed and w_lm are the frozen tables the draft shares with the target. */
+typedef struct {
+  const void*  embed;       /* [vocab, d] */
+  const float* attn_norm;   /* [d] */
+  const void*  w_qkv;       /* [(Hq + 2 Hkv) hd, d] */
+  const void*  w_o;         /* [d, Hq hd] */
+  const float* mlp_norm;    /* [d] */
+  const void*  w_gate;      /* [d_ff, d] */
+  const void*  w_up;        /* [d_ff, d] */
+  const void*  w_down;      /* [d, d_ff] */
+  const float* final_norm;  /* [d] */
+  const void*  w_lm;        /* [vocab, d] */
+} eagle_verify_weights_t;
+
+/* One call's inputs (device): the emitted tree as eagle_draft_tree writes it, and the
+ * target's verified-prefix cache, packed like the draft's. */
+typedef struct {
+  int32_t        B;            /* requests, 1..max_batch */
+  int32_t        S;            /* slots per request, 1..max_slots */
+  const int32_t* tokens;       /* [B, S] */
+  const int32_t* positions;    /* [B, S] */
+  const uint8_t* mask;         /* [B, S, S] 1 = slot j is visible to slot i (ancestor or self) */
+  const int32_t* parents;      /* [B, S] parent slot (-1 for the root); needed only for acceptance */
+  const void*    k_cache;      /* bf16 [sum n_b, Hkv, hd] target keys, post-RoPE */
+  const void*    v_cache;      /* bf16 [sum n_b, Hkv, hd] */
+  const int32_t* cu_seqlens;   /* [B + 1] */
+} eagle_verify_inputs_t;
+
+/* Outputs (device; any of them may be NULL, acceptance runs when accept_len is set). */
+typedef struct {
+  int32_t* top_id;        /* [B, S] the target's most likely next token after slot i's path */
+  float*   top_logp;      /* [B, S] its log-probability */
+  float*   lse;           /* [B, S] log-sum-exp of the slot's logits */
+  float*   hidden;        /* [B, S, d] layer output before the final norm */
+  int32_t* accept_len;    /* [B] accepted draft tokens (root excluded) */
+  int32_t* accept_slots;  /* [B, S] the accepted slots in path order, -1 after accept_len */
+  int32_t* correction;    /* [B] the target's most likely token after the accepted path */
+} eagle_verify_outputs_t;
+
+typedef struct eagle_verify eagle_verify_t;
+
+/* Validates the shapes, allocates the workspace (owned by the handle), builds the weights'
+ * TMA descriptors and the rotary tables.  EAGLE_ERR_UNSUPPORTED outside bf16 / head_dim
+ * 128 / multiples of 128 / the slot limits above. */
+EAGLE_API eagle_status_t eagle_verify_create(const eagle_verify_config_t* cfg, const eagle_verify_weights_t* weights,
+                                             eagle_verify_t** out_handle);
+/* Enqueues one verification pass (and, with accept_len set, the greedy acceptance walk)
+ * on `stream`.  Stream-ordered and asynchronous; kernel-side problems (a token outside
+ * [0, vocab), a position past the rotary table, a parent that does not precede its slot)
+ * set the handle's device error word, read by eagle_verify_check. */
+EAGLE_API eagle_status_t eagle_verify_tree(eagle_verify_t* handle, const eagle_verify_inputs_t* inputs,
+                                           const eagle_verify_outputs_t* outputs, void* stream);
+/* Synchronises; EAGLE_ERR_DEVICE (bits in *word) if the device error word is set, then clears it. */
+EAGLE_API eagle_status_t eagle_verify_check(eagle_verify_t* handle, uint32_t* word);
+EAGLE_API void eagle_verify_destroy(eagle_verify_t* handle);
 
 /* Thread-local description of the last error (never NULL). */
 EAGLE_API const char* eagle_draft_last_error(void);

@@ -32,6 +32,8 @@ def select_requests(cfg, I, out, tr, reqs):
     lens = [int(cu[b + 1] - cu[b]) for b in reqs]
     sub = {"root_feat": I["root_feat"][reqs], "root_tok": I["root_tok"][reqs],
            "cu_seqlens": np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)}
+    if "seeds" in I:
+        sub["seeds"] = I["seeds"][reqs]
     for key in ("k_cache", "v_cache"):
         sub[key] = np.concatenate([I[key][int(cu[b]):int(cu[b + 1])] for b in reqs], axis=0)
     o = {k: v[reqs] for k, v in out.items()}

@@ -80,12 +80,38 @@ def test_null_handles(lib):
     lib.eagle_draft_destroy(None)
 
 
-def test_struct_layout_matches_header():
-    # the config struct: 14 int/float fields + 16 branching + 3 = 33 four-byte fields
-    assert C.sizeof(eb.Config) == 33 * 4
-    assert C.sizeof(eb.Weights) == 11 * 8
-    assert C.sizeof(eb.Inputs) == 6 * 8
-    assert C.sizeof(eb.Info) == 8 * 4 + 8
+STRUCTS = [("eagle_draft_config_t", "Config"), ("eagle_draft_weights_t", "Weights"),
+           ("eagle_draft_inputs_t", "Inputs"), ("eagle_draft_outputs_t", "Outputs"),
+           ("eagle_draft_trace_t", "Trace"), ("eagle_draft_info_t", "Info"),
+           ("eagle_verify_config_t", "VerifyConfig"), ("eagle_verify_weights_t", "VerifyWeights"),
+           ("eagle_verify_inputs_t", "VerifyInputs"), ("eagle_verify_outputs_t", "VerifyOutputs")]
+
+
+def test_struct_layout_matches_header(tmp_path):
+    """Every struct the binding passes has the header's size and field offsets (the header
+    compiled by the host C compiler)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void) {"]
+    for cname, pyname in STRUCTS:
+        lines.append(f'  printf("{pyname} size %zu\\n", sizeof({cname}));')
+        for f, _ in getattr(eb, pyname)._fields_:
+            lines.append(f'  printf("{pyname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("  return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, str(src), "-o", str(exe)], check=True)
+    got = [x for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n") if x]
+    assert len(got) == sum(1 + len(getattr(eb, p)._fields_) for _, p in STRUCTS)
+    for line in got:
+        pyname, field, value = line.split()
+        cls = getattr(eb, pyname)
+        want = C.sizeof(cls) if field == "size" else getattr(cls, field).offset
+        assert int(value) == want, (pyname, field, value, want)
 
 
 def test_noalloc_binding_rejects_wrong_dtypes(lib):
