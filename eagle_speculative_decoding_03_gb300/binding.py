@@ -83,7 +83,7 @@ class VerifyInputs(C.Structure):
         [(n, C.c_void_p) for n in ("tokens", "positions", "mask", "parents", "k_cache", "v_cache", "cu_seqlens")]
 
 
-VERIFY_OUTPUTS = ("top_id", "top_logp", "lse", "hidden", "accept_len", "accept_slots", "correction")
+VERIFY_OUTPUTS = ("top_id", "top_logp", "lse", "hidden", "logits", "accept_len", "accept_slots", "correction")
 
 
 class VerifyOutputs(C.Structure):
@@ -131,6 +131,8 @@ def load(path: str = LIB_PATH):
     lib.eagle_verify_check.restype = C.c_int
     lib.eagle_verify_destroy.argtypes = [P]
     lib.eagle_verify_destroy.restype = None
+    lib.eagle_speculative_accept.argtypes = [C.c_int32, C.c_int32, C.c_int32, P, P, P, P, P, P, P, P, P, P]
+    lib.eagle_speculative_accept.restype = C.c_int
     lib.eagle_draft_last_error.argtypes = []
     lib.eagle_draft_last_error.restype = C.c_char_p
     _lib = lib
@@ -334,7 +336,7 @@ class EagleVerify:
             pass
 
     def verify(self, tree: dict, cache: dict, cu_seqlens, accept: bool = True, hidden: bool = False,
-               stream=None) -> dict:
+               logits: bool = False, stream=None) -> dict:
         """tree: device tensors tokens / positions / parents [B,S] int32 and mask [B,S,S] uint8
         (as eagle_draft_tree emits them); cache: the target's k_cache / v_cache."""
         import torch
@@ -345,6 +347,8 @@ class EagleVerify:
                "lse": torch.empty((B, S), dtype=torch.float32, device=dev)}
         if hidden:
             out["hidden"] = torch.empty((B, S, self.cfg.d), dtype=torch.float32, device=dev)
+        if logits:
+            out["logits"] = torch.empty((B, S, self.cfg.vocab), dtype=torch.float32, device=dev)
         if accept:
             out["accept_len"] = torch.empty((B,), dtype=torch.int32, device=dev)
             out["accept_slots"] = torch.empty((B, S), dtype=torch.int32, device=dev)
@@ -364,3 +368,27 @@ class EagleVerify:
         if st != EAGLE_OK:
             raise EagleError(st, load().eagle_draft_last_error().decode())
         return w.value
+
+
+def speculative_accept(tree: dict, logits_target, logits_draft, seeds, stream=None) -> dict:
+    """Multi-round speculative sampling over emitted trees (device tensors): tokens / parents
+    [B,S] int32, logits [B,S,V] float32, seeds [B] (int64 bits of the uint64 seeds).
+    Returns accept_len [B], accept_slots [B,S], correction [B] and the error word [1]."""
+    import torch
+    B, S = (int(x) for x in tree["tokens"].shape)
+    V = int(logits_target.shape[-1])
+    if logits_target.dtype != torch.float32 or logits_draft.dtype != torch.float32:
+        raise EagleError(EAGLE_ERR_INVALID_ARG, "speculative_accept: logits must be float32")
+    if tuple(logits_target.shape) != (B, S, V) or tuple(logits_draft.shape) != (B, S, V):
+        raise EagleError(EAGLE_ERR_INVALID_ARG, "speculative_accept: logits must be [B, S, vocab]")
+    dev = tree["tokens"].device
+    out = {"accept_len": torch.empty((B,), dtype=torch.int32, device=dev),
+           "accept_slots": torch.empty((B, S), dtype=torch.int32, device=dev),
+           "correction": torch.empty((B,), dtype=torch.int32, device=dev),
+           "err": torch.zeros((1,), dtype=torch.int32, device=dev)}
+    st = None if stream is None else stream.cuda_stream
+    _check(load().eagle_speculative_accept(B, S, V, _ptr(tree["tokens"]), _ptr(tree["parents"]),
+                                           _ptr(logits_target.contiguous()), _ptr(logits_draft.contiguous()),
+                                           _ptr(seeds), _ptr(out["accept_len"]), _ptr(out["accept_slots"]),
+                                           _ptr(out["correction"]), _ptr(out["err"]), st))
+    return out

@@ -136,3 +136,56 @@ ALL = {**CONFIGS, **SMALL}
 
 def get(name: str) -> DraftConfig:
     return ALL[name]
+
+
+@dataclass(frozen=True)
+class DFlashConfig:
+    """A DFlash block-parallel draft ("DFlash-1: parallel block + KV injection", zackli.ai):
+    ``layers`` draft layers, a block of the anchor plus ``gamma`` mask slots, the top-``k``
+    tokens of each mask slot; the target's fused context is injected as per-layer KV."""
+    name: str
+    d: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    d_ff: int
+    vocab: int
+    rms_eps: float
+    rope_theta: float
+    dtype: str
+    layers: int
+    gamma: int
+    k: int = 1
+    B: int = 1
+    prefix: Tuple[int, int] = (0, 0)
+    seed: int = 1000
+    logit_std: float = 3.0
+    gamma_jitter: float = 0.0
+    mask_token: int = -1       # -1: the last id of the table
+
+    @property
+    def mask_id(self) -> int:
+        return self.vocab - 1 if self.mask_token < 0 else self.mask_token
+
+    @property
+    def qkv_dim(self) -> int:
+        return (self.n_heads + 2 * self.n_kv_heads) * self.head_dim
+
+    @property
+    def attn_dim(self) -> int:
+        return self.n_heads * self.head_dim
+
+    def with_(self, **kw) -> "DFlashConfig":
+        return replace(self, **kw)
+
+
+DFLASH = {
+    # the Llama-3-8B-shaped head as a 5-layer DFlash drafting a block of 16 ("A 5-layer DFlash
+    # drafting 16"), prefix 2048, B=1
+    "dflash_b1": DFlashConfig(name="dflash_b1", **LLAMA3_8B_HEAD, layers=5, gamma=16, k=1, B=1,
+                              prefix=(2048, 2048), seed=1006),
+    "small_dflash": DFlashConfig(
+        name="small_dflash", d=512, n_heads=4, n_kv_heads=2, head_dim=128, d_ff=1280, vocab=4096,
+        rms_eps=1e-6, rope_theta=1e4, dtype="bf16", layers=3, gamma=8, k=3, B=3, prefix=(37, 301),
+        seed=2006, gamma_jitter=0.1),
+}

@@ -302,6 +302,7 @@ struct EpiArgs {
   // sample_depth), row = sample_row0 + the launch's row; the log-sum-exp stays unperturbed
   const unsigned long long* seeds;
   int sample_rows, sample_depth, sample_row0;
+  float* logits;           // EPI_LMHEAD (nullable): the rows' full logits [N][M] (after the factored norm)
   // operand copy for the next GEMM (EPI_STORE, EPI_SWIGLU):
   // hl[2 row][m] = hi, hl[2 row + 1][m] = lo of value * hl_gamma[m] (hl_gamma may be null)
   uint16_t* hl;

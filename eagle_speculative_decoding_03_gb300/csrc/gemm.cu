@@ -446,6 +446,11 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
 #pragma unroll
     for (int r = 0; r < 16; ++r)   // (a factored RMSNorm of the operand - a final norm - applies here)
       key[r] = !tvalid ? -INFINITY : (e.nss && n0 + r < g.N) ? v[r] * es.rstd[n0 + r] : v[r];
+    if (e.logits && tvalid) {   // (optional) the full logits, one coalesced row segment per row
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (n0 + r < g.N) e.logits[static_cast<size_t>(n0 + r) * g.M + tok] = key[r];
+    }
     // this tile's log-sum-exp state of every row: per warp (max, sum of exp) with the 16 rows'
     // shuffle chains side by side, combined over the 4 warps by one thread per row below
     {

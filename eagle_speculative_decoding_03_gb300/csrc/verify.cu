@@ -420,6 +420,7 @@ eagle_status_t enqueue_verify(eagle_verify* h, const eagle_verify_inputs_t* in, 
       e.kind = EPI_LMHEAD;
       e.topk = 1;
       factored_norm(e, h->ss_h + r0, dt, nmax, d, c.rms_eps);
+      if (out->logits) e.logits = out->logits + static_cast<size_t>(r0) * c.vocab;
       if (!plan_gemm(p, n)) return vfail(EAGLE_ERR_UNSUPPORTED, "verify LM head does not fit");
       G = p.grid;
       e.lm_max = h->lm_max + r0 * T;

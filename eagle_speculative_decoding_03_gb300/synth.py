@@ -167,3 +167,57 @@ def make_target_cache(cfg: DraftConfig, inp: dict, seed_offset: int = 0) -> dict
     shape = (int(inp["cu_seqlens"][-1]), cfg.n_kv_heads, cfg.head_dim)
     return {"k_cache": normal(shape, (s, 48), 1.0, cfg.dtype),
             "v_cache": normal(shape, (s, 49), 1.0, cfg.dtype)}
+
+
+# -------------------------------------------------- DFlash block-parallel draft
+LAYER_NAMES = ("attn_norm", "w_qkv", "w_o", "mlp_norm", "w_gate", "w_up", "w_down")
+
+
+def make_dflash_weights(cfg) -> dict:
+    """Per-layer weights of the draft stack (the recipe of ``make_weights``), the final
+    RMSNorm gain, the frozen embedding and the frozen LM head.  The LM head reads a
+    normalised state (rms ~ 1), so its scale is logit_std / sqrt(d)."""
+    d, V, ff, s, dt = cfg.d, cfg.vocab, cfg.d_ff, cfg.seed, cfg.dtype
+
+    def gain(key):
+        if cfg.gamma_jitter:
+            return normal((d,), (s, key), cfg.gamma_jitter, "f32", 1.0)
+        return np.ones(d, np.float32)
+
+    layers = []
+    for l in range(cfg.layers):
+        base = 100 + 10 * l
+        layers.append({
+            "attn_norm": gain(base),
+            "w_qkv": normal((cfg.qkv_dim, d), (s, base + 1), (1.0 / d) ** 0.5, dt),
+            "w_o": normal((d, cfg.attn_dim), (s, base + 2), (1.0 / cfg.attn_dim) ** 0.5, dt),
+            "mlp_norm": gain(base + 3),
+            "w_gate": normal((ff, d), (s, base + 4), (1.0 / d) ** 0.5, dt),
+            "w_up": normal((ff, d), (s, base + 5), (1.0 / d) ** 0.5, dt),
+            "w_down": normal((d, ff), (s, base + 6), (1.0 / ff) ** 0.5, dt),
+        })
+    return {"embed": normal((V, d), (s, 1), 1.0, dt),
+            "w_lm": normal((V, d), (s, 11), cfg.logit_std / d ** 0.5, dt),
+            "final_norm": gain(12), "layers": layers}
+
+
+def make_dflash_inputs(cfg, B: int | None = None, seed_offset: int = 0) -> dict:
+    """Anchor tokens, prefix lengths and every layer's injected context keys / values of the
+    verified prefix (packed [sum n_b, Hkv, hd], keys post-RoPE, N(0,1))."""
+    B = cfg.B if B is None else B
+    s = cfg.seed + 7919 * seed_offset
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([s, 20])))
+    lo, hi = cfg.prefix
+    n = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    cu = np.zeros(B + 1, np.int32)
+    cu[1:] = np.cumsum(n)
+    anchor = rng.integers(0, cfg.vocab - 1, size=B).astype(np.int32)
+    shape = (int(cu[-1]), cfg.n_kv_heads, cfg.head_dim)
+    return {"anchor": anchor, "cu_seqlens": cu,
+            "ctx_k": [normal(shape, (s, 60 + 2 * l), 1.0, cfg.dtype) for l in range(cfg.layers)],
+            "ctx_v": [normal(shape, (s, 61 + 2 * l), 1.0, cfg.dtype) for l in range(cfg.layers)]}
+
+
+def dflash_oracle_cfg(cfg) -> dict:
+    return dict(d=cfg.d, n_heads=cfg.n_heads, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,
+                rms_eps=cfg.rms_eps, rope_theta=cfg.rope_theta, gamma=cfg.gamma, mask_token=cfg.mask_id)

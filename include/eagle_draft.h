@@ -326,6 +326,7 @@ typedef struct {
   float*   top_logp;      /* [B, S] its log-probability */
   float*   lse;           /* [B, S] log-sum-exp of the slot's logits */
   float*   hidden;        /* [B, S, d] layer output before the final norm */
+  float*   logits;        /* [B, S, vocab] the target's logits per slot (input of eagle_speculative_accept) */
   int32_t* accept_len;    /* [B] accepted draft tokens (root excluded) */
   int32_t* accept_slots;  /* [B, S] the accepted slots in path order, -1 after accept_len */
   int32_t* correction;    /* [B] the target's most likely token after the accepted path */
@@ -347,6 +348,31 @@ EAGLE_API eagle_status_t eagle_verify_tree(eagle_verify_t* handle, const eagle_v
 /* Synchronises; EAGLE_ERR_DEVICE (bits in *word) if the device error word is set, then clears it. */
 EAGLE_API eagle_status_t eagle_verify_check(eagle_verify_t* handle, uint32_t* word);
 EAGLE_API void eagle_verify_destroy(eagle_verify_t* handle);
+
+/* Multi-round speculative sampling over emitted trees ("Speculative Decoding Deep Dive III",
+ * zackli.ai, EAGLE-1: tree attention plus multi-round speculative sampling; "How speculative
+ * decoding works", kaushalya.io: accept a drafted token with probability min(1, p/q), else draw
+ * from the renormalised residual max(0, p - q)).  Per request, from the root, the children of
+ * the current slot are tried in slot order (the draw order of sampled drafting): child x is
+ * accepted when U * q(x) < p(x); on rejection the target becomes norm(max(0, p - q)) and x leaves
+ * the proposal (q restricted to the untried tokens, renormalised).  The walk moves to an accepted
+ * child; where none is accepted (or at a leaf) one token is drawn from the current target by
+ * Gumbel-max, and the walk ends.  p and q at slot u are the softmax of the target's and the
+ * draft's logits there (the draft's are those u's children were drawn from).  Random numbers:
+ * Philox4x32-10 keyed by seeds[b]: trying child slot c uses U = (x + 1/2) / 2^32, x word 0 of
+ * counter (c, 0, 0, 2); the token drawn at slot u after r rejections takes the Gumbel noise of
+ * word (t mod 128) / 32 of counter (32 (t / 128) + t mod 32, u, r, 1) for token t.
+ * Device pointers: tokens, parents [B, S] int32 (as eagle_draft_tree emits them; S <= 64);
+ * logits_target, logits_draft [B, S, vocab] f32; seeds [B] uint64; outputs accept_len [B],
+ * accept_slots [B, S] (accepted slots in path order, -1 after), correction [B] (the drawn
+ * token).  *err_word (device, caller-owned) gets EAGLE_DEVERR_TOKEN for a token outside
+ * [0, vocab) or a parent that does not precede its slot, EAGLE_DEVERR_SELECT when no token had
+ * positive probability.  Allocates nothing; stream-ordered. */
+EAGLE_API eagle_status_t eagle_speculative_accept(int32_t B, int32_t S, int32_t vocab, const int32_t* tokens,
+                                                  const int32_t* parents, const float* logits_target,
+                                                  const float* logits_draft, const uint64_t* seeds,
+                                                  int32_t* accept_len, int32_t* accept_slots, int32_t* correction,
+                                                  uint32_t* err_word, void* stream);
 
 /* Thread-local description of the last error (never NULL). */
 EAGLE_API const char* eagle_draft_last_error(void);
