@@ -22,7 +22,7 @@ TREE_STATIC, TREE_DYNAMIC = 1, 2
 FEAT_F, FEAT_FUSED = 1, 3
 FLAG_NO_GRAPH, FLAG_NO_PDL, FLAG_GEMM_TWO_CTA = 1, 2, 4
 MAX_DEPTH = 16
-KERNEL_KINDS = 13
+KERNEL_KINDS = 14
 DEVERR_TIMEOUT, DEVERR_PREFIX, DEVERR_TOKEN, DEVERR_SELECT = 1, 2, 4, 8
 
 

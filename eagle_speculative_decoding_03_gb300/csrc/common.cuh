@@ -269,7 +269,7 @@ struct BSrc {
   int emb_bf16;
 };
 
-enum EpiKind : int { EPI_STORE = 0, EPI_QKV = 1, EPI_LMHEAD = 2, EPI_SWIGLU = 3 };
+enum EpiKind : int { EPI_STORE = 0, EPI_QKV = 1, EPI_LMHEAD = 2, EPI_SWIGLU = 3, EPI_LOGITS = 4 };
 
 struct EpiArgs {
   int kind;
@@ -302,7 +302,8 @@ struct EpiArgs {
   // sample_depth), row = sample_row0 + the launch's row; the log-sum-exp stays unperturbed
   const unsigned long long* seeds;
   int sample_rows, sample_depth, sample_row0;
-  float* logits;           // EPI_LMHEAD (nullable): the rows' full logits [N][M] (after the factored norm)
+  float* logits;           // EPI_LOGITS, or EPI_LMHEAD (nullable): the rows' full logits [N][M]
+                           // (after the factored norm)
   // operand copy for the next GEMM (EPI_STORE, EPI_SWIGLU):
   // hl[2 row][m] = hi, hl[2 row + 1][m] = lo of value * hl_gamma[m] (hl_gamma may be null)
   uint16_t* hl;

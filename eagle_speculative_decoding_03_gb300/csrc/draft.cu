@@ -62,6 +62,7 @@ struct eagle_draft {
   float *ss_h = nullptr, *ss_y = nullptr, *g_root = nullptr, *tk = nullptr, *tv = nullptr;
   float *rope_cos = nullptr, *rope_sin = nullptr, *part = nullptr;
   float *lm_max = nullptr, *lm_sum = nullptr, *lm_val = nullptr;
+  float* logits = nullptr;   // [N_max][vocab] LM heads over many rows: logits, then a select kernel
   // bf16 hi/lo operand copies [2 N_max][K] written by the producing epilogue (tensor-core path)
   uint16_t *xa_hl = nullptr, *o_hl = nullptr, *xm_hl = nullptr, *s_hl = nullptr, *a_hl = nullptr, *fc_hl = nullptr;
   int *lm_id = nullptr, *counters = nullptr;
@@ -85,7 +86,8 @@ struct eagle_draft {
 };
 
 static const char* kKernelNames[EAGLE_K_COUNT] = {"init", "fc3", "fc", "qkv_rope", "attention", "o_proj",
-                                                  "gate_up", "down", "lm_head", "expand", "rerank", "lm_merge", "fc_operand"};
+                                                  "gate_up", "down", "lm_head", "expand", "rerank", "lm_merge", "fc_operand",
+                                                  "lm_select"};
 
 // Event pair around one launch (profiling mode only).
 struct ProfScope {
@@ -112,6 +114,12 @@ struct ProfScope {
 };
 
 static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// LM-head launches of at least this many rows store the logits and select in a second
+// kernel; fewer rows keep the log-sum-exp and top-k in the GEMM's epilogue.  (The fused
+// epilogue's per-row work grows with the rows of a tile and, past a few dozen rows, outlasts
+// the tile's weight stream.)
+constexpr int LM_LOGITS_MIN_ROWS = 64;
 
 // --------------------------------------------------------------- validation
 static eagle_status_t validate(const eagle_draft_config_t& c, const eagle_draft_weights_t* w) {
@@ -192,6 +200,7 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   h->lm_val = cv.take<float>(lmn * KMAX);
   h->lm_id = cv.take<int>(lmn * KMAX);
   h->counters = cv.take<int>(16384);
+  h->logits = (h->tc && n >= LM_LOGITS_MIN_ROWS) ? cv.take<float>(static_cast<size_t>(n) * c.vocab) : nullptr;
   const size_t nn = static_cast<size_t>(B) * h->max_nodes;
   h->node_tok = cv.take<int>(nn);
   h->node_parent = cv.take<int>(nn);
@@ -338,8 +347,12 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
     return fail(EAGLE_ERR_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
   }
   h->launches = 1 + (c.feat_kind == EAGLE_FEAT_FUSED ? 1 : 0) + (h->tc ? 9 : 8) * c.depth + 1;
-  if (h->tc)   // LM heads over more than 128 rows run as several launches (at max_batch)
-    for (int s = 0; s < h->D; ++s) h->launches += ceil_div(c.max_batch * h->rows[s], MAX_ROWS_PER_BLOCK) - 1;
+  if (h->tc)   // LM heads over more than 128 rows run as several launches (at max_batch), and
+               // those over many rows add one select launch each
+    for (int s = 0; s < h->D; ++s) {
+      const int N = c.max_batch * h->rows[s], parts = ceil_div(N, MAX_ROWS_PER_BLOCK);
+      h->launches += parts - 1 + (N >= LM_LOGITS_MIN_ROWS ? parts : 0);
+    }
   *out = h;
   return EAGLE_OK;
 }
@@ -399,6 +412,7 @@ static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t 
 }
 
 static LmPartials lm_partials(eagle_draft* h, int N);
+static LmPartials lm_partials(eagle_draft* h, int N, bool via_logits);
 
 // Sampled drafting of the LM head's top-k: per-request seeds, rows per request and depth.
 struct SampleArgs {
@@ -413,9 +427,33 @@ static void set_sampling(EpiArgs& e, const SampleArgs& sa, int row0) {
   e.sample_row0 = row0;
 }
 
+static bool lm_via_logits(const eagle_draft* h, const uint16_t* a_hl, int N) {
+  return h->logits && a_hl && N >= LM_LOGITS_MIN_ROWS;
+}
+
 static eagle_status_t lm_head(eagle_draft* h, const float* a, const uint16_t* a_hl, int N, int topk,
                               cudaStream_t st, const SampleArgs& sa = SampleArgs()) {
   const eagle_draft_config_t& c = h->cfg;
+  if (lm_via_logits(h, a_hl, N)) {
+    // launches of <= 128 rows (double-buffered accumulators) that store the logits, each
+    // followed by the select kernel over its rows
+    const int parts = ceil_div(N, MAX_ROWS_PER_BLOCK), per = ceil_div(N, parts);
+    const LmPartials lm = lm_partials(h, N, true);
+    for (int r0 = 0; r0 < N; r0 += per) {
+      const int n = std::min(per, N - r0);
+      GemmPlan p = base_plan(h, h->tm_lm, nullptr, h->w.w_lm, nullptr, c.vocab, c.d, c.vocab);
+      tma_operand(p, a_hl + 2 * static_cast<size_t>(r0) * c.d);
+      EpiArgs& e = p.args.e;
+      e.kind = EPI_LOGITS;
+      e.logits = h->logits + static_cast<size_t>(r0) * c.vocab;
+      eagle_status_t r = run_gemm(h, p, n, st, EAGLE_K_LMHEAD);
+      if (r != EAGLE_OK) return r;
+      ProfScope ps(h, EAGLE_K_LM_SELECT, st);
+      CU(launch_lm_select(h->logits + static_cast<size_t>(r0) * c.vocab, n, c.vocab, topk, sa.seeds, sa.rows,
+                          sa.depth, r0, lm, st, h->use_pdl && !h->profiling));
+    }
+    return EAGLE_OK;
+  }
   if (a_hl && N > MAX_ROWS_PER_BLOCK) {
     // More rows than one TMEM accumulator pair holds: launches of <= 128 rows each, so the
     // accumulators stay double-buffered (the top-k epilogue of one tile overlaps the next
@@ -458,19 +496,25 @@ static eagle_status_t lm_head(eagle_draft* h, const float* a, const uint16_t* a_
   return run_gemm(h, p, N, st, EAGLE_K_LMHEAD);
 }
 
-static LmPartials lm_partials(eagle_draft* h, int N) {
+static LmPartials lm_partials(eagle_draft* h, int N, bool via_logits) {
   LmPartials lm;
   lm.poison_if = nullptr;   // the handle reports kernel-side problems through eagle_draft_check
   lm.max = h->lm_max;
   lm.sum = h->lm_sum;
   lm.val = h->lm_val;
   lm.id = h->lm_id;
+  if (via_logits) {   // one list and one log-sum-exp state per vocabulary part
+    lm.T = lm.G = lm_select_parts(h->cfg.vocab);
+    return lm;
+  }
   lm.T = ceil_div(h->cfg.vocab, BM);
   lm.G = h->tc ? std::min<long long>(num_sms(), static_cast<long long>(ceil_div(h->cfg.vocab, BM)) * ceil_div(h->cfg.d, BK))
                : ceil_div(h->cfg.vocab, BM);
   (void)N;
   return lm;
 }
+
+static LmPartials lm_partials(eagle_draft* h, int N) { return lm_partials(h, N, false); }
 
 // ------------------------------------------------------- the launch sequence
 static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* in, const eagle_draft_outputs_t* out,
@@ -719,7 +763,8 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       }
       tr.f_max = h->f_max;
       ProfScope ps(h, EAGLE_K_EXPAND, st);
-      CU(launch_expand(t, s, lm_partials(h, N), cur, nxt, tr, st, pdl));
+      CU(launch_expand(t, s, lm_partials(h, N, lm_via_logits(h, h->tc ? h->a_hl : nullptr, N)), cur, nxt, tr, st,
+                       pdl));
     }
     if (trc) {
       const size_t o = static_cast<size_t>(s - 1) * nmax;

@@ -108,54 +108,33 @@ EAGLE_DEV void compute_rstd(const BSrc& b, int N, float* rstd, int tid, int nthr
 // ==================================================================== epilogues
 // Shared-memory scratch of the 128 epilogue threads.
 struct EpiScratch {
-  float xch[16][BM];       // row-major exchange tile (rotary partners; STORE: the chunk's output
-                           // rows before the vector stores; LM head: the warps' sorted top lists)
-  float red[4][16];        // per-warp partial sums of squares / LM head: per-warp row maxima
-  float red2[4][16];       // LM head: per-warp row sums of exp
+  float xch[16][BM];       // row-major exchange tile (rotary partners, LM-head transpose;
+                           // STORE: the chunk's output rows before the vector stores)
+  float red[4][16];        // per-warp partial sums of squares
   int meta[3][16];         // rows of the chunk: position, request, request-local slot
 };
-
-// LM head: candidates of one 16-row chunk that beat their row's threshold are staged here
-// (per row) and inserted by one thread per row; more than this many in one row of a chunk
-// sends the chunk down the sorting path instead.
-constexpr int LM_STAGE = 24;
-constexpr int LM_FIXED_BYTES = 16 * LM_STAGE * 8 + 16 * 4 + 16;
-
 // Views of the epilogue's shared memory (the pointers themselves live in registers).
 struct EpiSmem {
   EpiScratch* s;
-  float2* stage;           // LM head: [16][LM_STAGE] staged (key, id) of the chunk's rows
-  int* stage_cnt;          // [16] staged entries per row of the chunk
-  int* flag;               // [4] chunk flags (staging overflow)
-  int* st_cnt;             // [N] list length per row
-  float* thr_v;            // [N] the row's threshold: its list's k-th key (or -inf while shorter)
-  int* thr_i;              // [N] and its token id (INT_MAX while shorter)
-  float* lv;               // [N][k] running top-k keys (sorted, best first)
+  float* st_max;           // LM head, per row: running max, running sum of exp, list length
+  float* st_sum;
+  int* st_cnt;
+  float* lv;               // [N][k] running top-k values (sorted)
   int* li;                 // [N][k] and their token ids
-  float* rstd;             // [N] factored RMSNorm scale of each row (EPI_QKV / EPI_SWIGLU / EPI_LMHEAD)
-  uint16_t* shl;           // STORE / SWIGLU: [32][BM] operand-copy rows (hi, lo) before the vector stores
+  float* rstd;             // [N] factored RMSNorm scale of each row (EPI_QKV / EPI_SWIGLU)
+  uint16_t* shl;            // STORE / SWIGLU: [32][BM] operand-copy rows (hi, lo) before the vector stores
 };
 
 EAGLE_DEV EpiSmem epi_views(void* scratch, void* lm, int N, int topk) {
   EpiSmem es;
   es.s = reinterpret_cast<EpiScratch*>(scratch);
   es.shl = reinterpret_cast<uint16_t*>(lm);   // STORE / SWIGLU only (no LM-head lists then)
-  char* p = reinterpret_cast<char*>(lm);
-  es.stage = reinterpret_cast<float2*>(p);
-  p += 16 * LM_STAGE * 8;
-  es.stage_cnt = reinterpret_cast<int*>(p);
-  p += 16 * 4;
-  es.flag = reinterpret_cast<int*>(p);
-  p += 16;
-  es.st_cnt = reinterpret_cast<int*>(p);
-  p += static_cast<size_t>(N) * 4;
-  es.thr_v = reinterpret_cast<float*>(p);
-  p += static_cast<size_t>(N) * 4;
-  es.thr_i = reinterpret_cast<int*>(p);
-  p += static_cast<size_t>(N) * 4;
-  es.lv = reinterpret_cast<float*>(p);
-  p += static_cast<size_t>(N) * topk * 4;
-  es.li = reinterpret_cast<int*>(p);
+  float* f = reinterpret_cast<float*>(lm);
+  es.st_max = f;
+  es.st_sum = f + N;
+  es.st_cnt = reinterpret_cast<int*>(f + 2 * N);
+  es.lv = f + 3 * N;
+  es.li = reinterpret_cast<int*>(f + 3 * N + N * topk);
   es.rstd = nullptr;
   return es;
 }
@@ -191,6 +170,89 @@ EAGLE_DEV bool epi_all(bool p) {
       : "r"(p ? 1u : 0u)
       : "memory");
   return r != 0;
+}
+
+// Merge a warp's 128 new (value, id) candidates (4 per lane) into a row's sorted top-k
+// list (length cnt <= k) held in shared memory: k rounds of warp arg-max.  Used to fill
+// a list that is not full yet.
+EAGLE_DEV void warp_topk_merge(float* lv, int* li, int* cnt_p, int k, const float* nv, const int* nid,
+                               int lane) {
+  const int cnt = *cnt_p;
+  float cv[5];
+  int ci[5];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) { cv[j] = nv[j]; ci[j] = nid[j]; }
+  cv[4] = lane < cnt ? lv[lane] : -INFINITY;
+  ci[4] = lane < cnt ? li[lane] : INT_MAX;
+  unsigned taken = 0;
+  float outv = -INFINITY;
+  int outi = INT_MAX;
+  int rounds = 0;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int j = 0; j < 5; ++j)
+      if (!(taken >> j & 1u) && ci[j] != INT_MAX && beats(cv[j], ci[j], bv, bi)) { bv = cv[j]; bi = ci[j]; }
+    float wv = bv;
+    int wi = bi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+      if (beats(ov, oi, wv, wi)) { wv = ov; wi = oi; }
+    }
+    if (wi == INT_MAX) break;
+#pragma unroll
+    for (int j = 0; j < 5; ++j)
+      if (ci[j] == wi) taken |= 1u << j;
+    if (lane == r) { outv = wv; outi = wi; }
+    ++rounds;
+  }
+  __syncwarp();
+  if (lane < rounds) { lv[lane] = outv; li[lane] = outi; }
+  if (lane == 0) *cnt_p = rounds;
+  __syncwarp();
+}
+
+// Insert the warp's candidates that beat the current k-th entry of a full list (best
+// first, in shared memory).  The list lives one entry per lane while inserting; each
+// candidate costs a ballot, a popcount and a shuffle-shift.  Only a few values per tile
+// qualify once the list holds the best of earlier tiles.
+EAGLE_DEV void warp_topk_insert(float* lv, int* li, int k, const float* nv, int* nid, int lane) {
+  float myv = lane < k ? lv[lane] : -INFINITY;
+  int myi = lane < k ? li[lane] : INT_MAX;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    for (;;) {
+      const float kv = __shfl_sync(0xffffffffu, myv, k - 1);
+      const int ki = __shfl_sync(0xffffffffu, myi, k - 1);
+      const unsigned m = __ballot_sync(0xffffffffu, nid[j] != INT_MAX && beats(nv[j], nid[j], kv, ki));
+      if (!m) break;
+      const int src = __ffs(m) - 1;
+      const float cv = __shfl_sync(0xffffffffu, nv[j], src);
+      const int ci = __shfl_sync(0xffffffffu, nid[j], src);
+      // entries better than the candidate stay; the rest move down one place
+      const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && beats(myv, myi, cv, ci)));
+      const float upv = __shfl_up_sync(0xffffffffu, myv, 1);
+      const int upi = __shfl_up_sync(0xffffffffu, myi, 1);
+      if (lane > pos) {
+        myv = upv;
+        myi = upi;
+      }
+      if (lane == pos) {
+        myv = cv;
+        myi = ci;
+      }
+      if (lane == src) nid[j] = INT_MAX;   // consumed
+    }
+  }
+  __syncwarp();
+  if (lane < k) {
+    lv[lane] = myv;
+    li[lane] = myi;
+  }
+  __syncwarp();
 }
 
 // One 16-row chunk of accumulators: thread tl (0..127) holds feature m0 + tl of rows
@@ -437,199 +499,87 @@ EAGLE_DEV void epilogue_chunk(const GemmArgs& g, EpiSmem& es, int mt, int n0, co
       }
     }
     named_bar(1, 128);
-  } else {  // EPI_LMHEAD
-    // Thread tl holds vocabulary entry tok = tile * 128 + tl of the chunk's 16 rows.
-    const int k = e.topk;
+  } else if (e.kind == EPI_LOGITS) {
+    // the rows' logits only (a separate kernel takes the log-sum-exp and the top-k): one
+    // coalesced 512-byte row segment per row
     const int tok = mt * BM + tl;
-    const bool tvalid = tok < g.M;
-    float key[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r)   // (a factored RMSNorm of the operand - a final norm - applies here)
-      key[r] = !tvalid ? -INFINITY : (e.nss && n0 + r < g.N) ? v[r] * es.rstd[n0 + r] : v[r];
-    if (e.logits && tvalid) {   // (optional) the full logits, one coalesced row segment per row
+    if (tok < g.M) {
 #pragma unroll
       for (int r = 0; r < 16; ++r)
-        if (n0 + r < g.N) e.logits[static_cast<size_t>(n0 + r) * g.M + tok] = key[r];
+        if (n0 + r < g.N)
+          e.logits[static_cast<size_t>(n0 + r) * g.M + tok] = e.nss ? v[r] * es.rstd[n0 + r] : v[r];
     }
-    // this tile's log-sum-exp state of every row: per warp (max, sum of exp) with the 16 rows'
-    // shuffle chains side by side, combined over the 4 warps by one thread per row below
-    {
-      float wm[16], wsum[16];
+  } else {  // EPI_LMHEAD
+    // (with a factored RMSNorm of the operand, e.g. a final norm before the LM head, the
+    // row scale is applied here)
 #pragma unroll
-      for (int r = 0; r < 16; ++r) wm[r] = key[r];
+    for (int r = 0; r < 16; ++r) es.s->xch[r][tl] = (e.nss && n0 + r < g.N) ? v[r] * es.rstd[n0 + r] : v[r];
+    if (e.logits && mt * BM + tl < g.M) {   // (optional) the full logits as well
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
+      for (int r = 0; r < 16; ++r)
+        if (n0 + r < g.N) e.logits[static_cast<size_t>(n0 + r) * g.M + mt * BM + tl] = es.s->xch[r][tl];
+    }
+    named_bar(1, 128);
+    const int k = e.topk;
+    for (int r = warp_q; r < 16; r += 4) {
+      const int n = n0 + r;
+      if (n >= g.N) continue;                       // warp-uniform
+      float val[4];
+      int id[4];
+      float lmax = -INFINITY;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) wm[r] = fmaxf(wm[r], __shfl_xor_sync(0xffffffffu, wm[r], o));
-#pragma unroll
-      for (int r = 0; r < 16; ++r) wsum[r] = key[r] == -INFINITY ? 0.f : expf(key[r] - wm[r]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int r = 0; r < 16; ++r) wsum[r] += __shfl_xor_sync(0xffffffffu, wsum[r], o);
-      if (lane == 0) {
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          es.s->red[warp_q][r] = wm[r];
-          es.s->red2[warp_q][r] = wsum[r];
-        }
+      for (int j = 0; j < 4; ++j) {
+        id[j] = mt * BM + lane + 32 * j;
+        val[j] = id[j] < g.M ? es.s->xch[r][lane + 32 * j] : -INFINITY;
+        if (id[j] >= g.M) id[j] = INT_MAX;
+        lmax = fmaxf(lmax, val[j]);
       }
-    }
-    // top-k keys: the logit, or (sampled drafting) the logit plus the row's Gumbel noise -
-    // word tl / 32 of Philox(counter = (32 tile + tl mod 32, frontier slot, depth, 0))
-    if (e.seeds && tvalid) {
+      // this tile's log-sum-exp state (max, sum of exp) of the row, merged later in tile order
+      const float tmax = warp_max(lmax);
+      float s = 0.f;
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        const int gr = e.sample_row0 + min(n0 + r, g.N - 1);
+      for (int j = 0; j < 4; ++j) s += id[j] != INT_MAX ? expf(val[j] - tmax) : 0.f;
+      s = warp_sum(s);
+      if (lane == 0) {
+        e.lm_max[static_cast<size_t>(n) * g.MT + mt] = tmax;
+        e.lm_sum[static_cast<size_t>(n) * g.MT + mt] = s;
+      }
+      // top-k (sampled drafting: of logit + Gumbel noise; one Philox call gives the lane's
+      // four tokens, t = tile * 128 + lane + 32 j -> word j of counter 32 tile + lane)
+      if (e.seeds) {
+        const int gr = e.sample_row0 + n;
         const int b = gr / e.sample_rows, i = gr - b * e.sample_rows;
         const unsigned long long sd = __ldg(e.seeds + b);
-        const uint4 w = philox4x32_10(make_uint4(32u * static_cast<uint32_t>(mt) + (tl & 31), static_cast<uint32_t>(i),
+        const uint4 w = philox4x32_10(make_uint4(32u * static_cast<uint32_t>(mt) + lane, static_cast<uint32_t>(i),
                                                  static_cast<uint32_t>(e.sample_depth), 0u),
                                       static_cast<uint32_t>(sd), static_cast<uint32_t>(sd >> 32));
-        const int j = tl >> 5;
-        key[r] += gumbel_of_word(j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (id[j] != INT_MAX) val[j] += gumbel_of_word(ws[j]);
       }
-    }
-    // an entry takes part when its row exists, its token exists and its key is not NaN
-    int kid[16];
+      const int cnt = es.st_cnt[n];
+      float* lv = es.lv + static_cast<size_t>(n) * k;
+      int* li = es.li + static_cast<size_t>(n) * k;
+      const float tv = cnt < k ? -INFINITY : lv[k - 1];
+      const int ti = cnt < k ? INT_MAX : li[k - 1];
+      bool cand = false;
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const bool ok = n0 + r < g.N && tvalid && !(key[r] != key[r]);
-      kid[r] = ok ? tok : INT_MAX;
-      if (!ok) key[r] = -INFINITY;
-    }
-    // candidates: keys that beat their row's threshold (its list's k-th entry), staged
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      if (kid[r] != INT_MAX && beats(key[r], kid[r], es.thr_v[n0 + r], es.thr_i[n0 + r])) {
-        const int slot = atomicAdd(es.stage_cnt + r, 1);
-        if (slot < LM_STAGE) es.stage[r * LM_STAGE + slot] = make_float2(key[r], __int_as_float(kid[r]));
+      for (int j = 0; j < 4; ++j) cand |= id[j] != INT_MAX && beats(val[j], id[j], tv, ti);
+      __syncwarp();
+      if (__any_sync(0xffffffffu, cand)) {
+        if (cnt < k) warp_topk_merge(lv, li, es.st_cnt + n, k, val, id, lane);
+        else warp_topk_insert(lv, li, k, val, id, lane);
       }
-    }
-    named_bar(1, 128);
-    if (tl < 16 && n0 + tl < g.N) {
-      const int r = tl, n = n0 + r;
-      float M = es.s->red[0][r];
-#pragma unroll
-      for (int q = 1; q < 4; ++q) M = fmaxf(M, es.s->red[q][r]);
-      float S = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float mq = es.s->red[q][r];
-        S += mq == -INFINITY ? 0.f : es.s->red2[q][r] * expf(mq - M);
-      }
-      e.lm_max[static_cast<size_t>(n) * g.MT + mt] = M;
-      e.lm_sum[static_cast<size_t>(n) * g.MT + mt] = S;
-      if (es.stage_cnt[r] > LM_STAGE) es.flag[0] = 1;
+      __syncwarp();
     }
     named_bar(1, 128);
-    if (es.flag[0] == 0) {
-      // the common case: a few staged entries per row, inserted by the row's thread
-      if (tl < 16 && n0 + tl < g.N) {
-        const int r = tl, n = n0 + r;
-        float* lv = es.lv + static_cast<size_t>(n) * k;
-        int* li = es.li + static_cast<size_t>(n) * k;
-        int cnt = es.st_cnt[n];
-        const int c = es.stage_cnt[r];
-        for (int q = 0; q < c; ++q) {
-          const float2 en = es.stage[r * LM_STAGE + q];
-          const float ev = en.x;
-          const int ei = __float_as_int(en.y);
-          int pos;
-          if (cnt < k) {
-            pos = cnt++;
-          } else {
-            if (!beats(ev, ei, lv[k - 1], li[k - 1])) continue;
-            pos = k - 1;
-          }
-          while (pos > 0 && beats(ev, ei, lv[pos - 1], li[pos - 1])) {
-            lv[pos] = lv[pos - 1];
-            li[pos] = li[pos - 1];
-            --pos;
-          }
-          lv[pos] = ev;
-          li[pos] = ei;
-        }
-        es.st_cnt[n] = cnt;
-        es.thr_v[n] = cnt < k ? -INFINITY : lv[k - 1];
-        es.thr_i[n] = cnt < k ? INT_MAX : li[k - 1];
-        es.stage_cnt[r] = 0;
-      }
-    } else {
-      // some row had more candidates than its staging holds (always on a CTA's first tile):
-      // each warp sorts its 32 entries of every row (bitonic, best first), its top k go to
-      // shared memory, and each row's thread merges them with the row's list
-#pragma unroll
-      for (int k2 = 2; k2 <= 32; k2 <<= 1) {
-#pragma unroll
-        for (int j = k2 >> 1; j > 0; j >>= 1) {
-          const bool keep_better = ((lane & j) == 0) == ((lane & k2) == 0);
-#pragma unroll
-          for (int r = 0; r < 16; ++r) {
-            const float ov = __shfl_xor_sync(0xffffffffu, key[r], j);
-            const int oi = __shfl_xor_sync(0xffffffffu, kid[r], j);
-            if (keep_better == beats(ov, oi, key[r], kid[r])) {
-              key[r] = ov;
-              kid[r] = oi;
-            }
-          }
-        }
-      }
-      float2* mbuf = reinterpret_cast<float2*>(&es.s->xch[0][0]);   // [16 rows][4 warps][16]
-      if (lane < k) {
-#pragma unroll
-        for (int r = 0; r < 16; ++r) mbuf[(r * 4 + warp_q) * 16 + lane] = make_float2(key[r], __int_as_float(kid[r]));
-      }
-      named_bar(1, 128);
-      if (tl == 0) es.flag[0] = 0;   // every thread read it before the barrier above
-      if (tl < 16 && n0 + tl < g.N) {
-        const int r = tl, n = n0 + r;
-        float* lv = es.lv + static_cast<size_t>(n) * k;
-        int* li = es.li + static_cast<size_t>(n) * k;
-        const int cnt = es.st_cnt[n];
-        const float2* w0 = mbuf + (r * 4) * 16;
-        int p0 = 0, p1 = 0, p2 = 0, p3 = 0, p4 = 0, o = 0;
-        float2* tmp = es.stage + r * LM_STAGE;   // (LM_STAGE >= 16 >= k)
-        for (; o < k; ++o) {
-          float bv = -INFINITY;
-          int bi = INT_MAX, bl = -1;
-          if (p0 < cnt && beats(lv[p0], li[p0], bv, bi)) { bv = lv[p0]; bi = li[p0]; bl = 0; }
-          float2 x;
-          if (p1 < k) { x = w0[p1]; if (beats(x.x, __float_as_int(x.y), bv, bi)) { bv = x.x; bi = __float_as_int(x.y); bl = 1; } }
-          if (p2 < k) { x = w0[16 + p2]; if (beats(x.x, __float_as_int(x.y), bv, bi)) { bv = x.x; bi = __float_as_int(x.y); bl = 2; } }
-          if (p3 < k) { x = w0[32 + p3]; if (beats(x.x, __float_as_int(x.y), bv, bi)) { bv = x.x; bi = __float_as_int(x.y); bl = 3; } }
-          if (p4 < k) { x = w0[48 + p4]; if (beats(x.x, __float_as_int(x.y), bv, bi)) { bv = x.x; bi = __float_as_int(x.y); bl = 4; } }
-          if (bl < 0) break;
-          p0 += bl == 0;
-          p1 += bl == 1;
-          p2 += bl == 2;
-          p3 += bl == 3;
-          p4 += bl == 4;
-          tmp[o] = make_float2(bv, __int_as_float(bi));
-        }
-        for (int q = 0; q < o; ++q) {
-          lv[q] = tmp[q].x;
-          li[q] = __float_as_int(tmp[q].y);
-        }
-        es.st_cnt[n] = o;
-        es.thr_v[n] = o < k ? -INFINITY : lv[k - 1];
-        es.thr_i[n] = o < k ? INT_MAX : li[k - 1];
-      }
-      if (tl < 16) es.stage_cnt[tl] = 0;
-    }
-    named_bar(1, 128);   // lists and thresholds settled before the next chunk stages against them
   }
 }
 
 // Per-CTA LM-head state: reset before the first tile, written out after the last.
 EAGLE_DEV void lmhead_init(const GemmArgs& g, EpiSmem& es, int tl) {
-  for (int n = tl; n < g.N; n += 128) {
-    es.st_cnt[n] = 0;
-    es.thr_v[n] = -INFINITY;
-    es.thr_i[n] = INT_MAX;
-  }
-  if (tl < 16) es.stage_cnt[tl] = 0;
-  if (tl < 4) es.flag[tl] = 0;
+  for (int n = tl; n < g.N; n += 128) es.st_cnt[n] = 0;
   named_bar(1, 128);
 }
 EAGLE_DEV void lmhead_flush(const GemmArgs& g, EpiSmem& es, int cta, int tl) {
@@ -706,7 +656,7 @@ __host__ __device__ inline TcLayout tc_layout(int npad, int stages, int kpair = 
 __host__ __device__ inline uint32_t tc_smem_bytes(int npad, int stages, int lm_rows, int topk, bool store,
                                                   int kpair = 0) {
   TcLayout L = tc_layout(npad, stages, kpair);
-  uint32_t tail = lm_rows ? static_cast<uint32_t>(lm_rows) * (3 + 2 * topk) * 4 + LM_FIXED_BYTES : 0u;
+  uint32_t tail = static_cast<uint32_t>(lm_rows) * (3 + 2 * topk) * 4;
   if (store && tail < 32 * BM * 2) tail = 32 * BM * 2;
   return L.lm_off + tail + 1024;  // +1024: base alignment
 }
@@ -1468,7 +1418,7 @@ bool plan_gemm(GemmPlan& p, int N) {
     p.grid = g.MT;
     p.grid_y = (N + SIMT_ROWS - 1) / SIMT_ROWS;
     p.smem = sizeof(float) * (SIMT_ROWS * g.K + SIMT_ROWS * BM + ((N + 31) & ~31)) + sizeof(EpiScratch) +
-             static_cast<size_t>(N) * (3 + 2 * std::max(1, g.e.topk)) * 4 + LM_FIXED_BYTES + 64;
+             static_cast<size_t>(N) * (3 + 2 * std::max(1, g.e.topk)) * 4 + 64;
     return p.smem <= (g_simt_smem_cap ? g_simt_smem_cap : static_cast<size_t>(TC_MAX_SMEM));
   }
   g.nrb = (N + MAX_ROWS_PER_BLOCK - 1) / MAX_ROWS_PER_BLOCK;
@@ -1491,7 +1441,7 @@ bool plan_gemm(GemmPlan& p, int N) {
   // counts the clusters would leave SMs idle for) the stream-K schedule.
   g.csplit = 0;
   const size_t part_bytes = static_cast<size_t>(g.nrb) * g.npad * BM * sizeof(float);
-  if (g.e.kind != EPI_LMHEAD && !p.stream_k) {
+  if (g.e.kind != EPI_LMHEAD && g.e.kind != EPI_LOGITS && !p.stream_k) {
     int S = std::min(std::min(8, g.KB), sms / g.MT);
     while (S >= 2 && gemm_active_clusters(S) < g.MT) --S;
     // Long K (fc's 2d, the FFN's d_ff) with one row block stays on stream-K: its CTAs start

@@ -186,5 +186,12 @@ cudaError_t launch_expand(const TreeArgs& t, int s, const LmPartials& lm, const 
 cudaError_t launch_rerank(const TreeArgs& t, const OutArgs& o, cudaStream_t st, bool pdl);
 cudaError_t launch_lm_merge(const LmPartials& lm, int N, int k, int* ids, float* logp, float* lse,
                             cudaStream_t st, bool pdl);
+// LM head over many rows, second half: the rows' stored logits [N][vocab] -> per (row, part)
+// log-sum-exp state and top-k keys (logit, or logit + Gumbel noise with seeds), written at
+// rows row0.. of `lm` (G = T = lm_select_parts(vocab)).  N rows of this launch.
+int lm_select_parts(int vocab);
+cudaError_t launch_lm_select(const float* logits, int N, int vocab, int k, const unsigned long long* seeds,
+                             int sample_rows, int sample_depth, int row0, const LmPartials& lm, cudaStream_t st,
+                             bool pdl);
 
 }  // namespace eagle

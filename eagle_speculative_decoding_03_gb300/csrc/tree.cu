@@ -206,6 +206,209 @@ EAGLE_DEV void merge_lm_row(const LmPartials& lm, int N, int kp, int n, int kout
   tournament(cand, G, kp, kout, my_val, my_id, lane);
 }
 
+// --------------------------------------------- LM-head selection from logits
+// For launches with many rows the LM-head GEMM only stores the rows' logits; this kernel
+// then takes, per (row, vocabulary part), the part's log-sum-exp state and its top-k keys,
+// in the per-CTA-list / per-tile-state layout the expansion merges (lists = parts, tiles =
+// parts).  Keys are the logits, or (sampled drafting) the logits plus the row's Gumbel
+// noise.  Exact top-k by radix select on order-preserving 32-bit images of the keys, ties
+// to the lower token id.
+constexpr int SEL_THREADS = 512;
+constexpr int SEL_WARPS = SEL_THREADS / 32;
+constexpr int SEL_PER = 64;                        // contiguous keys per thread in the passes
+constexpr int SEL_MAX_SPAN = SEL_THREADS * SEL_PER;   // 32768 keys per part (128 KB + padding)
+
+// order-preserving image of a float: larger float -> larger integer; NaN -> 0 (below all)
+EAGLE_DEV uint32_t key_bits(float x) {
+  if (x != x) return 0u;
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+EAGLE_DEV float key_float(uint32_t b) {
+  return __uint_as_float((b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b);
+}
+// element i of the part lives at i + i / 64: thread t's contiguous 64 keys start at 65 t,
+// so the threads of a warp read 32 different banks at every step
+EAGLE_DEV int sel_slot(int i) { return i + (i >> 6); }
+
+__global__ void __launch_bounds__(SEL_THREADS)
+lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, int k,
+                 const unsigned long long* seeds, int sample_rows, int sample_depth, int row0,
+                 float* out_max, float* out_sum, float* out_val, int* out_id) {
+  extern __shared__ uint32_t su[];                 // [span + span / 64] keys
+  __shared__ int hist[256];
+  __shared__ float red_m[SEL_WARPS], red_s[SEL_WARPS];
+  __shared__ int wsum[SEL_WARPS];
+  __shared__ int s_bin, s_krem, s_cnt;
+  __shared__ uint32_t s_key[KMAX];
+  __shared__ int s_id[KMAX];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = blockIdx.x / parts, part = blockIdx.x - n * parts;   // n: row of this launch
+  const int base = part * span;
+  const int len = max(0, min(span, V - base));
+  const float* x = logits + static_cast<size_t>(n) * V + base;
+  int sb = 0, si = 0;
+  unsigned long long sd = 0;
+  if (seeds) {
+    const int gr = row0 + n;
+    sb = gr / sample_rows;
+    si = gr - sb * sample_rows;
+    sd = __ldg(seeds + sb);
+  }
+  // stage the keys; the part's log-sum-exp state on the way
+  float m = -INFINITY, sm = 0.f;
+  for (int i = tid; i < span; i += SEL_THREADS) {
+    uint32_t kb = 0u;
+    if (i < len) {
+      const float v = __ldcg(x + i);
+      if (v > m) {
+        sm = sm * expf(m - v) + 1.f;
+        m = v;
+      } else if (v == v && v != -INFINITY) {
+        sm += expf(v - m);
+      } else if (v != v) {
+        sm = v;   // a NaN logit makes the row's log-sum-exp NaN, as the fused path does
+      }
+      kb = key_bits(seeds ? v + token_gumbel(base + i, si, sample_depth, sd) : v);
+    }
+    su[sel_slot(i)] = kb;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const float os = __shfl_xor_sync(0xffffffffu, sm, o);
+    const float M = fmaxf(m, om);
+    sm = (m == -INFINITY ? 0.f : sm * expf(m - M)) + (om == -INFINITY ? 0.f : os * expf(om - M));
+    m = M;
+  }
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_s[warp] = sm;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float M = -INFINITY, S = 0.f;
+    for (int w = 0; w < SEL_WARPS; ++w) {
+      const float mw = red_m[w], sw = red_s[w];
+      const float MM = fmaxf(M, mw);
+      S = (M == -INFINITY ? 0.f : S * expf(M - MM)) + (mw == -INFINITY ? 0.f : sw * expf(mw - MM));
+      M = MM;
+    }
+    out_max[static_cast<size_t>(n) * parts + part] = M;
+    out_sum[static_cast<size_t>(n) * parts + part] = S;
+  }
+  // the k-th largest key (or the smallest valid one when fewer than k are valid): four 8-bit
+  // digits from the top; a key takes part in a pass while its higher digits match the prefix
+  const int i0 = tid * SEL_PER, i1 = min(span, i0 + SEL_PER);
+  int valid = 0;   // (the barrier above follows the staging loop)
+  for (int i = i0; i < i1; ++i) valid += su[sel_slot(i)] != 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) valid += __shfl_xor_sync(0xffffffffu, valid, o);
+  if (lane == 0) wsum[warp] = valid;
+  __syncthreads();
+  if (tid == 0) {
+    int tot = 0;
+    for (int w = 0; w < SEL_WARPS; ++w) tot += wsum[w];
+    s_krem = min(k, tot);   // keys to select (0 when every key is NaN)
+  }
+  __syncthreads();
+  const int ksel = s_krem;
+  uint32_t prefix = 0u, pmask = 0u;
+  for (int shift = 24; shift >= 0 && ksel > 0; shift -= 8) {
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t kb = su[sel_slot(i)];
+      if (kb != 0u && (kb & pmask) == prefix) atomicAdd(hist + ((kb >> shift) & 255u), 1);
+    }
+    __syncthreads();
+    if (warp == 0) {   // the bin holding the krem-th largest, scanning down from bin 255
+      int c[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - (lane * 8 + j)];
+        tot += c[j];
+      }
+      int incl = tot;   // inclusive prefix over lanes (bins 255 .. down)
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - tot;
+      const int krem = s_krem;
+      if (excl < krem && incl >= krem) {
+        int run = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run < krem && run + c[j] >= krem) {
+            s_bin = 255 - (lane * 8 + j);
+            s_cnt = run;   // keys in higher bins
+          }
+          run += c[j];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) s_krem = krem - s_cnt;
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(s_bin) << shift;
+    pmask |= 255u << shift;
+  }
+  // keys above the k-th: all of them; keys equal to it: the lowest ids, in id order
+  const uint32_t kth = prefix;
+  const int need_eq = ksel > 0 ? s_krem : 0;   // equal keys still needed after the higher ones
+  int n_eq = 0;
+  for (int i = i0; i < i1; ++i) n_eq += ksel > 0 && su[sel_slot(i)] == kth;
+  int incl = n_eq;   // block-exclusive prefix of the equal keys, in thread (= id) order
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  if (tid == 0) s_cnt = 0;
+  __syncthreads();
+  int before = incl - n_eq;
+  for (int w = 0; w < warp; ++w) before += wsum[w];
+  if (ksel > 0) {
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t kb = su[sel_slot(i)];
+      bool take = kb > kth && kb != 0u;
+      if (kb == kth) {
+        take = before < need_eq;
+        ++before;
+      }
+      if (take) {
+        const int slot = atomicAdd(&s_cnt, 1);
+        if (slot < KMAX) {
+          s_key[slot] = kb;
+          s_id[slot] = base + i;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // the selected keys, best first (larger key, then lower id); empty places: -inf / -1
+  if (tid < k) {
+    const size_t o = (static_cast<size_t>(n) * parts + part) * k;
+    if (tid < ksel) {
+      const uint32_t kb = s_key[tid];
+      const int id = s_id[tid];
+      int rank = 0;
+      for (int j = 0; j < ksel; ++j)
+        rank += s_key[j] > kb || (s_key[j] == kb && s_id[j] < id);
+      out_val[o + rank] = key_float(kb);
+      out_id[o + rank] = id;
+    } else {
+      out_val[o + tid] = -INFINITY;
+      out_id[o + tid] = -1;
+    }
+  }
+}
+
 // ------------------------------------------------------------ expansion
 // One CTA per row (frontier node) of the depth: log-sum-exp and top-k children of the
 // row, written to the node table; the last CTA of a request to finish (arrival counter)
@@ -671,6 +874,9 @@ cudaError_t tree_setup_attributes() {
   cudaError_t e = cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sizeof(float2) * EXR_CAND));
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(lm_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sizeof(uint32_t) * (SEL_MAX_SPAN + SEL_MAX_SPAN / 64)));
+  if (e != cudaSuccess) return e;
   return allow_max_smem(reinterpret_cast<const void*>(lm_merge_kernel));
 }
 
@@ -714,6 +920,27 @@ cudaError_t launch_lm_merge(const LmPartials& lm, int N, int k, int* ids, float*
   const int w = merge_warps(lm.G, k);
   cudaLaunchConfig_t cfg = make_cfg(dim3((N + w - 1) / w), dim3(w * 32), merge_smem(lm.G, k), st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, lm_merge_kernel, lm, N, k, ids, logp, lse);
+}
+
+}  // namespace eagle
+
+namespace eagle {
+
+int lm_select_parts(int vocab) { return (vocab + SEL_MAX_SPAN - 1) / SEL_MAX_SPAN; }
+
+cudaError_t launch_lm_select(const float* logits, int N, int vocab, int k, const unsigned long long* seeds,
+                             int sample_rows, int sample_depth, int row0, const LmPartials& lm, cudaStream_t st,
+                             bool pdl) {
+  const int parts = lm_select_parts(vocab);
+  int span = (vocab + parts - 1) / parts;
+  span = (span + 31) & ~31;
+  if (span > SEL_MAX_SPAN || k < 1 || k > KMAX || lm.G != parts || lm.T != parts) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(N * parts), dim3(SEL_THREADS),
+                                    sizeof(uint32_t) * (span + span / 64 + 1), st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, lm_select_kernel, logits, vocab, span, parts, k, seeds, sample_rows, sample_depth,
+                            row0, lm.max + static_cast<size_t>(row0) * parts, lm.sum + static_cast<size_t>(row0) * parts,
+                            lm.val + static_cast<size_t>(row0) * parts * k, lm.id + static_cast<size_t>(row0) * parts * k);
 }
 
 }  // namespace eagle

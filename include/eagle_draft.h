@@ -239,7 +239,8 @@ EAGLE_API eagle_status_t eagle_lm_head_topk_noalloc(const void* w_lm, int32_t vo
 typedef enum {
   EAGLE_K_INIT = 0, EAGLE_K_FC3 = 1, EAGLE_K_FC = 2, EAGLE_K_QKV = 3, EAGLE_K_ATTN = 4,
   EAGLE_K_OPROJ = 5, EAGLE_K_GATEUP = 6, EAGLE_K_DOWN = 7, EAGLE_K_LMHEAD = 8,
-  EAGLE_K_EXPAND = 9, EAGLE_K_RERANK = 10, EAGLE_K_MERGE = 11, EAGLE_K_FC_OPERAND = 12, EAGLE_K_COUNT = 13
+  EAGLE_K_EXPAND = 9, EAGLE_K_RERANK = 10, EAGLE_K_MERGE = 11, EAGLE_K_FC_OPERAND = 12, EAGLE_K_LM_SELECT = 13,
+  EAGLE_K_COUNT = 14
 } eagle_kernel_kind_t;
 
 /* Profiling mode (enable != 0): every later eagle_draft_tree call (without a trace)
