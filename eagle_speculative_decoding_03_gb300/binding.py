@@ -90,6 +90,28 @@ class VerifyOutputs(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in VERIFY_OUTPUTS]
 
 
+class DFlashConfigC(C.Structure):
+    _fields_ = [("d", C.c_int32), ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("d_ff", C.c_int32), ("vocab", C.c_int32),
+                ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("dtype", C.c_int32),
+                ("n_layers", C.c_int32), ("gamma", C.c_int32), ("k", C.c_int32), ("mask_token", C.c_int32),
+                ("max_batch", C.c_int32), ("max_prefix", C.c_int32), ("flags", C.c_int32)]
+
+
+class DFlashWeights(C.Structure):
+    _fields_ = [("embed", C.c_void_p), ("w_lm", C.c_void_p), ("final_norm", C.c_void_p)] + \
+        [(n, C.POINTER(C.c_void_p)) for n in ("attn_norm", "w_qkv", "w_o", "mlp_norm", "w_gate", "w_up", "w_down")]
+
+
+class DFlashInputs(C.Structure):
+    _fields_ = [("B", C.c_int32), ("anchor", C.c_void_p), ("ctx_k", C.POINTER(C.c_void_p)),
+                ("ctx_v", C.POINTER(C.c_void_p)), ("cu_seqlens", C.c_void_p)]
+
+
+class DFlashOutputs(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("tokens", "logp", "lse", "hidden")]
+
+
 _lib = None
 
 
@@ -131,6 +153,14 @@ def load(path: str = LIB_PATH):
     lib.eagle_verify_check.restype = C.c_int
     lib.eagle_verify_destroy.argtypes = [P]
     lib.eagle_verify_destroy.restype = None
+    lib.eagle_dflash_create.argtypes = [C.POINTER(DFlashConfigC), C.POINTER(DFlashWeights), C.POINTER(P)]
+    lib.eagle_dflash_create.restype = C.c_int
+    lib.eagle_dflash_draft.argtypes = [P, C.POINTER(DFlashInputs), C.POINTER(DFlashOutputs), P]
+    lib.eagle_dflash_draft.restype = C.c_int
+    lib.eagle_dflash_check.argtypes = [P, C.POINTER(C.c_uint32)]
+    lib.eagle_dflash_check.restype = C.c_int
+    lib.eagle_dflash_destroy.argtypes = [P]
+    lib.eagle_dflash_destroy.restype = None
     lib.eagle_speculative_accept.argtypes = [C.c_int32, C.c_int32, C.c_int32, P, P, P, P, P, P, P, P, P, P]
     lib.eagle_speculative_accept.restype = C.c_int
     lib.eagle_draft_last_error.argtypes = []
@@ -392,3 +422,74 @@ def speculative_accept(tree: dict, logits_target, logits_draft, seeds, stream=No
                                            _ptr(seeds), _ptr(out["accept_len"]), _ptr(out["accept_slots"]),
                                            _ptr(out["correction"]), _ptr(out["err"]), st))
     return out
+
+
+def _ptr_array(ts):
+    return (C.c_void_p * len(ts))(*[_ptr(t) for t in ts])
+
+
+def device_dflash_weights(W: dict, device="cuda") -> dict:
+    """DFlash weights (synth.make_dflash_weights) -> device tensors; per-layer lists kept."""
+    top = device_weights({k: W[k] for k in ("embed", "w_lm", "final_norm")}, device)
+    top["layers"] = [device_weights(L, device) for L in W["layers"]]
+    return top
+
+
+class EagleDFlash:
+    """Handle of the DFlash block-parallel draft (bf16)."""
+
+    def __init__(self, cfg, dW: dict, max_batch: int | None = None, max_prefix: int | None = None,
+                 flags: int = 0):
+        lib = load()
+        self.cfg = cfg
+        self._keep = dW
+        c = DFlashConfigC(d=cfg.d, n_heads=cfg.n_heads, n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim,
+                          d_ff=cfg.d_ff, vocab=cfg.vocab, rms_eps=cfg.rms_eps, rope_theta=cfg.rope_theta,
+                          dtype=DTYPE_BF16 if cfg.dtype == "bf16" else DTYPE_F32, n_layers=cfg.layers,
+                          gamma=cfg.gamma, k=cfg.k, mask_token=cfg.mask_id,
+                          max_batch=cfg.B if max_batch is None else max_batch,
+                          max_prefix=cfg.prefix[1] if max_prefix is None else max_prefix, flags=flags)
+        L = dW["layers"]
+        self._arrays = {n: _ptr_array([l[n] for l in L]) for n in
+                        ("attn_norm", "w_qkv", "w_o", "mlp_norm", "w_gate", "w_up", "w_down")}
+        w = DFlashWeights(embed=_ptr(dW["embed"]), w_lm=_ptr(dW["w_lm"]), final_norm=_ptr(dW["final_norm"]),
+                          **{n: C.cast(a, C.POINTER(C.c_void_p)) for n, a in self._arrays.items()})
+        h = C.c_void_p()
+        _check(lib.eagle_dflash_create(C.byref(c), C.byref(w), C.byref(h)))
+        self.h = h
+
+    def close(self):
+        if getattr(self, "h", None):
+            load().eagle_dflash_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def draft(self, dI: dict, hidden: bool = False, stream=None) -> dict:
+        """dI: anchor [B] int32, cu_seqlens [B+1], ctx_k / ctx_v lists of per-layer caches."""
+        import torch
+        B = int(dI["anchor"].shape[0])
+        g, k, dev = self.cfg.gamma, self.cfg.k, dI["anchor"].device
+        out = {"tokens": torch.empty((B, g, k), dtype=torch.int32, device=dev),
+               "logp": torch.empty((B, g, k), dtype=torch.float32, device=dev),
+               "lse": torch.empty((B, g), dtype=torch.float32, device=dev)}
+        if hidden:
+            out["hidden"] = torch.empty((B, g + 1, self.cfg.d), dtype=torch.float32, device=dev)
+        ck, cv = _ptr_array(dI["ctx_k"]), _ptr_array(dI["ctx_v"])
+        inp = DFlashInputs(B=B, anchor=_ptr(dI["anchor"]), ctx_k=C.cast(ck, C.POINTER(C.c_void_p)),
+                           ctx_v=C.cast(cv, C.POINTER(C.c_void_p)), cu_seqlens=_ptr(dI["cu_seqlens"]))
+        o = DFlashOutputs(**{n: _ptr(out.get(n)) for n in ("tokens", "logp", "lse", "hidden")})
+        st = None if stream is None else stream.cuda_stream
+        _check(load().eagle_dflash_draft(self.h, C.byref(inp), C.byref(o), st))
+        return out
+
+    def check(self) -> int:
+        w = C.c_uint32(0)
+        st = load().eagle_dflash_check(self.h, C.byref(w))
+        if st != EAGLE_OK:
+            raise EagleError(st, load().eagle_draft_last_error().decode())
+        return w.value

@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libeagle_draft.so")
-SOURCES = ["gemm.cu", "attention.cu", "tree.cu", "draft.cu", "noalloc.cu", "verify.cu", "accept.cu"]
+SOURCES = ["gemm.cu", "attention.cu", "tree.cu", "draft.cu", "noalloc.cu", "stack.cu", "accept.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

@@ -350,6 +350,74 @@ EAGLE_API eagle_status_t eagle_verify_tree(eagle_verify_t* handle, const eagle_v
 EAGLE_API eagle_status_t eagle_verify_check(eagle_verify_t* handle, uint32_t* word);
 EAGLE_API void eagle_verify_destroy(eagle_verify_t* handle);
 
+/* ------------------------------------------------------------------------------------
+ * DFlash block-parallel draft ("DFlash-1: parallel block + KV injection", zackli.ai
+ * "Speculative Decoding Deep Dive III"; "DFlash" card and algorithm sketch, kaushalya.io).
+ * Per request, the block [E(anchor), E(MASK) x gamma] (rows at positions n_b .. n_b + gamma)
+ * runs through n_layers draft layers in one pass: each Llama-style layer takes queries from
+ * the block's hidden states and keys / values from [the layer's injected context ; the block]
+ * - the target's fused context features of the verified prefix, projected by the layer, are
+ * its extra KV memory - with attention bidirectional inside the block.  A final RMSNorm and
+ * the frozen shared LM head give each mask row's draft distribution; the call returns its
+ * top-k tokens (ties to the lower id), their log-probabilities and the log-sum-exp.  The
+ * injected keys / values are a per-layer cache the caller keeps (keys rotated at the prefix
+ * positions), like the draft's own KV cache of the EAGLE step.  bf16, head_dim 128.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  int32_t d, n_heads, n_kv_heads, head_dim, d_ff, vocab;  /* as in eagle_draft_config_t */
+  float   rms_eps, rope_theta;
+  int32_t dtype;        /* EAGLE_DTYPE_BF16 */
+  int32_t n_layers;     /* draft layers, 1..16 */
+  int32_t gamma;        /* mask slots per block, 1..63 */
+  int32_t k;            /* tokens kept per mask slot, 1..16 */
+  int32_t mask_token;   /* the MASK row of the shared embedding table */
+  int32_t max_batch;    /* largest B; max_batch * (gamma + 1) <= 256 */
+  int32_t max_prefix;   /* largest prefix n_b */
+  int32_t flags;        /* EAGLE_FLAG_NO_PDL or 0 */
+} eagle_dflash_config_t;
+
+/* Weights (device, bf16 [out, in] row-major; gains f32), borrowed for the handle's lifetime.
+ * The per-layer members are HOST arrays of n_layers device pointers (copied at create). */
+typedef struct {
+  const void*  embed;                /* [vocab, d] frozen, shared with the target */
+  const void*  w_lm;                 /* [vocab, d] frozen, shared with the target */
+  const float* final_norm;           /* [d] */
+  const float* const* attn_norm;     /* [n_layers] -> [d] */
+  const void* const*  w_qkv;         /* [n_layers] -> [(Hq + 2 Hkv) hd, d] */
+  const void* const*  w_o;           /* [n_layers] -> [d, Hq hd] */
+  const float* const* mlp_norm;      /* [n_layers] -> [d] */
+  const void* const*  w_gate;        /* [n_layers] -> [d_ff, d] */
+  const void* const*  w_up;          /* [n_layers] -> [d_ff, d] */
+  const void* const*  w_down;        /* [n_layers] -> [d, d_ff] */
+} eagle_dflash_weights_t;
+
+typedef struct {
+  int32_t        B;            /* requests, 1..max_batch */
+  const int32_t* anchor;       /* [B] the verified anchor token of each block */
+  const void* const* ctx_k;    /* HOST array [n_layers] of device bf16 [sum n_b, Hkv, hd] injected keys */
+  const void* const* ctx_v;    /* HOST array [n_layers] of device bf16 [sum n_b, Hkv, hd] injected values */
+  const int32_t* cu_seqlens;   /* [B + 1] */
+} eagle_dflash_inputs_t;
+
+typedef struct {
+  int32_t* tokens;   /* [B, gamma, k] the draft's top-k tokens of each mask slot (best first) */
+  float*   logp;     /* [B, gamma, k] their log-probabilities */
+  float*   lse;      /* [B, gamma] log-sum-exp of each mask slot's logits */
+  float*   hidden;   /* [B, gamma + 1, d] (nullable) the last layer's output, anchor row included */
+} eagle_dflash_outputs_t;
+
+typedef struct eagle_dflash eagle_dflash_t;
+
+EAGLE_API eagle_status_t eagle_dflash_create(const eagle_dflash_config_t* cfg, const eagle_dflash_weights_t* weights,
+                                             eagle_dflash_t** out_handle);
+/* Enqueues one block-parallel draft on `stream`; stream-ordered, asynchronous.  An anchor or
+ * mask token outside [0, vocab) or a prefix longer than max_prefix sets the device error word
+ * (eagle_dflash_check). */
+EAGLE_API eagle_status_t eagle_dflash_draft(eagle_dflash_t* handle, const eagle_dflash_inputs_t* inputs,
+                                            const eagle_dflash_outputs_t* outputs, void* stream);
+EAGLE_API eagle_status_t eagle_dflash_check(eagle_dflash_t* handle, uint32_t* word);
+EAGLE_API void eagle_dflash_destroy(eagle_dflash_t* handle);
+
 /* Multi-round speculative sampling over emitted trees ("Speculative Decoding Deep Dive III",
  * zackli.ai, EAGLE-1: tree attention plus multi-round speculative sampling; "How speculative
  * decoding works", kaushalya.io: accept a drafted token with probability min(1, p/q), else draw

@@ -84,7 +84,9 @@ STRUCTS = [("eagle_draft_config_t", "Config"), ("eagle_draft_weights_t", "Weight
            ("eagle_draft_inputs_t", "Inputs"), ("eagle_draft_outputs_t", "Outputs"),
            ("eagle_draft_trace_t", "Trace"), ("eagle_draft_info_t", "Info"),
            ("eagle_verify_config_t", "VerifyConfig"), ("eagle_verify_weights_t", "VerifyWeights"),
-           ("eagle_verify_inputs_t", "VerifyInputs"), ("eagle_verify_outputs_t", "VerifyOutputs")]
+           ("eagle_verify_inputs_t", "VerifyInputs"), ("eagle_verify_outputs_t", "VerifyOutputs"),
+           ("eagle_dflash_config_t", "DFlashConfigC"), ("eagle_dflash_weights_t", "DFlashWeights"),
+           ("eagle_dflash_inputs_t", "DFlashInputs"), ("eagle_dflash_outputs_t", "DFlashOutputs")]
 
 
 def test_struct_layout_matches_header(tmp_path):
