@@ -236,6 +236,85 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------- rows after the draft step
+def _event_ms(fn, stream, steps, warmup):
+    """Average device time of fn() over `steps` calls (CUDA events on the stream)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def measure_extras(eb, cfg, W, dW, I, dI, d, out, stream, peak, rank, args) -> dict:
+    """Sampled drafting on the headline tree; the target's verification pass over the tree it
+    emits (one synthetic target layer, the frozen embedding and LM head); sampled acceptance
+    on the target's and a draft-like distribution; the DFlash block-parallel draft
+    (5 layers of the same head, a block of 16, prefix 2048).  Each timed on the stream with
+    CUDA events after warm-up; weights larger than L2, so every call streams them."""
+    import torch
+    steps, warm = max(5, min(args.steps, 50)), max(3, args.warmup)
+    res = {}
+    # sampled drafting: per-request seeds, the same tree step
+    I2 = dict(I, seeds=np.arange(1, cfg.B + 1, dtype=np.uint64) * np.uint64(0x9E3779B97F4A7C15))
+    dI2 = eb.device_inputs(I2)
+    out2 = d.alloc_outputs(cfg.B)
+    ms = _event_ms(lambda: d.tree(dI2, out=out2, stream=stream), stream, steps, warm)
+    d.check()
+    res["sampled_draft"] = {"value": cfg.B * cfg.kept_per_request() / (ms * 1e-3), "unit": UNIT, "ms_per_tree": ms}
+    # verification pass over the emitted tree
+    Wt, Ct = synth.make_target(cfg), synth.make_target_cache(cfg, I, seed_offset=rank)
+    dWt, dCt = eb.device_weights(Wt), eb.device_weights(Ct)
+    S = d.info["slots"]
+    tree = {k: out[k].contiguous() for k in ("tokens", "positions", "parents", "mask")}
+    v = eb.EagleVerify(cfg, dWt, dW, max_batch=cfg.B, max_slots=S)
+    cu = dI["cu_seqlens"]
+    vout = v.verify(tree, dCt, cu, accept=True, logits=True)
+    ms = _event_ms(lambda: v.verify(tree, dCt, cu, accept=True, stream=stream), stream, steps, warm)
+    v.check()
+    layer = 2 * (cfg.qkv_dim * cfg.d + cfg.d * cfg.attn_dim + 3 * cfg.d * cfg.d_ff)
+    vbytes = layer + 2 * cfg.vocab * cfg.d + int(I["cu_seqlens"][-1]) * cfg.n_kv_heads * cfg.head_dim * 4
+    res["verify"] = {"us_per_pass": ms * 1e3, "slots": cfg.B * S, "hbm_frac": vbytes / (ms * 1e-3) / 1e9 / peak,
+                     "algorithmic_bytes": vbytes,
+                     "what": "target layer + final RMSNorm + LM head (top-1) over the emitted tree, greedy acceptance"}
+    # sampled acceptance: the target's logits and a draft distribution near them
+    lp = vout["logits"]
+    g = torch.Generator(device=lp.device).manual_seed(7)
+    lq = lp + 0.5 * torch.randn(lp.shape, generator=g, device=lp.device)
+    seeds = torch.arange(1, cfg.B + 1, dtype=torch.int64, device=lp.device)
+    ms = _event_ms(lambda: eb.speculative_accept(tree, lp, lq, seeds, stream=stream), stream, steps, warm)
+    acc = eb.speculative_accept(tree, lp, lq, seeds)
+    res["sampled_accept"] = {"us_per_call": ms * 1e3, "accepted": acc["accept_len"].cpu().tolist(),
+                             "what": "multi-round speculative sampling over the emitted tree, |V| = %d" % cfg.vocab}
+    v.close()
+    del dWt, dCt, vout, lp, lq
+    # DFlash block-parallel draft
+    dc = configs.DFLASH["dflash_b1"]
+    DW = synth.make_dflash_weights(dc)
+    DI = synth.make_dflash_inputs(dc, seed_offset=rank)
+    dv = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).cuda()
+    dDI = {"anchor": dv(DI["anchor"]), "cu_seqlens": dv(DI["cu_seqlens"]),
+           "ctx_k": [dv(c) for c in DI["ctx_k"]], "ctx_v": [dv(c) for c in DI["ctx_v"]]}
+    f = eb.EagleDFlash(dc, eb.device_dflash_weights(DW))
+    ms = _event_ms(lambda: f.draft(dDI, stream=stream), stream, steps, warm)
+    f.check()
+    layer = 2 * (dc.qkv_dim * dc.d + dc.d * dc.attn_dim + 3 * dc.d * dc.d_ff)
+    n = int(DI["cu_seqlens"][-1])
+    dbytes = dc.layers * (layer + n * dc.n_kv_heads * dc.head_dim * 4) + 2 * dc.vocab * dc.d
+    res["dflash"] = {"workload": "dflash_b1: %d layers of the Llama-3-8B-shaped head, block of %d, prefix %d, B=%d"
+                                 % (dc.layers, dc.gamma, n, dc.B),
+                     "us_per_block": ms * 1e3, "draft_tokens_per_s": dc.B * dc.gamma / (ms * 1e-3),
+                     "hbm_frac": dbytes / (ms * 1e-3) / 1e9 / peak, "algorithmic_bytes": dbytes}
+    f.close()
+    return res
+
+
 # ------------------------------------------------------- replicas (one per rank)
 def max_over_ranks(ms, dist, device="cuda"):
     """The slowest rank's time, on every rank (one all-reduce; the identity on one rank)."""
@@ -376,6 +455,12 @@ def run_ours(args):
                "kernels_ms_per_tree": {k: v[0] / 3 for k, v in p4.items()}}
         d4.close()
 
+    # ---- the rows after the draft step: sampled drafting, the target's verification pass
+    # over the emitted tree, sampled acceptance, and the DFlash block-parallel draft
+    extras = None
+    if args.workload == "eagle2_b1" and not args.no_extras:
+        extras = measure_extras(eb, cfg, W, dW, I, dI, d, out, stream, peak, rank, args)
+
     # ---- CPU baseline: the float64 oracle on host cores (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -410,6 +495,8 @@ def run_ours(args):
     }
     if b32:
         line["b32"] = b32
+    if extras:
+        line.update(extras)
     if cpu:
         line["cpu_baseline"] = cpu
     if rank == 0:
@@ -429,6 +516,7 @@ def main():
     ap.add_argument("--workload", default="eagle2_b1", choices=sorted(configs.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-b32", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -215,8 +215,9 @@ EAGLE_DEV void merge_lm_row(const LmPartials& lm, int N, int kp, int n, int kout
 // to the lower token id.
 constexpr int SEL_THREADS = 512;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
-constexpr int SEL_PER = 64;                        // contiguous keys per thread in the passes
-constexpr int SEL_MAX_SPAN = SEL_THREADS * SEL_PER;   // 32768 keys per part (128 KB + padding)
+constexpr int SEL_PER = 32;                        // contiguous keys per thread in the passes
+constexpr int SEL_MAX_SPAN = SEL_THREADS * SEL_PER;   // 16384 keys per part (64 KB + padding)
+constexpr int SEL_CAP = 256;                       // candidates the threshold gather keeps
 
 // order-preserving image of a float: larger float -> larger integer; NaN -> 0 (below all)
 EAGLE_DEV uint32_t key_bits(float x) {
@@ -227,21 +228,25 @@ EAGLE_DEV uint32_t key_bits(float x) {
 EAGLE_DEV float key_float(uint32_t b) {
   return __uint_as_float((b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b);
 }
-// element i of the part lives at i + i / 64: thread t's contiguous 64 keys start at 65 t,
+// element i of the part lives at i + i / 32: thread t's contiguous 32 keys start at 33 t,
 // so the threads of a warp read 32 different banks at every step
-EAGLE_DEV int sel_slot(int i) { return i + (i >> 6); }
+EAGLE_DEV int sel_slot(int i) { return i + (i >> 5); }
 
 __global__ void __launch_bounds__(SEL_THREADS)
 lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, int k,
                  const unsigned long long* seeds, int sample_rows, int sample_depth, int row0,
                  float* out_max, float* out_sum, float* out_val, int* out_id) {
-  extern __shared__ uint32_t su[];                 // [span + span / 64] keys
+  extern __shared__ uint32_t su[];                 // [span + span / 32] keys
   __shared__ int hist[256];
   __shared__ float red_m[SEL_WARPS], red_s[SEL_WARPS];
   __shared__ int wsum[SEL_WARPS];
   __shared__ int s_bin, s_krem, s_cnt;
   __shared__ uint32_t s_key[KMAX];
   __shared__ int s_id[KMAX];
+  __shared__ uint32_t s_tmax[SEL_THREADS];
+  __shared__ uint32_t s_ckey[SEL_CAP];
+  __shared__ int s_cid[SEL_CAP];
+  __shared__ uint32_t s_theta;
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -315,6 +320,61 @@ lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, i
   }
   __syncthreads();
   const int ksel = s_krem;
+  // Fast path.  theta = the ksel-th largest of the threads' maxima (ties by thread index)
+  // is at most the ksel-th largest key (ksel threads hold a key >= theta), so every key of
+  // the top ksel is >= theta; usually only about ksel keys are.  Those are gathered and
+  // ranked exactly (larger key, then lower id).  Too many of them: the radix select below.
+  uint32_t tmax = 0u;
+  for (int i = i0; i < i1; ++i) tmax = max(tmax, su[sel_slot(i)]);
+  s_tmax[tid] = tmax;
+  if (tid == 0) {
+    s_theta = 0u;
+    s_cnt = 0;
+  }
+  __syncthreads();
+  if (ksel > 0) {
+    int rank = 0;
+    for (int j = 0; j < SEL_THREADS; ++j) {
+      const uint32_t m2 = s_tmax[j];
+      rank += m2 > tmax || (m2 == tmax && j < tid);
+    }
+    if (rank == ksel - 1) s_theta = tmax;
+  }
+  __syncthreads();
+  const uint32_t theta = s_theta;
+  if (ksel > 0 && theta != 0u) {
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t kb = su[sel_slot(i)];
+      if (kb >= theta) {
+        const int slot = atomicAdd(&s_cnt, 1);
+        if (slot < SEL_CAP) {
+          s_ckey[slot] = kb;
+          s_cid[slot] = base + i;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int nc = s_cnt;
+  if (ksel > 0 && theta != 0u && nc <= SEL_CAP) {
+    const size_t o = (static_cast<size_t>(n) * parts + part) * k;
+    if (tid < nc) {
+      const uint32_t kb = s_ckey[tid];
+      const int id = s_cid[tid];
+      int rank = 0;
+      for (int j = 0; j < nc; ++j) rank += s_ckey[j] > kb || (s_ckey[j] == kb && s_cid[j] < id);
+      if (rank < ksel) {
+        out_val[o + rank] = key_float(kb);
+        out_id[o + rank] = id;
+      }
+    }
+    if (tid >= ksel && tid < k) {
+      out_val[o + tid] = -INFINITY;
+      out_id[o + tid] = -1;
+    }
+    return;
+  }
+  __syncthreads();
   uint32_t prefix = 0u, pmask = 0u;
   for (int shift = 24; shift >= 0 && ksel > 0; shift -= 8) {
     if (tid < 256) hist[tid] = 0;
@@ -875,7 +935,7 @@ cudaError_t tree_setup_attributes() {
                                        static_cast<int>(sizeof(float2) * EXR_CAND));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(lm_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sizeof(uint32_t) * (SEL_MAX_SPAN + SEL_MAX_SPAN / 64)));
+                           static_cast<int>(sizeof(uint32_t) * (SEL_MAX_SPAN + SEL_MAX_SPAN / 32)));
   if (e != cudaSuccess) return e;
   return allow_max_smem(reinterpret_cast<const void*>(lm_merge_kernel));
 }
@@ -937,7 +997,7 @@ cudaError_t launch_lm_select(const float* logits, int N, int vocab, int k, const
   if (span > SEL_MAX_SPAN || k < 1 || k > KMAX || lm.G != parts || lm.T != parts) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(N * parts), dim3(SEL_THREADS),
-                                    sizeof(uint32_t) * (span + span / 64 + 1), st, pdl, attr);
+                                    sizeof(uint32_t) * (span + span / 32 + 1), st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, lm_select_kernel, logits, vocab, span, parts, k, seeds, sample_rows, sample_depth,
                             row0, lm.max + static_cast<size_t>(row0) * parts, lm.sum + static_cast<size_t>(row0) * parts,
                             lm.val + static_cast<size_t>(row0) * parts * k, lm.id + static_cast<size_t>(row0) * parts * k);
