@@ -135,6 +135,8 @@ def load(path: str = LIB_PATH):
     lib.eagle_draft_query.restype = C.c_int
     lib.eagle_draft_check.argtypes = [P, C.POINTER(C.c_uint32)]
     lib.eagle_draft_check.restype = C.c_int
+    lib.eagle_draft_set_wait_limit.argtypes = [P, C.c_int64]
+    lib.eagle_draft_set_wait_limit.restype = C.c_int
     lib.eagle_draft_destroy.argtypes = [P]
     lib.eagle_draft_destroy.restype = None
     lib.eagle_draft_profile.argtypes = [P, C.c_int32]
@@ -324,6 +326,9 @@ class EagleDraft:
         _check(load().eagle_draft_profile_read(self.h, ms, n))
         lib = load()
         return {lib.eagle_draft_kernel_name(i).decode(): (ms[i], n[i]) for i in range(KERNEL_KINDS) if n[i]}
+
+    def set_wait_limit(self, cycles: int):
+        _check(load().eagle_draft_set_wait_limit(self.h, int(cycles)))
 
     def check(self) -> int:
         """Synchronise; raise on a device error word or CUDA error."""

@@ -134,14 +134,15 @@ EAGLE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete.  Returns false (and
 // sets DEVERR_TIMEOUT in *err and the CTA-wide abort flag) when the limit runs out or
 // another role of the CTA already aborted.
-EAGLE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err, volatile int* abort_flag) {
+EAGLE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err, volatile int* abort_flag,
+                         long long limit = WAIT_LIMIT_CYCLES) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+      if (clock64() - t0 > limit) {
         atomicOr(err, DEVERR_TIMEOUT);
         *abort_flag = 1;
         return false;
@@ -333,6 +334,7 @@ struct GemmArgs {
                            // cluster when S > 1) on consecutive K ranges, reduced through DSMEM
   BSrc b;
   EpiArgs e;
+  long long wait_limit;    // clock cycles a bounded wait may take (0: the default, ~1 s)
   float* part;             // split-K partial scratch [grid][2][nrb*npad][BM]
   int* counters;           // per tile arrival counters (zero between launches)
   unsigned* err;

@@ -19,6 +19,7 @@
 #include <cstdarg>
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -50,6 +51,7 @@ struct eagle_draft {
   eagle_draft_weights_t w;
   bool tc = false;
   bool use_graph = true, use_pdl = true, gemm_occ2 = false;
+  long long wait_limit = 0;   // bounded waits of the GEMMs, clock cycles (0: the default)
   int D = 0, R = 0, gen = 0, S = 0, n_max = 0, k_max = 0, f_max = 0, max_nodes = 0;
   int rows[EAGLE_MAX_DEPTH], kids[EAGLE_MAX_DEPTH];
   int row_base[EAGLE_MAX_DEPTH + 1], node_base[EAGLE_MAX_DEPTH + 1];
@@ -114,6 +116,14 @@ struct ProfScope {
 };
 
 static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// EAGLE_FAULT in the environment makes a step fail on the host, for tests of the error paths:
+// "alloc" = the workspace allocation of eagle_draft_create, "launch" = a launch in the middle of
+// eagle_draft_tree (depth 2's attention, or the last depth's if there is one).
+static bool fault_injected(const char* what) {
+  const char* f = getenv("EAGLE_FAULT");
+  return f && strcmp(f, what) == 0;
+}
 
 // LM-head launches of at least this many rows store the logits and select in a second
 // kernel; fewer rows keep the log-sum-exp and top-k in the GEMM's epilogue.  (The fused
@@ -312,6 +322,10 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
   }
   size_t total = 0;
   carve(h, nullptr, &total);
+  if (fault_injected("alloc")) {
+    delete h;
+    return fail(EAGLE_ERR_OOM, "workspace of %zu bytes (failure injected by EAGLE_FAULT=alloc)", total);
+  }
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -393,15 +407,34 @@ extern "C" eagle_status_t eagle_draft_check(eagle_draft_t* h, uint32_t* word) {
   if (word) *word = w;
   if (w) {
     CU(cudaMemset(h->err, 0, sizeof(unsigned)));
+    if (w & DEVERR_TIMEOUT) {
+      // a GEMM CTA that gave up never arrived on its split tiles' counters: clear them (and
+      // the expansion's) so that the next call starts from zero
+      CU(cudaMemset(h->counters, 0, sizeof(int) * 16384));
+      CU(cudaMemset(h->exp_counters, 0, sizeof(int) * h->cfg.max_batch));
+    }
     return fail(EAGLE_ERR_DEVICE, "device error word 0x%x", w);
   }
   return EAGLE_OK;
 }
 
+extern "C" eagle_status_t eagle_draft_set_wait_limit(eagle_draft_t* h, int64_t cycles) {
+  if (!h || cycles < 0) return fail(EAGLE_ERR_INVALID_ARG, "null handle or negative limit");
+  if (h->wait_limit != cycles && h->graph) {   // the limit is a kernel argument of the cached graph
+    cudaGraphExecDestroy(h->graph);
+    h->graph = nullptr;
+  }
+  h->wait_limit = cycles;
+  return EAGLE_OK;
+}
+
+
 // ------------------------------------------------------------- GEMM setup
 static GemmPlan base_plan(eagle_draft* h, const CUtensorMap& tm0, const CUtensorMap* tm1, const void* w0,
                           const void* w1, int M, int K, int m_split) {
-  return gemm_plan(h->tc, tm0, tm1, w0, w1, M, K, m_split, h->part, h->counters, h->err);
+  GemmPlan p = gemm_plan(h->tc, tm0, tm1, w0, w1, M, K, m_split, h->part, h->counters, h->err);
+  p.args.wait_limit = h->wait_limit;
+  return p;
 }
 
 static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t st, int kind) {
@@ -686,6 +719,8 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       a.out = h->o;
       a.out_hl = h->tc ? h->o_hl : nullptr;
       ProfScope ps(h, EAGLE_K_ATTN, st);
+      if (s == std::min(2, h->D) && fault_injected("launch"))
+        return fail(EAGLE_ERR_CUDA, "launch_attention failed: injected by EAGLE_FAULT=launch (depth %d)", s);
       CU(launch_attention(a, st, pdl));
     }
     // O projection + residual

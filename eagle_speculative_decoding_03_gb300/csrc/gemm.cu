@@ -703,6 +703,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = g.KB;
+  const long long wlim = g.wait_limit > 0 ? g.wait_limit : WAIT_LIMIT_CYCLES;
   const int npad = g.npad, nrb = g.nrb, np2 = 2 * npad;
   const Sched sc{static_cast<long long>(g.MT) * KB, static_cast<int>(gridDim.x)};
   // units [u0, u1): stream-K range, or (csplit) K range r of tile blockIdx.x / S
@@ -763,7 +764,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
           for (int kb = kb0; kb < kb1 && ok;) {
             const int nk = min(KP, kb1 - kb);   // K blocks of this stage
             for (int rb = 0; rb < nrb && ok; ++rb) {
-              if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
+              if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag, wlim)) { ok = false; break; }
               const uint32_t dst = sbase + stage * L.stage_bytes;
               mbar_arrive_expect_tx(bar_full + 8 * stage, nk * A_STAGE_BYTES);
               for (int u = 0; u < nk; ++u) {
@@ -810,13 +811,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
           const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (s1 - i)));
           const int ab = static_cast<int>(uc % g.nbuf);
           const uint32_t ap = static_cast<uint32_t>((uc / g.nbuf) & 1);
-          if (!mbar_wait(bar_acce + 8 * ab, ap ^ 1, g.err, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar_acce + 8 * ab, ap ^ 1, g.err, abort_flag, wlim)) { ok = false; break; }
           tc_fence_after();
           // (the one-block loop is kept apart: this thread's per-stage work bounds the rate)
           if (KP == 1) {
             for (int kb = kb0; kb < kb1 && ok; ++kb) {
               for (int rb = 0; rb < nrb; ++rb) {
-                if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag, wlim)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>((ab * nrb + rb) * np2);
                 const uint64_t ad = adesc0 + stage * dstep, bd = bdesc0 + stage * dstep;
@@ -830,7 +831,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
           } else {   // one 16-row block (nrb == 1), two K blocks per stage
             const uint32_t d = tmem + static_cast<uint32_t>(ab * np2);
             for (int kb = kb0; kb < kb1 && ok;) {
-              if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag)) { ok = false; break; }
+              if (!mbar_wait(bar_full + 8 * stage, phase, g.err, abort_flag, wlim)) { ok = false; break; }
               tc_fence_after();
               const uint64_t ad = adesc0 + stage * dstep, bd = bdesc0 + stage * dstep;
   #pragma unroll
@@ -877,7 +878,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
           for (int kb = kb0; kb < kb1 && ok;) {
             const int nk = min(KP, kb1 - kb);
             for (int rb = 0; rb < nrb && ok; ++rb) {
-              if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag)) { ok = false; break; }
+              if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag, wlim)) { ok = false; break; }
               mbar_arrive_expect_tx(bar_full + 8 * stage, nk * b_bytes);
               for (int u = 0; u < nk; ++u)
                 tma_load_2d(sbase + stage * L.stage_bytes + L.b_off + u * b_bytes, &tmB, (kb + u) * BK, rb * np2,
@@ -919,7 +920,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
           const bool bf = g.b.mode == B_BF16 || (g.b.mode == B_FC && k0 >= g.b.split);
           const uint32_t rowbytes = bf ? 128u : 256u;
           for (int rb = 0; rb < nrb; ++rb) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag, wlim));
             if (!ok) break;
             const int r0 = rb * npad;
             const int rows = min(npad, g.N - r0);
@@ -976,7 +977,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
           const bool bf = g.b.mode == B_BF16 || (g.b.mode == B_FC && k0 >= g.b.split);
           for (int rb = 0; rb < nrb; ++rb, ++it) {
             if (it % TC_NCW == cw) {
-              ok = __all_sync(0xffffffffu, mbar_wait(bar_bfull + 8 * stage, phase, g.err, abort_flag));
+              ok = __all_sync(0xffffffffu, mbar_wait(bar_bfull + 8 * stage, phase, g.err, abort_flag, wlim));
               if (!ok) break;
               float gm0 = 1.f, gm1 = 1.f;
               if (g.b.mode == B_NORM) {
@@ -1043,7 +1044,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
         const int kb1 = static_cast<int>(min(static_cast<long long>(KB), kb0 + (s1 - i)));
         const int ab = static_cast<int>(uc % g.nbuf);
         const uint32_t ap = static_cast<uint32_t>((uc / g.nbuf) & 1);
-        ok = epi_all(mbar_wait(bar_accf + 8 * ab, ap, g.err, abort_flag));
+        ok = epi_all(mbar_wait(bar_accf + 8 * ab, ap, g.err, abort_flag, wlim));
         if (!ok) break;
         tc_fence_after();
         const bool complete = kb0 == 0 && kb1 == KB;

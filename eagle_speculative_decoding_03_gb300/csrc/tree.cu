@@ -228,6 +228,78 @@ EAGLE_DEV uint32_t key_bits(float x) {
 EAGLE_DEV float key_float(uint32_t b) {
   return __uint_as_float((b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b);
 }
+// Scratch of block_select_top: a 256-bin histogram, per-warp totals, the chosen digit.
+struct SelectScratch {
+  int hist[256];
+  int wtot[32];
+  int bin, above;
+};
+
+// The k best of up to NT keys, one per thread (0 = no key): larger key first, ties to the lower
+// thread index.  A radix select on 8-bit digits from the top (histogram updates aggregated per
+// warp over lanes with the same digit), then the keys equal to the k-th in thread order.  Every
+// thread of the block calls it; returns whether this thread's key is among the k.
+template <int NT>
+EAGLE_DEV bool block_select_top(uint32_t kb, int k, SelectScratch& sc) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int present = __syncthreads_count(kb != 0u);
+  int krem = min(k, present);
+  if (krem <= 0) return false;
+  uint32_t prefix = 0u, pmask = 0u;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += NT) sc.hist[i] = 0;
+    __syncthreads();
+    const bool in = kb != 0u && (kb & pmask) == prefix;
+    const uint32_t dig = (kb >> shift) & 255u;
+    const unsigned act = __ballot_sync(0xffffffffu, in);
+    if (in) {
+      const unsigned peers = __match_any_sync(act, dig);
+      if (lane == __ffs(peers) - 1) atomicAdd(sc.hist + dig, __popc(peers));
+    }
+    __syncthreads();
+    if (warp == 0) {   // the bin holding the krem-th largest, scanning down from bin 255
+      int c[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sc.hist[255 - (lane * 8 + j)];
+        tot += c[j];
+      }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - tot;
+      if (excl < krem && incl >= krem) {
+        int run = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run < krem && run + c[j] >= krem) {
+            sc.bin = 255 - (lane * 8 + j);
+            sc.above = run;
+          }
+          run += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(sc.bin) << shift;
+    pmask |= 255u << shift;
+    krem -= sc.above;
+    __syncthreads();   // every thread has read bin / above before the next pass
+  }
+  const bool eq = kb != 0u && kb == prefix;
+  const unsigned bal = __ballot_sync(0xffffffffu, eq);
+  if (lane == 0) sc.wtot[warp] = __popc(bal);
+  __syncthreads();
+  int before = __popc(bal & ((1u << lane) - 1u));
+  for (int w = 0; w < warp; ++w) before += sc.wtot[w];
+  const bool keep = kb > prefix || (eq && before < krem);
+  __syncthreads();   // the scratch may be reused by the caller
+  return keep;
+}
+
 // element i of the part lives at i + i / 32: thread t's contiguous 32 keys start at 33 t,
 // so the threads of a warp read 32 different banks at every step
 EAGLE_DEV int sel_slot(int i) { return i + (i >> 5); }
@@ -489,11 +561,12 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
   __shared__ float s_lse;
   __shared__ int s_last;
   __shared__ float sv[256];
-  __shared__ int srank[256], spos[256];
+  __shared__ int spos[256];
   __shared__ int wcount[EXR_WARPS];
   __shared__ int s_u, s_slot, s_neff;
   __shared__ float s_vu;
   __shared__ unsigned long long s_pmask[64];
+  __shared__ SelectScratch ex_sel;
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -700,56 +773,12 @@ expand_kernel(const TreeArgs t, const int s, const LmPartials lm, const RowMeta 
       sv[c] = rank_value(__ldcg(scratch_v + b * 256 + c));
     }
   } else {
-    // the F best children (value, then generation index), kept in generation order.
-    // nc2 <= 256 = one child per thread.  Bound: in each warp, the F-th best of its
-    // children; the best such bound.  Exact ranks only among the children the bound
-    // does not beat; positions in generation order from per-warp ballots.
+    // the F best children (value, then generation index), kept in generation order: block
+    // radix select over the depth's children (one per thread, nc2 <= 256)
     const float vc = tid < nc2 ? rank_value(__ldcg(scratch_v + b * 256 + tid)) : -INFINITY;
-    const int idc = tid < nc2 ? tid : INT_MAX;
     if (tid < nc2) sv[tid] = vc;
-    {
-      int rk = 0;
-#pragma unroll 8
-      for (int o = 1; o < 32; ++o) {
-        const int src = (lane + o) & 31;
-        const float ov = __shfl_sync(0xffffffffu, vc, src);
-        const int oi = __shfl_sync(0xffffffffu, idc, src);
-        rk += (oi != INT_MAX) & ((ov > vc) | ((ov == vc) & (oi < idc)));
-      }
-      const int nv = __popc(__ballot_sync(0xffffffffu, idc != INT_MAX));
-      if (lane == 0) {
-        wb_v[warp] = -INFINITY;
-        wb_i[warp] = INT_MAX;
-      }
-      __syncwarp();
-      if (nv >= F && idc != INT_MAX && rk == F - 1) {
-        wb_v[warp] = vc;
-        wb_i[warp] = idc;
-      }
-    }
-    if (tid == 0) ncand = 0;
-    __syncthreads();
-    float tv = -INFINITY;
-    int ti = INT_MAX;
-#pragma unroll
-    for (int w = 0; w < EXR_WARPS; ++w)
-      if (wb_i[w] != INT_MAX && beats(wb_v[w], wb_i[w], tv, ti)) {
-        tv = wb_v[w];
-        ti = wb_i[w];
-      }
-    if (idc != INT_MAX && !beats(tv, ti, vc, idc)) srank[atomicAdd(&ncand, 1)] = idc;   // candidate list
-    __syncthreads();
-    const int nc = ncand;
-    bool keep = false;
-    if (idc != INT_MAX && !beats(tv, ti, vc, idc)) {
-      int rk = 0;
-      for (int j = 0; j < nc; ++j) {
-        const int c2 = srank[j];
-        const float w2 = sv[c2];
-        rk += (w2 > vc) | ((w2 == vc) & (c2 < idc));
-      }
-      keep = rk < F;
-    }
+    const bool keep = block_select_top<EXR_THREADS>(tid < nc2 ? key_bits(vc) : 0u, F, ex_sel);
+    const int idc = tid;
     const unsigned kb = __ballot_sync(0xffffffffu, keep);
     if (lane == 0) wcount[warp] = __popc(kb);
     __syncthreads();
@@ -797,6 +826,7 @@ __global__ void __launch_bounds__(RR_THREADS) rerank_kernel(const TreeArgs t, co
   __shared__ int slot_node[64];
   __shared__ int slot_par[64];
   __shared__ unsigned long long anc[64];
+  __shared__ SelectScratch rr_sel;
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -817,22 +847,13 @@ __global__ void __launch_bounds__(RR_THREADS) rerank_kernel(const TreeArgs t, co
   }
   const int neff = __ldcg(t.n_eff + b);
   __syncthreads();
-  // kept flags (node c = tid + 1): static trees keep every node, dynamic ones the m best
+  // kept flags (node c = tid + 1): static trees keep every node, dynamic ones the m best by V
+  // (ties to the lower generation index = the lower thread), by block radix select
   int kf = 0;
-  if (tid < G) {
-    const int c = tid + 1;
-    if (t.tree_kind == 1) {
-      kf = 1;
-    } else {
-      const float vc = vals[tid];
-      int rk = 0;
-#pragma unroll 8
-      for (int c2 = 1; c2 <= G; ++c2) {
-        const float w = vals[c2 - 1];
-        rk += (w > vc) | ((w == vc) & (c2 < c));
-      }
-      kf = rk < t.m;
-    }
+  if (t.tree_kind == 1) {
+    kf = tid < G;
+  } else {
+    kf = block_select_top<RR_THREADS>(tid < G ? key_bits(vals[tid]) : 0u, t.m, rr_sel);
   }
   keep[tid] = kf;
   scan[tid] = kf;

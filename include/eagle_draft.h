@@ -33,6 +33,9 @@
  * thread-local message.  Kernel-side problems (a prefix longer than max_prefix, a
  * wait that ran out) are recorded in a device error word that eagle_draft_check()
  * reads after synchronising.  Calls on one handle must not overlap on the GPU.
+ * Tests of the error paths: EAGLE_FAULT=alloc in the environment makes eagle_draft_create's
+ * workspace allocation fail (EAGLE_ERR_OOM, nothing allocated); EAGLE_FAULT=launch makes a
+ * launch in the middle of eagle_draft_tree fail (EAGLE_ERR_CUDA).
  */
 #ifndef EAGLE_DRAFT_H
 #define EAGLE_DRAFT_H
@@ -262,6 +265,13 @@ EAGLE_API eagle_status_t eagle_draft_query(const eagle_draft_t* handle, eagle_dr
  * (its bits in *word if word != NULL, host), EAGLE_ERR_CUDA on a sticky CUDA error, and
  * EAGLE_OK otherwise.  Clears the word. */
 EAGLE_API eagle_status_t eagle_draft_check(eagle_draft_t* handle, uint32_t* word);
+
+/* Sets how long (clock cycles) each bounded wait inside the GEMM kernels may take before the
+ * kernel gives up, sets EAGLE_DEVERR_TIMEOUT, lets its own copies and MMAs finish and returns;
+ * 0 restores the default (about one second).  A short limit makes the waits run out on purpose,
+ * for tests of that path: eagle_draft_check then reports the timeout, and clears the state a
+ * CTA that gave up leaves behind, so the next call on the handle is whole again. */
+EAGLE_API eagle_status_t eagle_draft_set_wait_limit(eagle_draft_t* handle, int64_t cycles);
 
 /* Frees the workspace and the handle.  NULL is accepted. */
 EAGLE_API void eagle_draft_destroy(eagle_draft_t* handle);
