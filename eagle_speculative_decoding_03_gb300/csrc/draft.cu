@@ -365,7 +365,8 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
                // those over many rows add one select launch each
     for (int s = 0; s < h->D; ++s) {
       const int N = c.max_batch * h->rows[s], parts = ceil_div(N, MAX_ROWS_PER_BLOCK);
-      h->launches += parts - 1 + (N >= LM_LOGITS_MIN_ROWS ? parts : 0);
+      // the LM head (+ a select per part when it stores logits), fc, QKV, O, gate|up and down
+      h->launches += parts - 1 + (N >= LM_LOGITS_MIN_ROWS ? parts : 0) + 5 * (parts - 1);
     }
   *out = h;
   return EAGLE_OK;
@@ -437,7 +438,41 @@ static GemmPlan base_plan(eagle_draft* h, const CUtensorMap& tm0, const CUtensor
   return p;
 }
 
+// The same GEMM restricted to rows [r0, r0 + n): every row-indexed pointer of the operand and
+// of the epilogue moves by r0 rows (tensor-core path with a TMA operand).
+static void offset_rows(GemmPlan& p, int r0) {
+  GemmArgs& g = p.args;
+  EpiArgs& e = g.e;
+  p.b_hl += 2 * static_cast<size_t>(r0) * g.K;
+  if (e.out) e.out += static_cast<size_t>(r0) * e.ldo;
+  if (e.resid) e.resid += static_cast<size_t>(r0) * e.ldr;
+  if (e.ss) e.ss += r0;
+  if (e.hl) e.hl += 2 * static_cast<size_t>(r0) * e.hl_ld;
+  if (e.nss) e.nss += r0;
+  if (e.q) e.q += static_cast<size_t>(r0) * e.Hq * e.hd;
+  if (e.row_req) e.row_req += r0;
+  if (e.row_slot) e.row_slot += r0;
+  if (e.row_pos) e.row_pos += r0;
+}
+
 static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t st, int kind) {
+  const EpiKind ek = static_cast<EpiKind>(p.args.e.kind);
+  if (p.tc && p.args.b_tma && N > MAX_ROWS_PER_BLOCK && (ek == EPI_STORE || ek == EPI_QKV || ek == EPI_SWIGLU)) {
+    // More rows than one accumulator block: launches of <= 128 rows, each with the
+    // double-buffered accumulators and a stage ring of whole 128-row operand tiles (one
+    // launch over two row blocks holds only two 80 KB stages and starves the weight stream;
+    // the weights are streamed once per launch instead)
+    const int parts = ceil_div(N, MAX_ROWS_PER_BLOCK), per = ceil_div(N, parts);
+    for (int r0 = 0; r0 < N; r0 += per) {
+      GemmPlan q = p;
+      offset_rows(q, r0);
+      const int n = std::min(per, N - r0);
+      if (!plan_gemm(q, n)) return fail(EAGLE_ERR_UNSUPPORTED, "GEMM M=%d K=%d N=%d does not fit", q.args.M, q.args.K, n);
+      ProfScope ps(h, kind, st);
+      CU(launch_gemm(q, st, h->use_pdl && !h->profiling));
+    }
+    return EAGLE_OK;
+  }
   if (!plan_gemm(p, N)) return fail(EAGLE_ERR_UNSUPPORTED, "GEMM M=%d K=%d N=%d does not fit", p.args.M, p.args.K, N);
   ProfScope ps(h, kind, st);
   CU(launch_gemm(p, st, h->use_pdl && !h->profiling));

@@ -308,14 +308,14 @@ __global__ void __launch_bounds__(SEL_THREADS)
 lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, int k,
                  const unsigned long long* seeds, int sample_rows, int sample_depth, int row0,
                  float* out_max, float* out_sum, float* out_val, int* out_id) {
-  extern __shared__ uint32_t su[];                 // [span + span / 32] keys
+  extern __shared__ uint32_t su[];                 // [span + span / 32] keys (fallback only)
   __shared__ int hist[256];
   __shared__ float red_m[SEL_WARPS], red_s[SEL_WARPS];
   __shared__ int wsum[SEL_WARPS];
+  __shared__ uint32_t wmax[SEL_WARPS];
   __shared__ int s_bin, s_krem, s_cnt;
   __shared__ uint32_t s_key[KMAX];
   __shared__ int s_id[KMAX];
-  __shared__ uint32_t s_tmax[SEL_THREADS];
   __shared__ uint32_t s_ckey[SEL_CAP];
   __shared__ int s_cid[SEL_CAP];
   __shared__ uint32_t s_theta;
@@ -334,24 +334,30 @@ lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, i
     si = gr - sb * sample_rows;
     sd = __ldg(seeds + sb);
   }
-  // stage the keys; the part's log-sum-exp state on the way
-  float m = -INFINITY, sm = 0.f;
-  for (int i = tid; i < span; i += SEL_THREADS) {
-    uint32_t kb = 0u;
-    if (i < len) {
-      const float v = __ldcg(x + i);
-      if (v > m) {
-        sm = sm * expf(m - v) + 1.f;
-        m = v;
-      } else if (v == v && v != -INFINITY) {
-        sm += expf(v - m);
-      } else if (v != v) {
-        sm = v;   // a NaN logit makes the row's log-sum-exp NaN, as the fused path does
-      }
-      kb = key_bits(seeds ? v + token_gumbel(base + i, si, sample_depth, sd) : v);
-    }
-    su[sel_slot(i)] = kb;
+  // this thread's keys i = tid + 512 j (coalesced), in registers; 0 = no key (past the part,
+  // or NaN)
+  float v[SEL_PER];
+  uint32_t kr[SEL_PER];
+#pragma unroll
+  for (int j = 0; j < SEL_PER; ++j) {
+    const int i = tid + SEL_THREADS * j;
+    v[j] = i < len ? __ldcg(x + i) : -INFINITY;
   }
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < SEL_PER; ++j) m = fmaxf(m, v[j]);
+  float sm = 0.f;
+  uint32_t tmax = 0u;
+  int nvalid = 0;
+#pragma unroll
+  for (int j = 0; j < SEL_PER; ++j) {
+    sm += v[j] == -INFINITY ? 0.f : expf(v[j] - m);   // (a NaN logit makes the sum NaN)
+    const int i = tid + SEL_THREADS * j;
+    kr[j] = i < len ? key_bits(seeds ? v[j] + token_gumbel(base + i, si, sample_depth, sd) : v[j]) : 0u;
+    tmax = max(tmax, kr[j]);
+    nvalid += kr[j] != 0u;
+  }
+  // the part's log-sum-exp state
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float om = __shfl_xor_sync(0xffffffffu, m, o);
@@ -360,83 +366,73 @@ lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, i
     sm = (m == -INFINITY ? 0.f : sm * expf(m - M)) + (om == -INFINITY ? 0.f : os * expf(om - M));
     m = M;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    nvalid += __shfl_xor_sync(0xffffffffu, nvalid, o);
+  }
   if (lane == 0) {
     red_m[warp] = m;
     red_s[warp] = sm;
+    wmax[warp] = tmax;
+    wsum[warp] = nvalid;
   }
+  if (tid == 0) s_cnt = 0;
   __syncthreads();
   if (tid == 0) {
     float M = -INFINITY, S = 0.f;
+    int tot = 0;
     for (int w = 0; w < SEL_WARPS; ++w) {
       const float mw = red_m[w], sw = red_s[w];
       const float MM = fmaxf(M, mw);
       S = (M == -INFINITY ? 0.f : S * expf(M - MM)) + (mw == -INFINITY ? 0.f : sw * expf(mw - MM));
       M = MM;
+      tot += wsum[w];
     }
     out_max[static_cast<size_t>(n) * parts + part] = M;
     out_sum[static_cast<size_t>(n) * parts + part] = S;
-  }
-  // the k-th largest key (or the smallest valid one when fewer than k are valid): four 8-bit
-  // digits from the top; a key takes part in a pass while its higher digits match the prefix
-  const int i0 = tid * SEL_PER, i1 = min(span, i0 + SEL_PER);
-  int valid = 0;   // (the barrier above follows the staging loop)
-  for (int i = i0; i < i1; ++i) valid += su[sel_slot(i)] != 0u;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) valid += __shfl_xor_sync(0xffffffffu, valid, o);
-  if (lane == 0) wsum[warp] = valid;
-  __syncthreads();
-  if (tid == 0) {
-    int tot = 0;
-    for (int w = 0; w < SEL_WARPS; ++w) tot += wsum[w];
-    s_krem = min(k, tot);   // keys to select (0 when every key is NaN)
+    const int ks = min(k, tot);   // keys to select (0 when every key is NaN)
+    s_krem = ks;
+    // theta = the ks-th largest warp maximum (ties by warp) is at most the ks-th largest key
+    // (ks warps hold a key >= theta), so every key of the top ks is >= theta
+    uint32_t th = 0u;
+    if (ks > 0) {
+      for (int w = 0; w < SEL_WARPS; ++w) {
+        int rk = 0;
+        for (int w2 = 0; w2 < SEL_WARPS; ++w2) rk += wmax[w2] > wmax[w] || (wmax[w2] == wmax[w] && w2 < w);
+        if (rk == ks - 1) th = wmax[w];
+      }
+    }
+    s_theta = th;
   }
   __syncthreads();
   const int ksel = s_krem;
-  // Fast path.  theta = the ksel-th largest of the threads' maxima (ties by thread index)
-  // is at most the ksel-th largest key (ksel threads hold a key >= theta), so every key of
-  // the top ksel is >= theta; usually only about ksel keys are.  Those are gathered and
-  // ranked exactly (larger key, then lower id).  Too many of them: the radix select below.
-  uint32_t tmax = 0u;
-  for (int i = i0; i < i1; ++i) tmax = max(tmax, su[sel_slot(i)]);
-  s_tmax[tid] = tmax;
-  if (tid == 0) {
-    s_theta = 0u;
-    s_cnt = 0;
-  }
-  __syncthreads();
-  if (ksel > 0) {
-    int rank = 0;
-    for (int j = 0; j < SEL_THREADS; ++j) {
-      const uint32_t m2 = s_tmax[j];
-      rank += m2 > tmax || (m2 == tmax && j < tid);
-    }
-    if (rank == ksel - 1) s_theta = tmax;
-  }
-  __syncthreads();
   const uint32_t theta = s_theta;
+  // fast path: the keys >= theta (usually a few more than ksel), ranked exactly (larger key,
+  // then lower id); more than SEL_CAP of them: the radix select below
   if (ksel > 0 && theta != 0u) {
-    for (int i = i0; i < i1; ++i) {
-      const uint32_t kb = su[sel_slot(i)];
-      if (kb >= theta) {
+#pragma unroll
+    for (int j = 0; j < SEL_PER; ++j) {
+      if (kr[j] >= theta) {
         const int slot = atomicAdd(&s_cnt, 1);
         if (slot < SEL_CAP) {
-          s_ckey[slot] = kb;
-          s_cid[slot] = base + i;
+          s_ckey[slot] = kr[j];
+          s_cid[slot] = base + tid + SEL_THREADS * j;
         }
       }
     }
   }
   __syncthreads();
   const int nc = s_cnt;
-  if (ksel > 0 && theta != 0u && nc <= SEL_CAP) {
+  if (ksel == 0 || (theta != 0u && nc <= SEL_CAP)) {
     const size_t o = (static_cast<size_t>(n) * parts + part) * k;
-    if (tid < nc) {
-      const uint32_t kb = s_ckey[tid];
+    if (ksel > 0 && tid < nc) {
+      const uint32_t kk = s_ckey[tid];
       const int id = s_cid[tid];
       int rank = 0;
-      for (int j = 0; j < nc; ++j) rank += s_ckey[j] > kb || (s_ckey[j] == kb && s_cid[j] < id);
+      for (int j = 0; j < nc; ++j) rank += s_ckey[j] > kk || (s_ckey[j] == kk && s_cid[j] < id);
       if (rank < ksel) {
-        out_val[o + rank] = key_float(kb);
+        out_val[o + rank] = key_float(kk);
         out_id[o + rank] = id;
       }
     }
@@ -446,7 +442,14 @@ lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, i
     }
     return;
   }
+  // fallback (many keys tie around the k-th): stage the keys, contiguous ranges per thread
+#pragma unroll
+  for (int j = 0; j < SEL_PER; ++j) {
+    const int i = tid + SEL_THREADS * j;
+    if (i < span) su[sel_slot(i)] = kr[j];
+  }
   __syncthreads();
+  const int i0 = tid * SEL_PER, i1 = min(span, i0 + SEL_PER);
   uint32_t prefix = 0u, pmask = 0u;
   for (int shift = 24; shift >= 0 && ksel > 0; shift -= 8) {
     if (tid < 256) hist[tid] = 0;
