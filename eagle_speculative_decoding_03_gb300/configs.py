@@ -131,6 +131,12 @@ SMALL = {
         name="small_wide", d=256, n_heads=2, n_kv_heads=1, head_dim=128, d_ff=640, vocab=33152,
         rms_eps=1e-6, rope_theta=1e4, dtype="bf16", tree="dynamic", depth=3, k=4, m=10,
         B=16, prefix=(5, 60), seed=2007, gamma_jitter=0.1),
+    # 48 requests x 4 rows = 192 rows per depth: GEMMs and the LM head run as CTA pairs sharing
+    # the weight stream (two row blocks), the LM head stores logits for the select kernel
+    "small_pairs": DraftConfig(
+        name="small_pairs", d=256, n_heads=2, n_kv_heads=1, head_dim=128, d_ff=640, vocab=16384,
+        rms_eps=1e-6, rope_theta=1e4, dtype="bf16", tree="dynamic", depth=3, k=4, m=10,
+        B=48, prefix=(5, 40), seed=2008, gamma_jitter=0.1),
     "small_f32": DraftConfig(
         name="small_f32", d=192, n_heads=3, n_kv_heads=1, head_dim=64, d_ff=400, vocab=700,
         rms_eps=1e-6, rope_theta=1e4, dtype="f32", tree="dynamic", depth=3, k=3, m=7,

@@ -167,6 +167,16 @@ EAGLE_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, 
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
       : "memory");
 }
+// the same tile into the shared memory of every CTA of the cluster in cta_mask (same offset),
+// completing the bytes on the mbarrier at the same offset in each
+EAGLE_DEV void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int c0, int c1, uint32_t bar, uint64_t policy,
+                              uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask), "l"(policy)
+      : "memory");
+}
 EAGLE_DEV void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
@@ -201,6 +211,14 @@ EAGLE_DEV void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint
 EAGLE_DEV void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+// arrive on the mbarrier at offset `bar` of every CTA in cta_mask once this thread's
+// tcgen05 ops so far have completed
+EAGLE_DEV void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
 }
 // 16 consecutive 32-bit columns of this warp's 32 TMEM lanes
 EAGLE_DEV void tmem_ld16(uint32_t taddr, float* v) {

@@ -365,8 +365,10 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
                // those over many rows add one select launch each
     for (int s = 0; s < h->D; ++s) {
       const int N = c.max_batch * h->rows[s], parts = ceil_div(N, MAX_ROWS_PER_BLOCK);
-      // the LM head (+ a select per part when it stores logits), fc, QKV, O, gate|up and down
-      h->launches += parts - 1 + (N >= LM_LOGITS_MIN_ROWS ? parts : 0) + 5 * (parts - 1);
+      // the LM head (+ a select per launch when it stores logits); up to 256 rows run as one
+      // launch of CTA pairs
+      const int launches = N <= 2 * MAX_ROWS_PER_BLOCK ? 1 : parts;
+      h->launches += launches - 1 + (N >= LM_LOGITS_MIN_ROWS ? launches : 0);
     }
   *out = h;
   return EAGLE_OK;
@@ -438,40 +440,20 @@ static GemmPlan base_plan(eagle_draft* h, const CUtensorMap& tm0, const CUtensor
   return p;
 }
 
-// The same GEMM restricted to rows [r0, r0 + n): every row-indexed pointer of the operand and
-// of the epilogue moves by r0 rows (tensor-core path with a TMA operand).
-static void offset_rows(GemmPlan& p, int r0) {
-  GemmArgs& g = p.args;
-  EpiArgs& e = g.e;
-  p.b_hl += 2 * static_cast<size_t>(r0) * g.K;
-  if (e.out) e.out += static_cast<size_t>(r0) * e.ldo;
-  if (e.resid) e.resid += static_cast<size_t>(r0) * e.ldr;
-  if (e.ss) e.ss += r0;
-  if (e.hl) e.hl += 2 * static_cast<size_t>(r0) * e.hl_ld;
-  if (e.nss) e.nss += r0;
-  if (e.q) e.q += static_cast<size_t>(r0) * e.Hq * e.hd;
-  if (e.row_req) e.row_req += r0;
-  if (e.row_slot) e.row_slot += r0;
-  if (e.row_pos) e.row_pos += r0;
-}
+// split-K scratch of one rank of a CTA pair (the buffer holds two)
+static size_t part_half() { return static_cast<size_t>(num_sms() / 2) * 2 * MAX_ROWS_PER_BLOCK * BM; }
 
 static eagle_status_t run_gemm(eagle_draft* h, GemmPlan& p, int N, cudaStream_t st, int kind) {
   const EpiKind ek = static_cast<EpiKind>(p.args.e.kind);
-  if (p.tc && p.args.b_tma && N > MAX_ROWS_PER_BLOCK && (ek == EPI_STORE || ek == EPI_QKV || ek == EPI_SWIGLU)) {
-    // More rows than one accumulator block: launches of <= 128 rows, each with the
-    // double-buffered accumulators and a stage ring of whole 128-row operand tiles (one
-    // launch over two row blocks holds only two 80 KB stages and starves the weight stream;
-    // the weights are streamed once per launch instead)
-    const int parts = ceil_div(N, MAX_ROWS_PER_BLOCK), per = ceil_div(N, parts);
-    for (int r0 = 0; r0 < N; r0 += per) {
-      GemmPlan q = p;
-      offset_rows(q, r0);
-      const int n = std::min(per, N - r0);
-      if (!plan_gemm(q, n)) return fail(EAGLE_ERR_UNSUPPORTED, "GEMM M=%d K=%d N=%d does not fit", q.args.M, q.args.K, n);
+  if (p.tc && p.args.b_tma && N > MAX_ROWS_PER_BLOCK && N <= 2 * MAX_ROWS_PER_BLOCK &&
+      (ek == EPI_STORE || ek == EPI_QKV || ek == EPI_SWIGLU || ek == EPI_LOGITS)) {
+    // up to 256 rows: one launch of CTA pairs, each weight stage loaded once for both halves
+    GemmPlan q = p;
+    if (plan_gemm_pair(q, N, part_half())) {
       ProfScope ps(h, kind, st);
       CU(launch_gemm(q, st, h->use_pdl && !h->profiling));
+      return EAGLE_OK;
     }
-    return EAGLE_OK;
   }
   if (!plan_gemm(p, N)) return fail(EAGLE_ERR_UNSUPPORTED, "GEMM M=%d K=%d N=%d does not fit", p.args.M, p.args.K, N);
   ProfScope ps(h, kind, st);
@@ -503,10 +485,24 @@ static eagle_status_t lm_head(eagle_draft* h, const float* a, const uint16_t* a_
                               cudaStream_t st, const SampleArgs& sa = SampleArgs()) {
   const eagle_draft_config_t& c = h->cfg;
   if (lm_via_logits(h, a_hl, N)) {
+    const LmPartials lm = lm_partials(h, N, true);
+    if (N > MAX_ROWS_PER_BLOCK && N <= 2 * MAX_ROWS_PER_BLOCK) {
+      // one launch of CTA pairs storing the logits of all rows (the LM head streamed once),
+      // then the select kernel over them
+      GemmPlan p = base_plan(h, h->tm_lm, nullptr, h->w.w_lm, nullptr, c.vocab, c.d, c.vocab);
+      tma_operand(p, a_hl);
+      p.args.e.kind = EPI_LOGITS;
+      p.args.e.logits = h->logits;
+      eagle_status_t r = run_gemm(h, p, N, st, EAGLE_K_LMHEAD);
+      if (r != EAGLE_OK) return r;
+      ProfScope ps(h, EAGLE_K_LM_SELECT, st);
+      CU(launch_lm_select(h->logits, N, c.vocab, topk, sa.seeds, sa.rows, sa.depth, 0, lm, st,
+                          h->use_pdl && !h->profiling));
+      return EAGLE_OK;
+    }
     // launches of <= 128 rows (double-buffered accumulators) that store the logits, each
     // followed by the select kernel over its rows
     const int parts = ceil_div(N, MAX_ROWS_PER_BLOCK), per = ceil_div(N, parts);
-    const LmPartials lm = lm_partials(h, N, true);
     for (int r0 = 0; r0 < N; r0 += per) {
       const int n = std::min(per, N - r0);
       GemmPlan p = base_plan(h, h->tm_lm, nullptr, h->w.w_lm, nullptr, c.vocab, c.d, c.vocab);

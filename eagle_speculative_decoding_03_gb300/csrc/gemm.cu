@@ -582,12 +582,12 @@ EAGLE_DEV void lmhead_init(const GemmArgs& g, EpiSmem& es, int tl) {
   for (int n = tl; n < g.N; n += 128) es.st_cnt[n] = 0;
   named_bar(1, 128);
 }
-EAGLE_DEV void lmhead_flush(const GemmArgs& g, EpiSmem& es, int cta, int tl) {
+EAGLE_DEV void lmhead_flush(const GemmArgs& g, EpiSmem& es, int cta, int ncta, int tl) {
   const EpiArgs& e = g.e;
   const int k = e.topk;
   named_bar(1, 128);
   for (int n = tl; n < g.N; n += 128) {
-    const size_t o = static_cast<size_t>(n) * gridDim.x + cta;   // lists of one row are contiguous
+    const size_t o = static_cast<size_t>(n) * ncta + cta;   // lists of one row are contiguous
     const int cnt = es.st_cnt[n];
     for (int j = 0; j < k; ++j) {
       e.lm_val[o * k + j] = j < cnt ? es.lv[static_cast<size_t>(n) * k + j] : -INFINITY;
@@ -680,10 +680,22 @@ constexpr uint32_t TC_SMEM_OCC2 = 113 * 1024;   // two CTAs per SM
 // accumulator column 2r + 1 holds the low-order correction of column 2r.
 // NT = TC_THREADS (converter warps present, one CTA per SM) or 7 warps (operand by TMA only;
 // MINB = 1: the whole register file, MINB = 2: two CTAs per SM).
-template <int NT, int MINB, bool SEG>
+//
+// PAIR: a cluster of two CTAs on the same (tile, K block) units, rank r on its own rows (its
+// own argument block g_r and operand map tmB_r): rank 0 loads each weight stage once, by TMA
+// multicast into both CTAs; each CTA's MMA commits release the stage in both, so a stage is
+// refilled only when both have consumed it.
+template <int NT, int MINB, bool SEG, bool PAIR = false>
 __global__ void __launch_bounds__(NT, MINB)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
-               const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+               const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ GemmArgs g0,
+               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ GemmArgs g1) {
+  uint32_t crank = 0;
+  if (PAIR) crank = cooperative_groups::this_cluster().block_rank();
+  const GemmArgs& g = (PAIR && crank) ? g1 : g0;
+  const CUtensorMap& tmB = (PAIR && crank) ? tmB1 : tmB0;
+  const int cta = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);   // schedule index
+  const int ncta = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const TcLayout L = tc_layout(g.npad, g.stages, g.kpair);
@@ -705,21 +717,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
   const int KB = g.KB;
   const long long wlim = g.wait_limit > 0 ? g.wait_limit : WAIT_LIMIT_CYCLES;
   const int npad = g.npad, nrb = g.nrb, np2 = 2 * npad;
-  const Sched sc{static_cast<long long>(g.MT) * KB, static_cast<int>(gridDim.x)};
+  const Sched sc{static_cast<long long>(g.MT) * KB, ncta};
   // units [u0, u1): stream-K range, or (csplit) K range r of tile blockIdx.x / S
   const int cs_t = g.csplit > 0 ? static_cast<int>(blockIdx.x) / g.csplit : 0;
   const int cs_r = g.csplit > 0 ? static_cast<int>(blockIdx.x) - cs_t * g.csplit : 0;
   const long long u0 = g.csplit > 0 ? static_cast<long long>(cs_t) * KB + static_cast<long long>(cs_r) * KB / g.csplit
-                                    : sc.begin(blockIdx.x);
+                                    : sc.begin(cta);
   const long long u1 = g.csplit > 0
                            ? static_cast<long long>(cs_t) * KB + static_cast<long long>(cs_r + 1) * KB / g.csplit
-                           : sc.begin(blockIdx.x + 1);
+                           : sc.begin(cta + 1);
   const bool reorder = SEG && g.csplit == 0;   // (compiled out of the other instances)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < g.stages; ++s) {
       mbar_init(bar_full + 8 * s, 2);            // weight bytes + activation (TMA bytes or converter)
-      mbar_init(bar_empty + 8 * s, 1);           // tcgen05.commit
+      mbar_init(bar_empty + 8 * s, PAIR ? 2 : 1);   // tcgen05.commit (of both CTAs of a pair)
       mbar_init(bar_bfull + 8 * s, 1);           // bulk-copy bytes of the source rows
     }
     for (int b = 0; b < 2; ++b) {
@@ -741,6 +753,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (PAIR) cooperative_groups::this_cluster().sync();   // both CTAs' barriers exist before any remote use
   const uint32_t tmem = *tmem_slot;
   pdl_trigger();
 
@@ -767,9 +780,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
               if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag, wlim)) { ok = false; break; }
               const uint32_t dst = sbase + stage * L.stage_bytes;
               mbar_arrive_expect_tx(bar_full + 8 * stage, nk * A_STAGE_BYTES);
-              for (int u = 0; u < nk; ++u) {
+              for (int u = 0; u < nk && (!PAIR || crank == 0); ++u) {
                 const uint32_t du = dst + u * A_STAGE_BYTES;
-                if (g.a_pair) {  // rows 0-63 from map 0 (gate), rows 64-127 from map 1 (up)
+                if (PAIR) {      // one load, into both CTAs of the pair
+                  if (g.a_pair) {
+                    tma_load_2d_mc(du, &tm0, (kb + u) * BK, mrow, bar_full + 8 * stage, pol, 3);
+                    tma_load_2d_mc(du + A_STAGE_BYTES / 2, &tm1, (kb + u) * BK, mrow, bar_full + 8 * stage, pol, 3);
+                  } else {
+                    tma_load_2d_mc(du, tm, (kb + u) * BK, mrow, bar_full + 8 * stage, pol, 3);
+                  }
+                } else if (g.a_pair) {  // rows 0-63 from map 0 (gate), rows 64-127 from map 1 (up)
                   tma_load_2d(du, &tm0, (kb + u) * BK, mrow, bar_full + 8 * stage, pol);
                   tma_load_2d(du + A_STAGE_BYTES / 2, &tm1, (kb + u) * BK, mrow, bar_full + 8 * stage, pol);
                 } else {
@@ -787,6 +807,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
         // let copies already issued land before the CTA releases its shared memory
         const long long t0 = clock64();
         while (clock64() - t0 < 4000000) {
+        }
+      } else if (PAIR) {
+        // every stage released once more: all of both CTAs' commits (remote arrivals on this
+        // CTA's barriers) have landed before the pair's closing cluster barrier
+        for (int s = 0; s < g.stages && ok; ++s) {
+          ok = mbar_wait(bar_empty + 8 * stage, phase ^ 1, g.err, abort_flag, wlim);
+          if (++stage == g.stages) { stage = 0; phase ^= 1; }
         }
       }
     }
@@ -824,7 +851,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
   #pragma unroll
                 for (int j = 0; j < BK / 16; ++j)   // 16 bf16 of K = 32 bytes = 2 descriptor units
                   tc_mma_bf16(d, ad + 2 * j, bd + 2 * j, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
-                tc_commit(bar_empty + 8 * stage);
+                if (PAIR) tc_commit_mc(bar_empty + 8 * stage, 3);
+                else tc_commit(bar_empty + 8 * stage);
                 if (++stage == g.stages) { stage = 0; phase ^= 1; }
               }
             }
@@ -842,7 +870,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
                 for (int j = 0; j < BK / 16; ++j)
                   tc_mma_bf16(d, ad + astep2 + 2 * j, bd + bstep2 + 2 * j, idesc, 1u);
               }
-              tc_commit(bar_empty + 8 * stage);
+              if (PAIR) tc_commit_mc(bar_empty + 8 * stage, 3);
+              else tc_commit(bar_empty + 8 * stage);
               if (++stage == g.stages) { stage = 0; phase ^= 1; }
               kb += 2;
             }
@@ -1049,7 +1078,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
         tc_fence_after();
         const bool complete = kb0 == 0 && kb1 == KB;
         const int slot = (mt == u0 / KB) ? 0 : 1;   // the CTA's first tile or its last
-        float* mypart = g.part + (static_cast<size_t>(blockIdx.x) * 2 + slot) * rows_total * BM;
+        float* mypart = g.part + (static_cast<size_t>(cta) * 2 + slot) * rows_total * BM;
         for (int rb = 0; rb < nrb; ++rb) {
           for (int c0 = 0; c0 < npad; c0 += 16) {
             const int n0 = rb * npad + c0;
@@ -1126,7 +1155,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
         i += kb1 - kb0;
       }
     }
-    if (g.e.kind == EPI_LMHEAD) lmhead_flush(g, es, blockIdx.x, tl);
+    if (g.e.kind == EPI_LMHEAD) lmhead_flush(g, es, cta, ncta, tl);
   }
 
   if (g.csplit > 1) {
@@ -1184,6 +1213,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
     tc_fence_after();
     tmem_dealloc(tmem, g.tmem_cols);
   }
+  if (PAIR) cooperative_groups::this_cluster().sync();   // neither CTA leaves while the other may signal it
 }
 
 // ============================================================ SIMT mainloop (f32)
@@ -1432,7 +1462,7 @@ bool plan_gemm(GemmPlan& p, int N) {
   g.tmem_cols = cols;
   const long long total = static_cast<long long>(g.MT) * g.KB;
   const int sms = num_sms();
-  p.grid = static_cast<int>(std::min<long long>(sms, total));
+  p.grid = p.pair ? 2 * static_cast<int>(std::min<long long>(sms / 2, total)) : static_cast<int>(std::min<long long>(sms, total));
   p.grid_y = 1;
   const int topk = std::max(1, g.e.topk);
   const int lm_rows = g.e.kind == EPI_LMHEAD ? N : 0;
@@ -1483,6 +1513,7 @@ bool plan_gemm(GemmPlan& p, int N) {
     g.csplit = 0;
     p.grid = static_cast<int>(std::min<long long>(sms, total));
   }
+  if (p.pair && (g.csplit != 0 || p.occ != 1 || g.kpair)) return false;
   g.stages = stages;
   p.smem = tc_smem_bytes(g.npad, stages, lm_rows, topk, staged, g.kpair);
   if (g.b_tma) {
@@ -1494,8 +1525,42 @@ bool plan_gemm(GemmPlan& p, int N) {
   return true;
 }
 
+bool plan_gemm_pair(GemmPlan& p, int N, size_t part_half) {
+  const int per = (N + 1) / 2, n1 = N - per;
+  if (!p.tc || !p.args.b_tma || n1 < 1 || per > MAX_ROWS_PER_BLOCK) return false;
+  const EpiKind ek = static_cast<EpiKind>(p.args.e.kind);
+  if (ek != EPI_STORE && ek != EPI_QKV && ek != EPI_SWIGLU && ek != EPI_LOGITS) return false;
+  p.pair = true;
+  p.stream_k = true;
+  p.occ = 1;
+  const uint16_t* b_hl = p.b_hl;
+  if (!plan_gemm(p, per)) return false;
+  if (p.args.MT > 8192 || p.args.nrb != 1) return false;
+  // rank 1: the same plan on rows [per, N)
+  GemmArgs& g1 = p.args1;
+  g1 = p.args;
+  g1.N = n1;
+  EpiArgs& e = g1.e;
+  if (e.out) e.out += static_cast<size_t>(per) * e.ldo;
+  if (e.resid) e.resid += static_cast<size_t>(per) * e.ldr;
+  if (e.ss) e.ss += per;
+  if (e.hl) e.hl += 2 * static_cast<size_t>(per) * e.hl_ld;
+  if (e.nss) e.nss += per;
+  if (e.q) e.q += static_cast<size_t>(per) * e.Hq * e.hd;
+  if (e.row_req) e.row_req += per;
+  if (e.row_slot) e.row_slot += per;
+  if (e.row_pos) e.row_pos += per;
+  if (e.logits) e.logits += static_cast<size_t>(per) * g1.M;
+  if (e.seeds) e.sample_row0 += per;
+  g1.counters = p.args.counters + 8192;
+  g1.part = p.args.part + part_half;
+  return make_act_map(&p.tmB1, b_hl + 2 * static_cast<size_t>(per) * g1.K, 2 * n1, g1.K, 2 * g1.npad);
+}
+
 cudaError_t gemm_setup_attributes() {
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS, 1, false>), &g_tc_smem_cap);
+  if (e != cudaSuccess) return e;
+  e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS_TMA, 1, false, true>));
   if (e != cudaSuccess) return e;
   e = allow_max_smem(reinterpret_cast<const void*>(gemm_tc_kernel<TC_THREADS_TMA, 2, false>));
   if (e != cudaSuccess) return e;
@@ -1516,23 +1581,32 @@ cudaError_t launch_gemm(const GemmPlan& p, cudaStream_t st, bool pdl) {
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = p.tc && p.args.csplit > 1 ? 2 : 1;
+  cfg.numAttrs = p.tc && (p.args.csplit > 1 || p.pair) ? 2 : 1;
   cfg.stream = st;
   cfg.dynamicSmemBytes = p.smem;
   if (p.tc) {
     cfg.gridDim = dim3(p.grid, 1, 1);
+    if (p.pair) {   // clusters of two CTAs sharing the weight stream
+      attr[1].val.clusterDim.x = 2;
+      cfg.blockDim = dim3(TC_THREADS_TMA, 1, 1);
+      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 1, false, true>, p.tm0, p.tm1, p.tmB, p.args,
+                                p.tmB1, p.args1);
+    }
     if (p.occ == 2) {
       cfg.blockDim = dim3(TC_THREADS_TMA, 1, 1);
-      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 2, false>, p.tm0, p.tm1, p.tmB, p.args);
+      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 2, false>, p.tm0, p.tm1, p.tmB, p.args, p.tmB,
+                                p.args);
     }
     if (p.args.b_tma) {   // no converter warps: the full register file for 7 warps
       cfg.blockDim = dim3(TC_THREADS_TMA, 1, 1);
       if (p.args.e.kind == EPI_LMHEAD && p.args.N <= 16)   // stream-K with the split tiles first
-        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 1, true>, p.tm0, p.tm1, p.tmB, p.args);
-      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 1, false>, p.tm0, p.tm1, p.tmB, p.args);
+        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 1, true>, p.tm0, p.tm1, p.tmB, p.args, p.tmB,
+                                  p.args);
+      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS_TMA, 1, false>, p.tm0, p.tm1, p.tmB, p.args, p.tmB,
+                                p.args);
     }
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS, 1, false>, p.tm0, p.tm1, p.tmB, p.args);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC_THREADS, 1, false>, p.tm0, p.tm1, p.tmB, p.args, p.tmB, p.args);
   }
   cfg.gridDim = dim3(p.grid, p.grid_y, 1);
   cfg.blockDim = dim3(256, 1, 1);

@@ -21,7 +21,17 @@ struct GemmPlan {
   size_t smem = 0;
   int occ = 1;                   // tc with TMA operand: 2 = two CTAs per SM (smaller ring)
   bool stream_k = false;         // force the stream-K schedule (no per-tile CTA clusters)
+  // pair: clusters of two CTAs sharing the weight stream, rank 1 on the rows of args1 / tmB1
+  bool pair = false;
+  GemmArgs args1{};
+  CUtensorMap tmB1;
 };
+
+// Plans GEMM p over N > 128 rows (TMA operand, STORE / QKV / SWIGLU / LOGITS epilogue) as one
+// launch of CTA pairs: rank 0 on the first ceil(N/2) rows, rank 1 on the rest, each weight
+// stage loaded once for both.  `part_half` floats of split-K scratch and 8192 counters apart
+// per rank.  Returns false when the shape does not fit.
+bool plan_gemm_pair(GemmPlan& p, int N, size_t part_half);
 
 // Allow `func` the device's opt-in maximum of dynamic shared memory (minus its static use).
 cudaError_t allow_max_smem(const void* func, size_t* granted = nullptr);

@@ -351,7 +351,7 @@ lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, i
   int nvalid = 0;
 #pragma unroll
   for (int j = 0; j < SEL_PER; ++j) {
-    sm += v[j] == -INFINITY ? 0.f : expf(v[j] - m);   // (a NaN logit makes the sum NaN)
+    sm += v[j] == -INFINITY ? 0.f : __expf(v[j] - m);   // (a NaN logit makes the sum NaN)
     const int i = tid + SEL_THREADS * j;
     kr[j] = i < len ? key_bits(seeds ? v[j] + token_gumbel(base + i, si, sample_depth, sd) : v[j]) : 0u;
     tmax = max(tmax, kr[j]);

@@ -26,7 +26,7 @@ def _seeds(B, base):
     return np.array([(base * 0x9E3779B97F4A7C15 + 0x1234567 * (b + 1)) % 2 ** 64 for b in range(B)], np.uint64)
 
 
-@pytest.mark.parametrize("name", ["small_dyn", "small_static", "small_fused", "small_max", "small_f32", "small_wide"])
+@pytest.mark.parametrize("name", ["small_dyn", "small_static", "small_fused", "small_max", "small_f32", "small_wide", "small_pairs"])
 def test_sampled_tree_matches_oracle(lib, name):
     cfg = configs.get(name)
     W, I = synth.make_weights(cfg), synth.make_inputs(cfg)

@@ -19,7 +19,7 @@ def lib():
     return eb.load()
 
 
-SMALL = ["tiny_chain", "small_f32", "small_dyn", "small_static", "small_fused", "small_max", "small_wide"]
+SMALL = ["tiny_chain", "small_f32", "small_dyn", "small_static", "small_fused", "small_max", "small_wide", "small_pairs"]
 
 
 @pytest.mark.parametrize("name", SMALL)
