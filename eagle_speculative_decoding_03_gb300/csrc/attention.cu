@@ -18,6 +18,7 @@
 
 #include <cooperative_groups.h>
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 namespace cg = cooperative_groups;
 
@@ -813,6 +814,12 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
       best_cs = cs;
       best_cost = cost;
     }
+  }
+  // tuning override: EAGLE_ATTN_CLUSTER = a cluster size to use when the device holds such
+  // clusters (sweeps of the launch shape); unset or 0 keeps the cost model's choice
+  if (const char* ov = getenv("EAGLE_ATTN_CLUSTER")) {
+    const int cs = atoi(ov);
+    if (cs >= 1 && cs <= cmax && cs <= a.max_splits && active_clusters(tc, cs, smem) > 0) best_cs = cs;
   }
   if (!best_cs) return cudaErrorInvalidConfiguration;
   attr[1].val.clusterDim.x = best_cs;

@@ -1021,7 +1021,7 @@ cudaError_t launch_lm_select(const float* logits, int N, int vocab, int k, const
   if (span > SEL_MAX_SPAN || k < 1 || k > KMAX || lm.G != parts || lm.T != parts) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(N * parts), dim3(SEL_THREADS),
-                                    sizeof(uint32_t) * (span + span / 32 + 1), st, pdl, attr);
+                                    sizeof(uint32_t) * (span + span / 32), st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, lm_select_kernel, logits, vocab, span, parts, k, seeds, sample_rows, sample_depth,
                             row0, lm.max + static_cast<size_t>(row0) * parts, lm.sum + static_cast<size_t>(row0) * parts,
                             lm.val + static_cast<size_t>(row0) * parts * k, lm.id + static_cast<size_t>(row0) * parts * k);
