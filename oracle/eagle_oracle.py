@@ -205,12 +205,25 @@ class _Req:
         return tuple(reversed(out))
 
 
-def _choose(values, k, keys, forced, tol, log, what):
-    """Exact top-k, or the forced choice when it is a valid top-k up to tol."""
+def _choose(values, k, keys, forced, tol, log, what, ordered=False):
+    """Exact top-k, or the forced choice when it is a valid top-k up to tol.
+
+    With ``ordered`` the order of the choice is part of the decision (sampled children are
+    kept in draw order, and a child's slot picks the noise its own row draws later): a
+    forced choice must then also list its values in descending order up to tol."""
     exact, margin = top_k(values, k, keys)
     if forced is None:
         return exact, margin
     forced = np.asarray(forced, dtype=np.int64)
+    if ordered:
+        if np.array_equal(forced, exact):
+            return exact, margin
+        if is_valid_top_k(values, forced, k, tol) and \
+                bool(np.all(values[forced[:-1]] >= values[forced[1:]] - tol)):
+            log["forced"].append(what)
+            return forced, margin
+        log["mismatch"].append(what)
+        return exact, margin
     if set(forced.tolist()) == set(exact.tolist()):
         return exact, margin
     if is_valid_top_k(values, forced, k, tol):
@@ -266,7 +279,8 @@ def expand_tree(cfg: dict, n_prefix, root_tok, step, force: dict | None = None,
             key = logp[i]
             if seeds is not None:           # draw order: largest perturbed value first
                 key = logp[i] + sampling.gumbel(len(logp[i]), r.frontier.index(u), s, int(seeds[b]))
-            sel, margin = _choose(key, kids, None, forced, tol, log, ("children", s, i))
+            sel, margin = _choose(key, kids, None, forced, tol, log, ("children", s, i),
+                                  ordered=seeds is not None)
             log["margins"].append(("children", s, i, margin))
             if seeds is None:
                 sel = np.sort(sel)

@@ -161,3 +161,22 @@ def test_sampler_reproduces_the_target_on_small_trees():
             second.setdefault(0, np.zeros(V))[emitted[1]] += 1
     assert _chi2(first, p_root) < CHI2_9999[V - 1]
     assert _chi2(second[0], p_c) < CHI2_9999[V - 1]
+
+
+def test_sampled_children_compare_their_draw_order():
+    """In sampled drafting the draw order is part of the decision (a child's slot picks the
+    noise of its own row later): the other side's order is adopted at a near-tie of the
+    perturbed values and is a mismatch beyond it; the greedy comparison ignores order."""
+    from oracle.eagle_oracle import _choose
+    v = np.array([0.1, 2.0, 1.0, 1.0 + 4e-4, -3.0, 0.5])
+    def run(forced, ordered):
+        log = {"forced": [], "mismatch": [], "margins": []}
+        sel, _ = _choose(v, 3, None, forced, 1e-3, log, "w", ordered=ordered)
+        return sel.tolist(), log
+    assert run([1, 3, 2], True) == ([1, 3, 2], {"forced": [], "mismatch": [], "margins": []})
+    sel, log = run([1, 2, 3], True)               # swapped within 4e-4: adopted
+    assert sel == [1, 2, 3] and log["forced"] == ["w"] and not log["mismatch"]
+    sel, log = run([2, 1, 3], True)               # 1.0 drawn before 2.0: a real difference
+    assert sel == [1, 3, 2] and log["mismatch"] == ["w"]
+    sel, log = run([2, 1, 3], False)              # greedy: the set decides
+    assert sel == [1, 3, 2] and not log["mismatch"] and not log["forced"]
