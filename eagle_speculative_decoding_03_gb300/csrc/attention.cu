@@ -18,7 +18,9 @@
 
 #include <cooperative_groups.h>
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 namespace cg = cooperative_groups;
 
@@ -292,30 +294,7 @@ tree_attention_kernel(const AttnArgs a) {
   cluster.sync();   // the other CTAs' shared memory stays alive until every read is done
 }
 
-// ============================================================ tensor-core path
-// bf16 prefix cache, head_dim 128.  Same cluster decomposition and merge as above; the
-// inner products run on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate)
-// with the fp32 operands (queries, probabilities, tree-row keys and values) split into
-// bf16 hi + lo parts, so each product keeps ~16 significant bits: S = Qhi K + Qlo K,
-// O += Phi V + Plo V (the bf16 cache is exact in bf16).  Warp (m, s) owns query vectors
-// [16 m, 16 m + 16) and the 16-key groups s, s + KS, ... of every chunk; its online
-// softmax state (row max, row sum, output tile) stays in registers.  Keys and values of
-// the CTA's prefix chunks stream through a 4-stage cp.async ring.
-constexpr int TA_HD = 128;
-constexpr int TA_ROWB = TA_HD * 2 + 16;                 // smem row stride: conflict-free ldmatrix
-constexpr int TA_TILE = ATT_CHUNK * TA_ROWB;             // one 64-key tile (bytes)
-constexpr int TA_NST = 4;
-constexpr size_t TA_RING = static_cast<size_t>(TA_NST) * 2 * TA_TILE;
-constexpr size_t TA_TREE = static_cast<size_t>(4) * TA_TILE;   // tree keys / values, hi and lo
-constexpr int TA_MAX_QV = 128;
-constexpr size_t TA_SMEM = TA_RING + TA_TREE + 4 * sizeof(float) * 4 * TA_MAX_QV;
-static_assert(sizeof(float) * TA_MAX_QV * TA_HD <= TA_RING, "merge state must fit the ring");
-
-EAGLE_DEV void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;   // 0: fill with zeros, read nothing
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-EAGLE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// ----------------------------------------------------------- shared helpers
 template <int N>
 EAGLE_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
@@ -342,334 +321,449 @@ EAGLE_DEV void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
   lo = lx | (static_cast<uint32_t>(ly) << 16);
 }
 
-// key groups (of 16) per warp for WM query tiles of 16 vectors on 8 warps
-__host__ __device__ inline int ta_key_splits(int wm) { return wm <= 2 ? 4 : (wm <= 4 ? 2 : 1); }
+// ============================================================ tensor-core path
+// bf16 prefix cache, head size 128, at most 128 query vectors (rows x query heads of the KV
+// group) per CTA.  Same cluster decomposition and merge as the SIMT kernel; per 64-key tile
+// the two products run on the 5th-generation tensor cores (tcgen05.mma, accumulators in
+// tensor memory):
+//   S   [query x key] = Q K^T     A = queries (bf16 hi and lo parts, 128 rows), B = key tile
+//   O^T [dim x query] += V^T P^T  A = value tile (MN-major), B = probabilities (hi and lo)
+// so each product keeps ~16 significant bits of the fp32 operands (the bf16 cache is exact;
+// tree-row keys and values, fp32, are split into hi and lo as well: three products).
+// Prefix tiles arrive by TMA (a 3-D map over [token][kv head][dim]); the last, partial tile
+// of a request is loaded shifted back to end on its last key, so no copy reads past the
+// request (rows before its first new key are masked).  S has two TMEM buffers (the next
+// tile's QK^T overlaps this tile's softmax), O^T stays in TMEM for the whole pass.
+// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2-3 tree-tile converters,
+// 4-7 softmax (thread = query vector = TMEM lane of S; = head dimension lane of O^T).  The
+// running max is raised only when a tile exceeds it by more than 2^8 (then the O^T
+// columns are rescaled in TMEM), so probabilities stay below 2^8.
+constexpr int UA_THREADS = 256;
+constexpr int UA_HD = 128;
+constexpr uint32_t UA_QPART = 32768;     // Q hi or Q lo: 128 rows x 128 dims (two 64-dim blocks)
+constexpr uint32_t UA_KBLK = 8192;       // 64 keys x 64 dims bf16, 128-byte swizzle
+constexpr uint32_t UA_SLOT = 4 * UA_KBLK;   // ring slot: K (dims 0-63, 64-127) | V (same)
+constexpr uint32_t UA_MISC = 2304;       // barriers, flags, rescale factors, merge m / l
+constexpr float UA_RESCALE = 8.0f;       // log2 units
+constexpr int UA_MAX_STAGES = 4;
+constexpr int UA_PREFETCH = 6;           // tiles requested into L2 ahead of their ring slot
 
-struct TaWarp {
-  uint32_t qh[8][4], ql[8][4];     // query fragments (A), 8 k-steps of 16 dims
-  float o[16][4];                  // output tile 16 x 128
-  float m0, m1, l0, l1;            // rows g and g + 8: running max (log2 units), partial sums
-  unsigned long long mk0, mk1;     // ancestor masks of the rows (tree chunk)
-};
-
-// one chunk (64 keys) for warp (its query tile, key groups ks, ks + KS, ...)
-template <bool TREE>
-EAGLE_DEV void ta_chunk(TaWarp& w, uint32_t khi, uint32_t klo, uint32_t vhi, uint32_t vlo, int nkeys, int ks,
-                        int KS, int lane) {
-  const int t4 = lane & 3;
-  float s[4][2][4];
-#pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    if (gi * KS + ks >= 4) break;
-    const int kg = ks + gi * KS;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[gi][nt][e] = 0.f;
-      const int key0 = kg * 16 + nt * 8;
-      const uint32_t roff = (key0 + (lane & 7)) * TA_ROWB + (lane >> 3) * 16;
-#pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(khi + roff + k2 * 64, b0, b1, b2, b3);
-        mma_bf16(s[gi][nt], w.qh[2 * k2], b0, b1);
-        mma_bf16(s[gi][nt], w.ql[2 * k2], b0, b1);
-        mma_bf16(s[gi][nt], w.qh[2 * k2 + 1], b2, b3);
-        mma_bf16(s[gi][nt], w.ql[2 * k2 + 1], b2, b3);
-        if (TREE) {
-          ldsm_x4(klo + roff + k2 * 64, b0, b1, b2, b3);
-          mma_bf16(s[gi][nt], w.qh[2 * k2], b0, b1);
-          mma_bf16(s[gi][nt], w.qh[2 * k2 + 1], b2, b3);
-        }
-      }
-      // visibility: key inside the chunk, and (tree rows) an ancestor of the query's row
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = key0 + 2 * t4 + (e & 1);
-        bool vis = key < nkeys;
-        if (TREE) vis = vis && (((e < 2 ? w.mk0 : w.mk1) >> key) & 1ull);
-        if (!vis) s[gi][nt][e] = -INFINITY;
-      }
-    }
-  }
-  // online softmax (log2 units; the queries carry log2(e) / sqrt(d))
-  float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    if (gi * KS + ks >= 4) break;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      mx0 = fmaxf(mx0, fmaxf(s[gi][nt][0], s[gi][nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[gi][nt][2], s[gi][nt][3]));
-    }
-  }
-#pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-  }
-  const float mn0 = fmaxf(w.m0, mx0), mn1 = fmaxf(w.m1, mx1);
-  const float al0 = w.m0 == -INFINITY ? 0.f : exp2f(w.m0 - mn0);
-  const float al1 = w.m1 == -INFINITY ? 0.f : exp2f(w.m1 - mn1);
-  w.m0 = mn0;
-  w.m1 = mn1;
-  float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    if (gi * KS + ks >= 4) break;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float mn = e < 2 ? mn0 : mn1;
-        const float pv = mn == -INFINITY ? 0.f : exp2f(s[gi][nt][e] - mn);
-        s[gi][nt][e] = pv;
-        if (e < 2) ps0 += pv; else ps1 += pv;
-      }
-    }
-  }
-  w.l0 = w.l0 * al0 + ps0;
-  w.l1 = w.l1 * al1 + ps1;
-#pragma unroll
-  for (int dn = 0; dn < 16; ++dn) {
-    w.o[dn][0] *= al0;
-    w.o[dn][1] *= al0;
-    w.o[dn][2] *= al1;
-    w.o[dn][3] *= al1;
-  }
-  // O += P V over this warp's key groups
-#pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    if (gi * KS + ks >= 4) break;
-    const int kg = ks + gi * KS;
-    uint32_t ph[4], pl[4];
-    split2(s[gi][0][0], s[gi][0][1], ph[0], pl[0]);
-    split2(s[gi][0][2], s[gi][0][3], ph[1], pl[1]);
-    split2(s[gi][1][0], s[gi][1][1], ph[2], pl[2]);
-    split2(s[gi][1][2], s[gi][1][3], ph[3], pl[3]);
-    const int mi = lane >> 3;
-    const uint32_t roff = (kg * 16 + (mi & 1) * 8 + (lane & 7)) * TA_ROWB + (mi >> 1) * 16;
-#pragma unroll
-    for (int d2 = 0; d2 < 8; ++d2) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(vhi + roff + d2 * 32, b0, b1, b2, b3);
-      mma_bf16(w.o[2 * d2], ph, b0, b1);
-      mma_bf16(w.o[2 * d2], pl, b0, b1);
-      mma_bf16(w.o[2 * d2 + 1], ph, b2, b3);
-      mma_bf16(w.o[2 * d2 + 1], pl, b2, b3);
-      if (TREE) {
-        ldsm_x4_t(vlo + roff + d2 * 32, b0, b1, b2, b3);
-        mma_bf16(w.o[2 * d2], ph, b0, b1);
-        mma_bf16(w.o[2 * d2 + 1], ph, b2, b3);
-      }
-    }
-  }
+__host__ __device__ inline uint32_t ua_p_bytes(int qvp) { return static_cast<uint32_t>(qvp) * 128u; }
+__host__ __device__ inline uint32_t ua_ring_off(int qvp) { return 2 * UA_QPART + 4 * ua_p_bytes(qvp); }
+__host__ __device__ inline size_t ua_smem_bytes(int qvp, int stages) {
+  return static_cast<size_t>(ua_ring_off(qvp)) + static_cast<size_t>(stages) * UA_SLOT + UA_MISC + 1024;
 }
 
-__global__ void __launch_bounds__(ATT_THREADS, 1)
-tree_attention_tc_kernel(const AttnArgs a) {
-  extern __shared__ __align__(128) uint8_t ta_smem[];
+// byte offset of 16-byte chunk c (0-7) of row r in a 128-byte-swizzled block of 128-byte rows
+EAGLE_DEV uint32_t ua_sw(int r, int c) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// 8 floats -> 8 bf16 hi parts and 8 bf16 lo parts, packed
+EAGLE_DEV void ua_split8(const float* x, uint4& hi, uint4& lo) {
+  split2_packed(x[0], x[1], hi.x, lo.x);
+  split2_packed(x[2], x[3], hi.y, lo.y);
+  split2_packed(x[4], x[5], hi.z, lo.z);
+  split2_packed(x[6], x[7], hi.w, lo.w);
+}
+EAGLE_DEV void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(UA_THREADS, 1)
+tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                         const AttnArgs a, const int qvp, const int NS) {
+  extern __shared__ uint8_t ua_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ua_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
-  // blockIdx.z = request * row groups + group: a request's rows may be split into groups
-  // of rows_per_group (each its own cluster, each reading the whole prefix) so that no CTA
-  // holds more than TA_MAX_QV query vectors
+  // blockIdx.z = request * row groups + group (see the SIMT kernel)
   const int G = a.row_groups > 1 ? a.row_groups : 1;
   const int kvh = blockIdx.y, b = blockIdx.z / G, grp = blockIdx.z - (blockIdx.z / G) * G;
   const int rpg = G > 1 ? a.rows_per_group : a.rows_per_req;
   const int rfirst = grp * rpg;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
   const int gq = a.Hq / a.Hkv;
   const int qv = max(0, min(rpg, a.rows_per_req - rfirst)) * gq;
-  const int WM = (qv + 15) >> 4, SROW = WM * 16;
-  const int KS = ta_key_splits(WM);
-  const int mt = warp / KS, ks = warp - mt * KS;
-  const bool active = mt < WM;
-  uint8_t* ring = ta_smem;
-  uint8_t* trees = ta_smem + TA_RING;
-  float* mst = reinterpret_cast<float*>(trees + TA_TREE);   // [KS][SROW]
-  float* lst = mst + 4 * TA_MAX_QV;
-  const uint32_t ring_u = smem_u32(ring), tree_u = smem_u32(trees);
-
-  // The prefix keys and values are inputs of the draft step that none of its kernels
-  // write, so the ring's first stages are issued before the wait on the previous kernel;
-  // the prefix length is clamped here the way the roots kernel clamps (and reports) it.
-  const int nb = min(max(__ldg(a.cu_seqlens + b + 1) - __ldg(a.cu_seqlens + b), 0), a.max_prefix);
-  const int npre = (nb + ATT_CHUNK - 1) / ATT_CHUNK;
   const int row0 = b * a.rows_per_req + rfirst;
-  const size_t kv_ld = static_cast<size_t>(a.Hkv) * TA_HD;
-  const size_t base = (static_cast<size_t>(__ldg(a.cu_seqlens + b)) * a.Hkv + kvh) * TA_HD;
-  const uint16_t* kc = static_cast<const uint16_t*>(a.k_cache) + base;
-  const uint16_t* vc = static_cast<const uint16_t*>(a.v_cache) + base;
-  const int np = rank < npre ? (npre - 1 - rank) / cs + 1 : 0;   // prefix chunks rank, rank + cs, ...
-  const bool has_tree = npre % cs == rank;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  auto issue = [&](int i) {
-    if (i < np) {
-      const int c = rank + i * cs;
-      const int nk = min(ATT_CHUNK, nb - c * ATT_CHUNK);
-      const uint32_t kt = ring_u + (i % TA_NST) * 2 * TA_TILE, vt = kt + TA_TILE;
-      for (int idx = tid; idx < ATT_CHUNK * 16; idx += ATT_THREADS) {
-        const int j = idx >> 4, p = idx & 15;
-        const bool ok = j < nk;
-        const size_t off = static_cast<size_t>(c * ATT_CHUNK + j) * kv_ld + p * 8;
-        cp_async16(kt + j * TA_ROWB + p * 16, ok ? kc + off : kc, ok);
-        cp_async16(vt + j * TA_ROWB + p * 16, ok ? vc + off : vc, ok);
-      }
+  const uint32_t pbytes = ua_p_bytes(qvp);
+  const uint32_t q_u = sb, p_u = sb + 2 * UA_QPART, ring_u = sb + ua_ring_off(qvp);
+  uint8_t* misc = sm + ua_ring_off(qvp) + static_cast<uint32_t>(NS) * UA_SLOT;
+  const uint32_t misc_u = smem_u32(misc);
+  const uint32_t bar_kvf = misc_u, bar_kve = misc_u + 32, bar_sf = misc_u + 64, bar_se = misc_u + 80,
+                 bar_pf = misc_u + 96, bar_pe = misc_u + 112, bar_od = misc_u + 128, bar_tg = misc_u + 136,
+                 bar_tf = misc_u + 144, bar_fin = misc_u + 152;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 160);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 164);
+  int* tree_slot = reinterpret_cast<int*>(misc + 168);
+  float* fac = reinterpret_cast<float*>(misc + 256);   // [2][128] rescale factor per query vector
+  float* mcta = fac + 256;                             // [128] the CTA's final state per vector
+  float* lcta = mcta + 128;
+  float* st = reinterpret_cast<float*>(sm);            // [qv][128] un-normalised output (Q region, at the end)
+
+  // this CTA's keys: prefix tiles rank, rank + cs, ... and (one CTA) the tree tile
+  const int tok0 = __ldg(a.cu_seqlens + b);
+  const int nb = min(max(__ldg(a.cu_seqlens + b + 1) - tok0, 0), a.max_prefix);
+  const int npre = (nb + ATT_CHUNK - 1) / ATT_CHUNK;
+  const int np = rank < npre ? (npre - 1 - rank) / cs + 1 : 0;
+  const bool has_tree = npre % cs == rank;
+  const int T = np + (has_tree ? 1 : 0);
+  const long long wlim = a.wait_limit > 0 ? a.wait_limit : WAIT_LIMIT_CYCLES;
+
+  if (tid == 0) {
+    for (int s = 0; s < UA_MAX_STAGES; ++s) {
+      mbar_init(bar_kvf + 8 * s, 1);
+      mbar_init(bar_kve + 8 * s, 1);
     }
-    cp_async_commit();
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_sf + 8 * i, 1);
+      mbar_init(bar_se + 8 * i, 4);
+      mbar_init(bar_pf + 8 * i, 4);
+      mbar_init(bar_pe + 8 * i, 1);
+    }
+    mbar_init(bar_od, 1);
+    mbar_init(bar_tg, 1);
+    mbar_init(bar_tf, 2);
+    mbar_init(bar_fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // The prefix cache is an input of the draft step that none of its kernels write: the
+  // first ring slots are filled before the wait on the previous kernel.
+  const uint64_t pol = a.kv_keep ? policy_evict_last() : policy_evict_first();
+  // first token of tile t (a partial tile is shifted back to end on the request's last key)
+  auto tile_t0 = [&](int t) {
+    const int c = rank + t * cs;
+    return tok0 + c * ATT_CHUNK - (ATT_CHUNK - min(ATT_CHUNK, nb - c * ATT_CHUNK));
   };
-#pragma unroll
-  for (int i = 0; i < TA_NST; ++i) issue(i);
+  // tiles are also requested into L2 UA_PREFETCH tiles ahead of their ring slot: a slot is
+  // refilled only once the tile that held it is done, so its copy then comes from L2
+  auto prefetch = [&](int t) {
+    if (t >= np) return;
+    const int t0 = tile_t0(t);
+    tma_prefetch_l2_3d(&tmk, 0, kvh, t0);
+    tma_prefetch_l2_3d(&tmk, 64, kvh, t0);
+    tma_prefetch_l2_3d(&tmv, 0, kvh, t0);
+    tma_prefetch_l2_3d(&tmv, 64, kvh, t0);
+  };
+  auto issue = [&](int t) {
+    const int slot = t % NS;
+    const int t0 = tile_t0(t);
+    const uint32_t dst = ring_u + slot * UA_SLOT, bar = bar_kvf + 8 * slot;
+    mbar_arrive_expect_tx(bar, UA_SLOT);
+    tma_load_3d(dst, &tmk, 0, kvh, t0, bar, pol);
+    tma_load_3d(dst + UA_KBLK, &tmk, 64, kvh, t0, bar, pol);
+    tma_load_3d(dst + 2 * UA_KBLK, &tmv, 0, kvh, t0, bar, pol);
+    tma_load_3d(dst + 3 * UA_KBLK, &tmv, 64, kvh, t0, bar, pol);
+  };
+  const int first = min(NS, np);
+  if (warp == 0 && lane == 0 && np > 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+    for (int t = 0; t < first; ++t) issue(t);
+    for (int t = first; t < first + UA_PREFETCH; ++t) prefetch(t);
+  }
   pdl_wait();
   pdl_trigger();
-  // one batch of loads in flight together: tree rows (if this CTA has the tree chunk),
-  // this warp's queries and its rows' ancestor masks (all written by the previous kernels)
-  constexpr int PER = ATT_CHUNK * (TA_HD / 4) / ATT_THREADS;   // float4 of tree keys (and values) per thread
-  float4 k4[PER], v4[PER];
-  if (has_tree) {
+
+  // queries of this CTA (scaled by log2(e) / sqrt(hd)) -> bf16 hi / lo, 128-byte swizzle;
+  // rows past qv are zero
+  {
+    const float qs = 1.4426950408889634f / sqrtf(static_cast<float>(UA_HD));
+    for (int it = tid; it < 128 * 16; it += UA_THREADS) {
+      const int v = it >> 4, c16 = it & 15;
+      float x[8];
+      if (v < qv) {
+        const int i = v / gq, gh = v - i * gq;
+        const float* src = a.q + (static_cast<size_t>(row0 + i) * a.Hq + kvh * gq + gh) * UA_HD + c16 * 8;
+        const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
+        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
+        x[0] = x0.x * qs; x[1] = x0.y * qs; x[2] = x0.z * qs; x[3] = x0.w * qs;
+        x[4] = x1.x * qs; x[5] = x1.y * qs; x[6] = x1.z * qs; x[7] = x1.w * qs;
+      } else {
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int idx = tid + u * ATT_THREADS;
-      const int j = idx / (TA_HD / 4), d4 = idx - j * (TA_HD / 4);
-      k4[u] = v4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (j < a.tree_upto) {
-        const size_t o = ((static_cast<size_t>(b) * a.tree_rows + j) * a.Hkv + kvh) * TA_HD + 4 * d4;
-        k4[u] = __ldcg(reinterpret_cast<const float4*>(a.tk + o));
-        v4[u] = __ldcg(reinterpret_cast<const float4*>(a.tv + o));
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
       }
+      uint4 hi, lo;
+      ua_split8(x, hi, lo);
+      const uint32_t off = (c16 >> 3) * (UA_QPART / 2) + ua_sw(v, c16 & 7);
+      st_shared_v4(q_u + off, hi);
+      st_shared_v4(q_u + UA_QPART + off, lo);
     }
   }
-  float2 qx[8][4];
-  TaWarp w;
-  w.mk0 = w.mk1 = 0ull;
-  if (active) {
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-#pragma unroll
-      for (int f = 0; f < 4; ++f) {
-        const int v = mt * 16 + g + (f & 1) * 8;
-        const int col = kk * 16 + 2 * t4 + (f >> 1) * 8;
-        qx[kk][f] = make_float2(0.f, 0.f);
-        if (v < qv) {
-          const int i = v / gq, gh = v - i * gq;
-          qx[kk][f] = __ldcg(reinterpret_cast<const float2*>(a.q + (static_cast<size_t>(row0 + i) * a.Hq + kvh * gq + gh) * TA_HD + col));
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  bool ok = true;
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int t = first; t < np + (has_tree ? 2 : 0) && ok; ++t) {   // ring positions
+        const int slot = t % NS;
+        if (t >= NS) ok = mbar_wait_sleepy(bar_kve + 8 * slot, ((t / NS) & 1) ^ 1, a.err, abort_flag, wlim);
+        if (!ok) break;
+        if (t < np) {
+          issue(t);
+          prefetch(t + UA_PREFETCH);
+        } else {
+          tree_slot[t - np] = slot;
+        }   // the tree tile takes two free slots (keys | values)
+      }
+      if (has_tree && ok) mbar_arrive(bar_tg);
+      if (!ok) {   // let copies already issued land before the CTA releases its shared memory
+        const long long t0 = clock64();
+        while (clock64() - t0 < 4000000) {
         }
       }
-    const int v0 = mt * 16 + g, v1 = v0 + 8;
-    if (v0 < qv) w.mk0 = __ldcg(a.row_mask + row0 + v0 / gq);
-    if (v1 < qv) w.mk1 = __ldcg(a.row_mask + row0 + v1 / gq);
-  }
-  if (has_tree) {   // fp32 tree keys / values -> bf16 hi and lo tiles
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int idx = tid + u * ATT_THREADS;
-      const int j = idx / (TA_HD / 4), d4 = idx - j * (TA_HD / 4);
-      uint32_t h0, l0, h1, l1;
-      const size_t so = static_cast<size_t>(j) * TA_ROWB + d4 * 8;
-      split2(k4[u].x, k4[u].y, h0, l0);
-      split2(k4[u].z, k4[u].w, h1, l1);
-      *reinterpret_cast<uint2*>(trees + so) = make_uint2(h0, h1);
-      *reinterpret_cast<uint2*>(trees + TA_TILE + so) = make_uint2(l0, l1);
-      split2(v4[u].x, v4[u].y, h0, l0);
-      split2(v4[u].z, v4[u].w, h1, l1);
-      *reinterpret_cast<uint2*>(trees + 2 * TA_TILE + so) = make_uint2(h0, h1);
-      *reinterpret_cast<uint2*>(trees + 3 * TA_TILE + so) = make_uint2(l0, l1);
     }
-  }
-  w.m0 = w.m1 = -INFINITY;
-  w.l0 = w.l1 = 0.f;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id1 = idesc_bf16_f32(128, 64);
+      const uint32_t id2 = idesc_bf16_f32(128, qvp) | (1u << 15);   // A (values) MN-major
+      const uint32_t tO = tmem + 128;
+      const uint64_t dq_hi = smem_desc_sw128(q_u), dq_lo = smem_desc_sw128(q_u + UA_QPART);
+      const uint64_t dp0 = smem_desc_sw128(p_u);
+      // Step t issues QK^T of tile t (into S buffer t & 1) and P V^T of tile t - 1; the tree
+      // tile (last) takes P V^T first, since its slots may wait for that product's release.
+      // (One copy of each issue sequence: the issue loop stays small.)
+      for (int t = 0; t <= T && ok; ++t) {
+        const bool tree_step = t == np && t < T;
+#pragma unroll 1
+        for (int ph = 0; ph < 2 && ok; ++ph) {
+          if ((ph == 0) != tree_step) {
+            if (t == T) continue;
+            // ---- S = Q K^T for tile t
+            ok = tree_step ? mbar_wait(bar_tf, 0, a.err, abort_flag, wlim)
+                           : mbar_wait(bar_kvf + 8 * (t % NS), (t / NS) & 1, a.err, abort_flag, wlim);
+            ok = ok && mbar_wait(bar_se + 8 * (t & 1), ((t >> 1) & 1) ^ 1, a.err, abort_flag, wlim);
+            if (!ok) break;
+            // (the tree tile's slots are known once the converters signalled)
+            const uint32_t kb = tree_step ? ring_u + tree_slot[0] * UA_SLOT : ring_u + (t % NS) * UA_SLOT;
+            tc_fence_after();
+            const uint32_t d = tmem + (t & 1) * 64;
+            // descriptors move only in their start-address field (16-byte units, no carry)
+            const uint64_t dk = smem_desc_sw128(kb), dkl = dk + ((2 * UA_KBLK) >> 4);
 #pragma unroll
-  for (int dn = 0; dn < 16; ++dn)
+            for (int j = 0; j < UA_HD / 16; ++j) {
+              const uint32_t qo = ((j >> 2) * (UA_QPART / 2) + (j & 3) * 32) >> 4;
+              const uint32_t ko = ((j >> 2) * UA_KBLK + (j & 3) * 32) >> 4;
+              tc_mma_bf16(d, dq_hi + qo, dk + ko, id1, j > 0 ? 1u : 0u);
+              tc_mma_bf16(d, dq_lo + qo, dk + ko, id1, 1u);
+              if (tree_step) tc_mma_bf16(d, dq_hi + qo, dkl + ko, id1, 1u);
+            }
+            tc_commit(bar_sf + 8 * (t & 1));
+          } else {
+            if (t == 0) continue;
+            // ---- O^T += V^T P^T for tile u = t - 1
+            const int u = t - 1;
+            const bool tree = u == np;
+            ok = mbar_wait(bar_pf + 8 * (u & 1), (u >> 1) & 1, a.err, abort_flag, wlim);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vhi = tree ? ring_u + tree_slot[1] * UA_SLOT : ring_u + (u % NS) * UA_SLOT + 2 * UA_KBLK;
+            const uint64_t dv = smem_desc_sw128_mn(vhi, UA_KBLK, 1024), dvl = dv + ((2 * UA_KBLK) >> 4);
+            const uint64_t dph = dp0 + (((u & 1) * 2 * pbytes) >> 4), dpl = dph + (pbytes >> 4);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w.o[dn][e] = 0.f;
-  {
-    const float qs = 1.4426950408889634f / sqrtf(static_cast<float>(TA_HD));
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-#pragma unroll
-      for (int f = 0; f < 4; ++f) split2(qx[kk][f].x * qs, qx[kk][f].y * qs, w.qh[kk][f], w.ql[kk][f]);
-  }
-  for (int i = 0; i < np; ++i) {
-    cp_async_wait<TA_NST - 1>();
-    __syncthreads();
-    if (active) {
-      const int c = rank + i * cs;
-      const uint32_t kt = ring_u + (i % TA_NST) * 2 * TA_TILE;
-      ta_chunk<false>(w, kt, 0, kt + TA_TILE, 0, min(ATT_CHUNK, nb - c * ATT_CHUNK), ks, KS, lane);
-    }
-    __syncthreads();
-    issue(i + TA_NST);
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-  if (has_tree && active)
-    ta_chunk<true>(w, tree_u, tree_u + TA_TILE, tree_u + 2 * TA_TILE, tree_u + 3 * TA_TILE, a.tree_upto, ks, KS, lane);
-  __syncthreads();   // every warp is done with the ring: it now holds the states
-
-  // publish the warp states: output [KS][SROW][hd], row max and row sum [KS][SROW]
-  float* st = reinterpret_cast<float*>(ring);
-  float* mcta = lst + 4 * TA_MAX_QV;   // [SROW] the CTA's merged state
-  float* lcta = mcta + TA_MAX_QV;
-  if (active) {
-    float l0 = w.l0, l1 = w.l1;
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
-    const int v0 = mt * 16 + g;
-    float* r0p = st + (static_cast<size_t>(ks) * SROW + v0) * TA_HD;
-    float* r1p = r0p + 8 * TA_HD;
-#pragma unroll
-    for (int dn = 0; dn < 16; ++dn) {
-      *reinterpret_cast<float2*>(r0p + dn * 8 + 2 * t4) = make_float2(w.o[dn][0], w.o[dn][1]);
-      *reinterpret_cast<float2*>(r1p + dn * 8 + 2 * t4) = make_float2(w.o[dn][2], w.o[dn][3]);
-    }
-    if (t4 == 0) {
-      mst[ks * SROW + v0] = w.m0;
-      mst[ks * SROW + v0 + 8] = w.m1;
-      lst[ks * SROW + v0] = l0;
-      lst[ks * SROW + v0 + 8] = l1;
-    }
-  }
-  __syncthreads();
-  // merge the KS warp states of each query vector inside the CTA (into split 0)
-  if (KS > 1) {
-    for (int idx = tid; idx < SROW * (TA_HD / 4); idx += ATT_THREADS) {
-      const int v = idx / (TA_HD / 4), d4 = idx - v * (TA_HD / 4);
-      float M = -INFINITY;
-      for (int k = 0; k < KS; ++k) M = fmaxf(M, mst[k * SROW + v]);
-      float L = 0.f;
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k = 0; k < KS; ++k) {
-        const float mk = mst[k * SROW + v];
-        const float wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
-        L += wk * lst[k * SROW + v];
-        const float4 x = *reinterpret_cast<const float4*>(st + (static_cast<size_t>(k) * SROW + v) * TA_HD + 4 * d4);
-        o.x += wk * x.x;
-        o.y += wk * x.y;
-        o.z += wk * x.z;
-        o.w += wk * x.w;
+            for (int j = 0; j < ATT_CHUNK / 16; ++j) {   // 16 keys: two 8-key groups of V (1024 bytes), 32 bytes of P
+              tc_mma_bf16(tO, dv + j * 128, dph + 2 * j, id2, (u > 0 || j > 0) ? 1u : 0u);
+              tc_mma_bf16(tO, dv + j * 128, dpl + 2 * j, id2, 1u);
+              if (tree) tc_mma_bf16(tO, dvl + j * 128, dph + 2 * j, id2, 1u);
+            }
+            tc_commit(bar_pe + 8 * (u & 1));
+            if (!tree) tc_commit(bar_kve + 8 * (u % NS));
+            tc_commit(bar_od);
+          }
+        }
       }
-      *reinterpret_cast<float4*>(st + static_cast<size_t>(v) * TA_HD + 4 * d4) = o;   // read by this thread only
-      if (d4 == 0) {
-        mcta[v] = M;
-        lcta[v] = L;
+      if (!ok) {   // let MMAs already issued finish before TMEM is released
+        const long long t0 = clock64();
+        while (clock64() - t0 < 4000000) {
+        }
       }
+      tc_commit(bar_fin);
+    }
+  } else if (warp < 4) {
+    // ------------------------------ tree tile: fp32 keys / values -> bf16 hi / lo tiles
+    if (has_tree) {
+      const int ct = tid - 64;
+      if (mbar_wait_sleepy(bar_tg, 0, a.err, abort_flag, wlim)) {
+        const uint32_t ks = ring_u + tree_slot[0] * UA_SLOT, vs = ring_u + tree_slot[1] * UA_SLOT;
+        for (int it = ct; it < ATT_CHUNK * 16; it += 64) {
+          const int j = it >> 4, c16 = it & 15;
+          float k8[8], v8[8];
+          if (j < a.tree_upto) {
+            const size_t o = ((static_cast<size_t>(b) * a.tree_rows + j) * a.Hkv + kvh) * UA_HD + c16 * 8;
+            const float4 k0 = __ldcg(reinterpret_cast<const float4*>(a.tk + o));
+            const float4 k1 = __ldcg(reinterpret_cast<const float4*>(a.tk + o + 4));
+            const float4 v0 = __ldcg(reinterpret_cast<const float4*>(a.tv + o));
+            const float4 v1 = __ldcg(reinterpret_cast<const float4*>(a.tv + o + 4));
+            k8[0] = k0.x; k8[1] = k0.y; k8[2] = k0.z; k8[3] = k0.w; k8[4] = k1.x; k8[5] = k1.y; k8[6] = k1.z; k8[7] = k1.w;
+            v8[0] = v0.x; v8[1] = v0.y; v8[2] = v0.z; v8[3] = v0.w; v8[4] = v1.x; v8[5] = v1.y; v8[6] = v1.z; v8[7] = v1.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) k8[e] = v8[e] = 0.f;
+          }
+          uint4 kh, kl, vh, vl;
+          ua_split8(k8, kh, kl);
+          ua_split8(v8, vh, vl);
+          const uint32_t off = (c16 >> 3) * UA_KBLK + ua_sw(j, c16 & 7);
+          st_shared_v4(ks + off, kh);
+          st_shared_v4(ks + 2 * UA_KBLK + off, kl);
+          st_shared_v4(vs + off, vh);
+          st_shared_v4(vs + 2 * UA_KBLK + off, vl);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tf);
     }
   } else {
-    for (int v = tid; v < SROW; v += ATT_THREADS) {
-      mcta[v] = mst[v];
-      lcta[v] = lst[v];
+    // ------------------------------------------------------------ softmax
+    const int v = tid - 128;                       // query vector = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const bool live = v < qv;
+    const unsigned long long mrow = (live && has_tree) ? __ldcg(a.row_mask + row0 + v / gq) : 0ull;
+    // tree keys a vector sees: rows that exist so far and are ancestors of (or are) its row
+    const unsigned long long vis_tree =
+        mrow & (a.tree_upto >= 64 ? ~0ull : ((1ull << max(a.tree_upto, 0)) - 1ull));
+    float m_run = -INFINITY, l_run = 0.f;
+    const uint32_t tO = tmem + lane_base + 128;
+    for (int t = 0; t < T; ++t) {
+      const bool tree = t == np;
+      ok = ok && mbar_wait_sleepy(bar_sf + 8 * (t & 1), (t >> 1) & 1, a.err, abort_flag, wlim);
+      tc_fence_after();
+      float s[ATT_CHUNK];
+      if (ok) {
+        const uint32_t ta = tmem + lane_base + (t & 1) * 64;
+        tmem_ld16(ta, s);
+        tmem_ld16(ta + 16, s + 16);
+        tmem_ld16(ta + 32, s + 32);
+        tmem_ld16(ta + 48, s + 48);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_se + 8 * (t & 1));
+      // visible keys of the tile as a bit mask: prefix rows [lo, 64) (a shifted partial tile
+      // starts late), tree rows that exist and are ancestors of (or are) the vector's row
+      const unsigned long long vis =
+          tree ? vis_tree : (~0ull << (ATT_CHUNK - min(ATT_CHUNK, nb - (rank + t * cs) * ATT_CHUNK)));
+      const bool work = live && ok;
+      if (work && vis != ~0ull) {
+#pragma unroll
+        for (int r = 0; r < ATT_CHUNK; ++r) s[r] = ((vis >> r) & 1ull) ? s[r] : -INFINITY;
+      }
+      float mt = -INFINITY;
+      if (work) {
+        float m8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = s[e];
+#pragma unroll
+        for (int r = 8; r < ATT_CHUNK; ++r) m8[r & 7] = fmaxf(m8[r & 7], s[r]);
+        mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      }
+      float f = 1.f, m_use = m_run;
+      bool resc = false;
+      if (mt != -INFINITY) {
+        if (m_run == -INFINITY) {
+          m_use = mt;
+        } else if (mt > m_run + UA_RESCALE) {
+          m_use = mt;
+          f = fast_exp2(m_run - mt);
+          resc = true;
+        }
+      }
+      fac[(t & 1) * 128 + v] = f;
+      if (named_bar_or(1, 128, resc)) {
+        // some vector's max rose: scale its O^T column once every earlier P V^T is done
+        ok = ok && mbar_wait(bar_od, (t - 1) & 1, a.err, abort_flag, wlim);
+        tc_fence_after();
+        if (ok) {
+          for (int c0 = 0; c0 < qvp; c0 += 16) {
+            float x[16];
+            tmem_ld16(tO + c0, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] *= fac[(t & 1) * 128 + c0 + e];
+            tmem_st16(tO + c0, x);
+          }
+          tmem_wait_st();
+        }
+      }
+      m_run = m_use;
+      l_run *= f;
+      // probabilities 2^(s - m) (a masked key gives 2^-inf = 0); rows without a key so far
+      // (and padding rows) write zeros
+      float ps = 0.f;
+      if (work && m_run != -INFINITY) {
+        float p8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) p8[e] = 0.f;
+#pragma unroll
+        for (int r = 0; r < ATT_CHUNK; ++r) {
+          s[r] = fast_exp2(s[r] - m_run);
+          p8[r & 7] += s[r];
+        }
+        ps = ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
+      } else {
+#pragma unroll
+        for (int r = 0; r < ATT_CHUNK; ++r) s[r] = 0.f;
+      }
+      l_run += ps;
+      // P row v (hi, lo) into buffer t & 1 once the product of tile t - 2 released it
+      ok = ok && mbar_wait_sleepy(bar_pe + 8 * (t & 1), ((t >> 1) & 1) ^ 1, a.err, abort_flag, wlim);
+      if (ok && v < qvp) {
+        const uint32_t phi = p_u + (t & 1) * 2 * pbytes, plo = phi + pbytes;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 hi, lo4;
+          ua_split8(s + 8 * c, hi, lo4);
+          st_shared_v4(phi + ua_sw(v, c), hi);
+          st_shared_v4(plo + ua_sw(v, c), lo4);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pf + 8 * (t & 1));
     }
+    // the CTA's state: O^T column v -> st[v][.] (thread = head dimension lane), m and l
+    ok = mbar_wait_sleepy(bar_fin, 0, a.err, abort_flag, wlim) && ok;
+    tc_fence_after();
+    if (ok && T > 0) {
+      for (int c0 = 0; c0 < qvp; c0 += 16) {
+        float x[16];
+        tmem_ld16(tO + c0, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (c0 + e < qv) st[static_cast<size_t>(c0 + e) * UA_HD + v] = x[e];
+      }
+    }
+    mcta[v] = (live && T > 0 && ok) ? m_run : -INFINITY;
+    lcta[v] = l_run;
   }
+  tc_fence_before();
+  __syncthreads();
   cluster.sync();
   // merge the cluster's CTA states (rank order) and normalise
-  const size_t ld = static_cast<size_t>(a.Hq) * TA_HD;
-  for (int idx = rank * ATT_THREADS + tid; idx < qv * (TA_HD / 4); idx += cs * ATT_THREADS) {
-    const int v = idx / (TA_HD / 4), d4 = idx - v * (TA_HD / 4);
+  const size_t ld = static_cast<size_t>(a.Hq) * UA_HD;
+  for (int idx = rank * UA_THREADS + tid; idx < qv * (UA_HD / 4); idx += cs * UA_THREADS) {
+    const int v = idx / (UA_HD / 4), d4 = idx - v * (UA_HD / 4);
     float mr[ATT_MAX_CLUSTER], lr[ATT_MAX_CLUSTER];
     float4 xr[ATT_MAX_CLUSTER];
 #pragma unroll
@@ -680,7 +774,7 @@ tree_attention_tc_kernel(const AttnArgs a) {
       if (r < cs) {
         mr[r] = cluster.map_shared_rank(mcta, r)[v];
         lr[r] = cluster.map_shared_rank(lcta, r)[v];
-        xr[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(st, r) + static_cast<size_t>(v) * TA_HD + 4 * d4);
+        xr[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(st, r) + static_cast<size_t>(v) * UA_HD + 4 * d4);
       }
     }
     float M = -INFINITY;
@@ -690,7 +784,8 @@ tree_attention_tc_kernel(const AttnArgs a) {
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < ATT_MAX_CLUSTER; ++r) {
-      const float wr = mr[r] == -INFINITY ? 0.f : exp2f(mr[r] - M);
+      if (mr[r] == -INFINITY) continue;   // a CTA that saw no key of this vector
+      const float wr = exp2f(mr[r] - M);
       L += wr * lr[r];
       o.x += wr * xr[r].x;
       o.y += wr * xr[r].y;
@@ -703,7 +798,7 @@ tree_attention_tc_kernel(const AttnArgs a) {
     o.z *= inv;
     o.w *= inv;
     const int i = v / gq, gh = v - i * gq;
-    const size_t col = static_cast<size_t>(kvh * gq + gh) * TA_HD + 4 * d4;
+    const size_t col = static_cast<size_t>(kvh * gq + gh) * UA_HD + 4 * d4;
     *reinterpret_cast<float4*>(a.out + static_cast<size_t>(row0 + i) * ld + col) = o;
     if (a.out_hl) {
       uint32_t h0, l0, h1, l1;
@@ -714,24 +809,27 @@ tree_attention_tc_kernel(const AttnArgs a) {
     }
   }
   cluster.sync();
+  if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
 static int rows_per_cta(const AttnArgs& a) {
   return a.row_groups > 1 ? std::min(a.rows_per_group, a.rows_per_req) : a.rows_per_req;
 }
 
+constexpr int UA_MAX_QV = 128;
 static bool use_tc(const AttnArgs& a) {
-  return a.cache_bf16 && a.hd == TA_HD && rows_per_cta(a) * (a.Hq / a.Hkv) <= TA_MAX_QV;
+  return a.cache_bf16 && a.hd == UA_HD && rows_per_cta(a) * (a.Hq / a.Hkv) <= UA_MAX_QV;
 }
 
-int attn_rows_per_group(int Hq, int Hkv) { return TA_MAX_QV / (Hq / Hkv); }
+int attn_rows_per_group(int Hq, int Hkv) { return UA_MAX_QV / (Hq / Hkv); }
 
 static int g_att_cluster = 0;
+static size_t g_ua_smem_cap = 0;
 
 cudaError_t attn_setup_attributes() {
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(tree_attention_kernel));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tree_attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(TA_SMEM));
+  e = allow_max_smem(reinterpret_cast<const void*>(tree_attention_tc_kernel), &g_ua_smem_cap);
   if (e != cudaSuccess) return e;
   if (!g_att_cluster) {
     // 16-CTA clusters when the device schedules them, else the portable 8
@@ -786,7 +884,12 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
                 static_cast<long long>(G - 1) * a.rows_per_group >= a.rows_per_req))
     return cudaErrorInvalidValue;   // groups only on the tensor-core path, each with >= 1 row
   const int qv = rows_per_cta(a) * (a.Hq / a.Hkv);
-  const size_t smem = tc ? TA_SMEM : attn_smem_bytes(qv, a.hd);
+  // tensor-core kernel: queries padded to the MMA's N granule; as many ring slots as fit
+  const int qvp = std::max(16, (qv + 15) / 16 * 16);
+  int stages = UA_MAX_STAGES;
+  while (stages > 2 && ua_smem_bytes(qvp, stages) > g_ua_smem_cap) --stages;
+  if (tc && ua_smem_bytes(qvp, stages) > g_ua_smem_cap) return cudaErrorInvalidConfiguration;
+  const size_t smem = tc ? ua_smem_bytes(qvp, stages) : attn_smem_bytes(qv, a.hd);
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
@@ -826,7 +929,17 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3(best_cs, a.Hkv, a.B * G);
-  if (tc) return cudaLaunchKernelEx(&cfg, tree_attention_tc_kernel, a);
+  if (tc) {
+    // key / value maps over every token the requests may hold (lengths are clamped to
+    // max_prefix, and no tile reads past its request's last key)
+    CUtensorMap tmk, tmv;
+    memset(&tmk, 0, sizeof(tmk));
+    memset(&tmv, 0, sizeof(tmv));
+    const long long tokens = static_cast<long long>(a.B) * a.max_prefix;
+    if (tokens > 0 && (!make_kv_map(&tmk, a.k_cache, tokens, a.Hkv) || !make_kv_map(&tmv, a.v_cache, tokens, a.Hkv)))
+      return cudaErrorInvalidValue;
+return cudaLaunchKernelEx(&cfg, tree_attention_tc_kernel, tmk, tmv, a, qvp, stages);
+  }
   return cudaLaunchKernelEx(&cfg, tree_attention_kernel, a);
 }
 

@@ -39,6 +39,20 @@ EAGLE_DEV uint16_t f32_to_bf16(float x) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
+// hi / lo parts (as above) of two floats, each pair packed with the first float in the low
+// half: one packed round-to-nearest-even conversion for the two hi parts, one for the lo parts
+EAGLE_DEV void split2_packed(float x, float y, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(y), "f"(x));
+  const float hx = __uint_as_float(hi << 16), hy = __uint_as_float(hi & 0xFFFF0000u);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(y - hy), "f"(x - hx));
+}
+// 2^x on the special-function unit (relative error ~2^-22; 2^-inf = 0)
+EAGLE_DEV float fast_exp2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): ~16 significant bits in two bf16s
 EAGLE_DEV void split_hilo(float x, uint16_t& hi, uint16_t& lo) {
   hi = f32_to_bf16(x);
@@ -106,6 +120,20 @@ EAGLE_DEV void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// named barrier that also returns whether `pred` held in any of the `nthreads` threads
+EAGLE_DEV bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // programmatic dependent launch
 EAGLE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 EAGLE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -150,6 +178,27 @@ EAGLE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err, volatile 
     }
   }
 }
+// The same wait for roles that can afford to wake up late: after a few polls the thread
+// sleeps between polls, so a waiting warp neither takes issue slots from its neighbours on the
+// SM sub-partition nor hammers the barrier's shared-memory bank.
+EAGLE_DEV bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, unsigned* err, volatile int* abort_flag,
+                                long long limit = WAIT_LIMIT_CYCLES) {
+  for (int i = 0; i < 4; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > limit) {
+        atomicOr(err, DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
 EAGLE_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 EAGLE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -157,6 +206,11 @@ EAGLE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared
 EAGLE_DEV uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+EAGLE_DEV uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 EAGLE_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, uint32_t bar,
@@ -176,6 +230,20 @@ EAGLE_DEV void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int c0, int c
       " [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask), "l"(policy)
       : "memory");
+}
+EAGLE_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2, uint32_t bar,
+                           uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
+// the same box into L2 only (no shared memory, no barrier)
+EAGLE_DEV void tma_prefetch_l2_3d(const CUtensorMap* tm, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 EAGLE_DEV void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
@@ -235,6 +303,17 @@ EAGLE_DEV void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 EAGLE_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes, from registers
+EAGLE_DEV void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+EAGLE_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle layout that
 // TMA's SWIZZLE_128B writes (rows of 128 bytes, 8-row atoms of 1024 bytes).
@@ -245,6 +324,17 @@ EAGLE_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1024 >> 4) << 32;             // stride byte offset: next 8-row atom
   d |= static_cast<uint64_t>(1) << 46;                     // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                     // layout: 128-byte swizzle
+  return d;
+}
+// The same for an MN-major operand (the MN index runs along the 128-byte rows): 64-element
+// groups of the MN dimension `lbo` bytes apart, 8-row groups of the K dimension `sbo` apart.
+EAGLE_DEV uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
   return d;
 }
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, f32 D, both K-major.

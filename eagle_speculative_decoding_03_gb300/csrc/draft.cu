@@ -52,6 +52,7 @@ struct eagle_draft {
   bool tc = false;
   bool use_graph = true, use_pdl = true, gemm_occ2 = false;
   long long wait_limit = 0;   // bounded waits of the GEMMs, clock cycles (0: the default)
+  int kv_keep = 0;            // the whole prefix cache stays in L2 between depths (evict-last hint)
   int D = 0, R = 0, gen = 0, S = 0, n_max = 0, k_max = 0, f_max = 0, max_nodes = 0;
   int rows[EAGLE_MAX_DEPTH], kids[EAGLE_MAX_DEPTH];
   int row_base[EAGLE_MAX_DEPTH + 1], node_base[EAGLE_MAX_DEPTH + 1];
@@ -253,6 +254,9 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
   h->use_graph = !(c.flags & EAGLE_FLAG_NO_GRAPH);
   h->use_pdl = !(c.flags & EAGLE_FLAG_NO_PDL);
   h->gemm_occ2 = (c.flags & EAGLE_FLAG_GEMM_TWO_CTA) != 0;
+  // every depth reads the whole prefix cache again: when all of it fits in a third of L2
+  // (the LM head streams past it with the evict-first hint) it is kept there
+  h->kv_keep = static_cast<double>(c.max_batch) * c.max_prefix * c.n_kv_heads * c.head_dim * 4.0 <= 40e6 ? 1 : 0;
   h->D = c.depth;
   // tree geometry
   int rb = 0, nb = 1, kmax = 0, fmax = 0, nmax_rows = 0;
@@ -749,6 +753,9 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
       a.max_splits = h->max_splits;
       a.out = h->o;
       a.out_hl = h->tc ? h->o_hl : nullptr;
+      a.kv_keep = h->kv_keep;
+      a.wait_limit = h->wait_limit;
+      a.err = h->err;
       ProfScope ps(h, EAGLE_K_ATTN, st);
       if (s == std::min(2, h->D) && fault_injected("launch"))
         return fail(EAGLE_ERR_CUDA, "launch_attention failed: injected by EAGLE_FAULT=launch (depth %d)", s);

@@ -1318,6 +1318,18 @@ bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K, int box_rows)
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_kv_map(CUtensorMap* tm, const void* cache, long long tokens, int Hkv) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !cache || tokens < 1 || Hkv < 1) return false;
+  const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(tokens)};
+  const cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(Hkv) * 256};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_act_map(CUtensorMap* tm, const void* hl, int rows, int K, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;

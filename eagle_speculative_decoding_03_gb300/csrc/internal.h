@@ -38,6 +38,9 @@ cudaError_t allow_max_smem(const void* func, size_t* granted = nullptr);
 size_t max_dyn_smem(const void* func);
 
 bool make_weight_map(CUtensorMap* tm, const void* w, int M, int K, int box_rows = BM);
+// 3-D map over a bf16 prefix cache [tokens][Hkv][128]: boxes of 64 tokens x 64 dims of one
+// KV head, 128-byte swizzle (the attention kernel's key / value tiles).
+bool make_kv_map(CUtensorMap* tm, const void* cache, long long tokens, int Hkv);
 
 // A GEMM over weights [M][K] (rows [0, m_split) from map / pointer 0, the rest from 1),
 // with the caller's split-K scratch, arrival counters and device error word.
@@ -93,6 +96,10 @@ struct AttnArgs {
   int rows_per_group;       // (tensor-core kernel only; 0 / 1 = one group)
   float* out;               // [N][Hq*hd]
   uint16_t* out_hl;         // [2N][Hq*hd] bf16 hi / lo rows of out (operand of the O projection)
+  int kv_keep;              // tensor-core kernel: prefix tiles loaded with the L2 evict-last hint
+                            // (0: evict-first; set when every request's prefix fits in L2 at once)
+  long long wait_limit;     // tensor-core kernel: clock cycles a bounded wait may take (0: ~1 s)
+  unsigned* err;            // tensor-core kernel: device error word (DEVERR_TIMEOUT)
 };
 size_t attn_smem_bytes(int qv, int hd);
 size_t attn_merge_capacity(int qv, int hd);

@@ -506,6 +506,7 @@ eagle_status_t stack_enqueue(Stack* h, const StackRows& in, int k, int* ids, flo
       }
       a.out = h->o;
       a.out_hl = h->o_hl;
+      a.err = h->err;
       VCU(launch_attention(a, st, pdl));
     }
     // O projection + residual (and the MLP's gained operand copy)
