@@ -324,34 +324,35 @@ EAGLE_DEV void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
 // ============================================================ tensor-core path
 // bf16 prefix cache, head size 128, at most 128 query vectors (rows x query heads of the KV
 // group) per CTA.  Same cluster decomposition and merge as the SIMT kernel; per 64-key tile
-// the two products run on the 5th-generation tensor cores (tcgen05.mma, accumulators in
-// tensor memory):
-//   S   [query x key] = Q K^T     A = queries (bf16 hi and lo parts, 128 rows), B = key tile
-//   O^T [dim x query] += V^T P^T  A = value tile (MN-major), B = probabilities (hi and lo)
+// the two products run on the 5th-generation tensor cores (tcgen05.mma) with every operand
+// that the CTA produces itself held in tensor memory:
+//   S [query x key]  = Q K^T   A = queries (TMEM, bf16 hi and lo parts), B = key tile (smem)
+//   O [query x dim] += P V     A = probabilities (TMEM, hi and lo, written over S), B = value
+//                              tile (smem, MN-major)
 // so each product keeps ~16 significant bits of the fp32 operands (the bf16 cache is exact;
-// tree-row keys and values, fp32, are split into hi and lo as well: three products).
-// Prefix tiles arrive by TMA (a 3-D map over [token][kv head][dim]); the last, partial tile
-// of a request is loaded shifted back to end on its last key, so no copy reads past the
-// request (rows before its first new key are masked).  S has two TMEM buffers (the next
-// tile's QK^T overlaps this tile's softmax), O^T stays in TMEM for the whole pass.
+// tree-row keys and values, fp32, are split into hi and lo as well: three products).  Shared
+// memory holds only the key / value ring, filled by TMA through a 3-D map over
+// [token][kv head][dim] (a request's partial last tile is loaded shifted back to end on its
+// last key, so no copy reads past the request; rows before its first new key are masked).
+// S / P has two TMEM buffers, so one tile's QK^T overlaps the previous tile's softmax.
 // Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2-3 tree-tile converters,
-// 4-7 softmax (thread = query vector = TMEM lane of S; = head dimension lane of O^T).  The
-// running max is raised only when a tile exceeds it by more than 2^8 (then the O^T
-// columns are rescaled in TMEM), so probabilities stay below 2^8.
+// 4-7 softmax (thread = query vector = TMEM lane).  The running max is raised only when a
+// tile exceeds it by more than 2^8 (the thread then rescales its row of O in TMEM), so
+// probabilities stay below 2^8.
 constexpr int UA_THREADS = 256;
 constexpr int UA_HD = 128;
-constexpr uint32_t UA_QPART = 32768;     // Q hi or Q lo: 128 rows x 128 dims (two 64-dim blocks)
 constexpr uint32_t UA_KBLK = 8192;       // 64 keys x 64 dims bf16, 128-byte swizzle
 constexpr uint32_t UA_SLOT = 4 * UA_KBLK;   // ring slot: K (dims 0-63, 64-127) | V (same)
-constexpr uint32_t UA_MISC = 2304;       // barriers, flags, rescale factors, merge m / l
+constexpr uint32_t UA_MISC = 1280;       // barriers, flags, merge m / l
 constexpr float UA_RESCALE = 8.0f;       // log2 units
-constexpr int UA_MAX_STAGES = 4;
-constexpr int UA_PREFETCH = 6;           // tiles requested into L2 ahead of their ring slot
+constexpr int UA_MAX_STAGES = 6;
+constexpr int UA_PREFETCH = 4;           // tiles requested into L2 beyond the ring
+constexpr int UA_ST_LD = UA_HD + 4;      // row stride (floats) of the CTA's final state in shared memory
+// TMEM columns: S / P buffers [0, 64), [64, 128); O [128, 256); Q hi [256, 320), Q lo [320, 384)
+constexpr uint32_t UA_T_O = 128, UA_T_QHI = 256, UA_T_QLO = 320, UA_TMEM_COLS = 512;
 
-__host__ __device__ inline uint32_t ua_p_bytes(int qvp) { return static_cast<uint32_t>(qvp) * 128u; }
-__host__ __device__ inline uint32_t ua_ring_off(int qvp) { return 2 * UA_QPART + 4 * ua_p_bytes(qvp); }
-__host__ __device__ inline size_t ua_smem_bytes(int qvp, int stages) {
-  return static_cast<size_t>(ua_ring_off(qvp)) + static_cast<size_t>(stages) * UA_SLOT + UA_MISC + 1024;
+__host__ __device__ inline size_t ua_smem_bytes(int stages) {
+  return static_cast<size_t>(stages) * UA_SLOT + UA_MISC + 1024;
 }
 
 // byte offset of 16-byte chunk c (0-7) of row r in a 128-byte-swizzled block of 128-byte rows
@@ -373,10 +374,9 @@ EAGLE_DEV void st_shared_v4(uint32_t addr, uint4 v) {
 
 __global__ void __launch_bounds__(UA_THREADS, 1)
 tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                         const AttnArgs a, const int qvp, const int NS) {
+                         const AttnArgs a, const int NS) {
   extern __shared__ uint8_t ua_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ua_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sb = smem_u32(sm);
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
@@ -390,20 +390,18 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
   const int row0 = b * a.rows_per_req + rfirst;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const uint32_t pbytes = ua_p_bytes(qvp);
-  const uint32_t q_u = sb, p_u = sb + 2 * UA_QPART, ring_u = sb + ua_ring_off(qvp);
-  uint8_t* misc = sm + ua_ring_off(qvp) + static_cast<uint32_t>(NS) * UA_SLOT;
+  const uint32_t ring_u = smem_u32(sm);
+  uint8_t* misc = sm + static_cast<uint32_t>(NS) * UA_SLOT;
   const uint32_t misc_u = smem_u32(misc);
-  const uint32_t bar_kvf = misc_u, bar_kve = misc_u + 32, bar_sf = misc_u + 64, bar_se = misc_u + 80,
-                 bar_pf = misc_u + 96, bar_pe = misc_u + 112, bar_od = misc_u + 128, bar_tg = misc_u + 136,
-                 bar_tf = misc_u + 144, bar_fin = misc_u + 152;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 160);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 164);
-  int* tree_slot = reinterpret_cast<int*>(misc + 168);
-  float* fac = reinterpret_cast<float*>(misc + 256);   // [2][128] rescale factor per query vector
-  float* mcta = fac + 256;                             // [128] the CTA's final state per vector
+  const uint32_t bar_kvf = misc_u, bar_kve = misc_u + 64, bar_sf = misc_u + 128, bar_pf = misc_u + 144,
+                 bar_pe = misc_u + 160, bar_od = misc_u + 176, bar_tg = misc_u + 184, bar_tf = misc_u + 192,
+                 bar_fin = misc_u + 200;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 208);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 212);
+  int* tree_slot = reinterpret_cast<int*>(misc + 216);
+  float* mcta = reinterpret_cast<float*>(misc + 256);   // [128] the CTA's final state per vector
   float* lcta = mcta + 128;
-  float* st = reinterpret_cast<float*>(sm);            // [qv][128] un-normalised output (Q region, at the end)
+  float* st = reinterpret_cast<float*>(sm);             // [qv][UA_ST_LD] un-normalised output (ring, at the end)
 
   // this CTA's keys: prefix tiles rank, rank + cs, ... and (one CTA) the tree tile
   const int tok0 = __ldg(a.cu_seqlens + b);
@@ -415,13 +413,12 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
   const long long wlim = a.wait_limit > 0 ? a.wait_limit : WAIT_LIMIT_CYCLES;
 
   if (tid == 0) {
-    for (int s = 0; s < UA_MAX_STAGES; ++s) {
+    for (int s = 0; s < 8; ++s) {
       mbar_init(bar_kvf + 8 * s, 1);
       mbar_init(bar_kve + 8 * s, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_sf + 8 * i, 1);
-      mbar_init(bar_se + 8 * i, 4);
       mbar_init(bar_pf + 8 * i, 4);
       mbar_init(bar_pe + 8 * i, 1);
     }
@@ -433,7 +430,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_alloc(smem_u32(tmem_slot), UA_TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -441,16 +438,12 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // The prefix cache is an input of the draft step that none of its kernels write: the
-  // first ring slots are filled before the wait on the previous kernel.
-  const uint64_t pol = a.kv_keep ? policy_evict_last() : policy_evict_first();
   // first token of tile t (a partial tile is shifted back to end on the request's last key)
   auto tile_t0 = [&](int t) {
     const int c = rank + t * cs;
     return tok0 + c * ATT_CHUNK - (ATT_CHUNK - min(ATT_CHUNK, nb - c * ATT_CHUNK));
   };
-  // tiles are also requested into L2 UA_PREFETCH tiles ahead of their ring slot: a slot is
-  // refilled only once the tile that held it is done, so its copy then comes from L2
+  // tiles beyond the ring are also requested into L2, so a slot's refill comes from L2
   auto prefetch = [&](int t) {
     if (t >= np) return;
     const int t0 = tile_t0(t);
@@ -459,6 +452,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
     tma_prefetch_l2_3d(&tmv, 0, kvh, t0);
     tma_prefetch_l2_3d(&tmv, 64, kvh, t0);
   };
+  const uint64_t pol = a.kv_keep ? policy_evict_last() : policy_evict_first();
   auto issue = [&](int t) {
     const int slot = t % NS;
     const int t0 = tile_t0(t);
@@ -469,6 +463,8 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
     tma_load_3d(dst + 2 * UA_KBLK, &tmv, 0, kvh, t0, bar, pol);
     tma_load_3d(dst + 3 * UA_KBLK, &tmv, 64, kvh, t0, bar, pol);
   };
+  // The prefix cache is an input of the draft step that none of its kernels write: the
+  // first ring slots are filled before the wait on the previous kernel.
   const int first = min(NS, np);
   if (warp == 0 && lane == 0 && np > 0) {
     tma_prefetch_desc(&tmk);
@@ -479,33 +475,35 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
   pdl_wait();
   pdl_trigger();
 
-  // queries of this CTA (scaled by log2(e) / sqrt(hd)) -> bf16 hi / lo, 128-byte swizzle;
-  // rows past qv are zero
-  {
+  // queries (scaled by log2(e) / sqrt(hd)) -> bf16 hi / lo parts in TMEM, one lane per
+  // query vector (lanes past qv hold zeros)
+  if (warp >= 4) {
+    const int v = tid - 128;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const float qs = 1.4426950408889634f / sqrtf(static_cast<float>(UA_HD));
-    for (int it = tid; it < 128 * 16; it += UA_THREADS) {
-      const int v = it >> 4, c16 = it & 15;
-      float x[8];
-      if (v < qv) {
-        const int i = v / gq, gh = v - i * gq;
-        const float* src = a.q + (static_cast<size_t>(row0 + i) * a.Hq + kvh * gq + gh) * UA_HD + c16 * 8;
-        const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
-        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-        x[0] = x0.x * qs; x[1] = x0.y * qs; x[2] = x0.z * qs; x[3] = x0.w * qs;
-        x[4] = x1.x * qs; x[5] = x1.y * qs; x[6] = x1.z * qs; x[7] = x1.w * qs;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = 0.f;
-      }
-      uint4 hi, lo;
-      ua_split8(x, hi, lo);
-      const uint32_t off = (c16 >> 3) * (UA_QPART / 2) + ua_sw(v, c16 & 7);
-      st_shared_v4(q_u + off, hi);
-      st_shared_v4(q_u + UA_QPART + off, lo);
+    const float* src = nullptr;
+    if (v < qv) {
+      const int i = v / gq, gh = v - i * gq;
+      src = a.q + (static_cast<size_t>(row0 + i) * a.Hq + kvh * gq + gh) * UA_HD;
     }
+#pragma unroll 1
+    for (int c0 = 0; c0 < UA_HD; c0 += 64) {   // 64 dims = 32 packed columns per part
+      uint32_t hi[32], lo[32];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (src) x = __ldcg(reinterpret_cast<const float4*>(src + c0 + 4 * e));
+        split2_packed(x.x * qs, x.y * qs, hi[2 * e], lo[2 * e]);
+        split2_packed(x.z * qs, x.w * qs, hi[2 * e + 1], lo[2 * e + 1]);
+      }
+      tmem_st32(tmem + lane_base + UA_T_QHI + c0 / 2, hi);
+      tmem_st32(tmem + lane_base + UA_T_QLO + c0 / 2, lo);
+    }
+    tmem_wait_st();
   }
-  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
 
   bool ok = true;
   if (warp == 0) {
@@ -519,8 +517,8 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
           issue(t);
           prefetch(t + UA_PREFETCH);
         } else {
-          tree_slot[t - np] = slot;
-        }   // the tree tile takes two free slots (keys | values)
+          tree_slot[t - np] = slot;   // the tree tile takes two free slots (keys | values)
+        }
       }
       if (has_tree && ok) mbar_arrive(bar_tg);
       if (!ok) {   // let copies already issued land before the CTA releases its shared memory
@@ -533,12 +531,10 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id1 = idesc_bf16_f32(128, 64);
-      const uint32_t id2 = idesc_bf16_f32(128, qvp) | (1u << 15);   // A (values) MN-major
-      const uint32_t tO = tmem + 128;
-      const uint64_t dq_hi = smem_desc_sw128(q_u), dq_lo = smem_desc_sw128(q_u + UA_QPART);
-      const uint64_t dp0 = smem_desc_sw128(p_u);
-      // Step t issues QK^T of tile t (into S buffer t & 1) and P V^T of tile t - 1; the tree
-      // tile (last) takes P V^T first, since its slots may wait for that product's release.
+      const uint32_t id2 = idesc_bf16_f32(128, UA_HD) | (1u << 16);   // B (values) MN-major
+      const uint32_t tO = tmem + UA_T_O;
+      // Step t issues QK^T of tile t (into S buffer t & 1) and P V of tile t - 1; the tree
+      // tile (last) takes P V first, since its slots may wait for that product's release.
       // (One copy of each issue sequence: the issue loop stays small.)
       for (int t = 0; t <= T && ok; ++t) {
         const bool tree_step = t == np && t < T;
@@ -546,10 +542,10 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
         for (int ph = 0; ph < 2 && ok; ++ph) {
           if ((ph == 0) != tree_step) {
             if (t == T) continue;
-            // ---- S = Q K^T for tile t
+            // ---- S = Q K^T for tile t, once P V of tile t - 2 (same TMEM buffer) is done
             ok = tree_step ? mbar_wait(bar_tf, 0, a.err, abort_flag, wlim)
                            : mbar_wait(bar_kvf + 8 * (t % NS), (t / NS) & 1, a.err, abort_flag, wlim);
-            ok = ok && mbar_wait(bar_se + 8 * (t & 1), ((t >> 1) & 1) ^ 1, a.err, abort_flag, wlim);
+            ok = ok && mbar_wait(bar_pe + 8 * (t & 1), ((t >> 1) & 1) ^ 1, a.err, abort_flag, wlim);
             if (!ok) break;
             // (the tree tile's slots are known once the converters signalled)
             const uint32_t kb = tree_step ? ring_u + tree_slot[0] * UA_SLOT : ring_u + (t % NS) * UA_SLOT;
@@ -558,30 +554,29 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
             // descriptors move only in their start-address field (16-byte units, no carry)
             const uint64_t dk = smem_desc_sw128(kb), dkl = dk + ((2 * UA_KBLK) >> 4);
 #pragma unroll
-            for (int j = 0; j < UA_HD / 16; ++j) {
-              const uint32_t qo = ((j >> 2) * (UA_QPART / 2) + (j & 3) * 32) >> 4;
+            for (int j = 0; j < UA_HD / 16; ++j) {   // 16 dims: 8 packed Q columns, 32 bytes of K
               const uint32_t ko = ((j >> 2) * UA_KBLK + (j & 3) * 32) >> 4;
-              tc_mma_bf16(d, dq_hi + qo, dk + ko, id1, j > 0 ? 1u : 0u);
-              tc_mma_bf16(d, dq_lo + qo, dk + ko, id1, 1u);
-              if (tree_step) tc_mma_bf16(d, dq_hi + qo, dkl + ko, id1, 1u);
+              tc_mma_bf16_ta(d, tmem + UA_T_QHI + 8 * j, dk + ko, id1, j > 0 ? 1u : 0u);
+              tc_mma_bf16_ta(d, tmem + UA_T_QLO + 8 * j, dk + ko, id1, 1u);
+              if (tree_step) tc_mma_bf16_ta(d, tmem + UA_T_QHI + 8 * j, dkl + ko, id1, 1u);
             }
             tc_commit(bar_sf + 8 * (t & 1));
           } else {
             if (t == 0) continue;
-            // ---- O^T += V^T P^T for tile u = t - 1
+            // ---- O += P V for tile u = t - 1 (P hi / lo in S buffer u & 1)
             const int u = t - 1;
             const bool tree = u == np;
             ok = mbar_wait(bar_pf + 8 * (u & 1), (u >> 1) & 1, a.err, abort_flag, wlim);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t vhi = tree ? ring_u + tree_slot[1] * UA_SLOT : ring_u + (u % NS) * UA_SLOT + 2 * UA_KBLK;
-            const uint64_t dv = smem_desc_sw128_mn(vhi, UA_KBLK, 1024), dvl = dv + ((2 * UA_KBLK) >> 4);
-            const uint64_t dph = dp0 + (((u & 1) * 2 * pbytes) >> 4), dpl = dph + (pbytes >> 4);
+            const uint32_t vb = tree ? ring_u + tree_slot[1] * UA_SLOT : ring_u + (u % NS) * UA_SLOT + 2 * UA_KBLK;
+            const uint64_t dv = smem_desc_sw128_mn(vb, UA_KBLK, 1024), dvl = dv + ((2 * UA_KBLK) >> 4);
+            const uint32_t tp = tmem + (u & 1) * 64;
 #pragma unroll
-            for (int j = 0; j < ATT_CHUNK / 16; ++j) {   // 16 keys: two 8-key groups of V (1024 bytes), 32 bytes of P
-              tc_mma_bf16(tO, dv + j * 128, dph + 2 * j, id2, (u > 0 || j > 0) ? 1u : 0u);
-              tc_mma_bf16(tO, dv + j * 128, dpl + 2 * j, id2, 1u);
-              if (tree) tc_mma_bf16(tO, dvl + j * 128, dph + 2 * j, id2, 1u);
+            for (int j = 0; j < ATT_CHUNK / 16; ++j) {   // 16 keys: 8 packed P columns, two 8-key V groups
+              tc_mma_bf16_ta(tO, tp + 8 * j, dv + j * 128, id2, (u > 0 || j > 0) ? 1u : 0u);
+              tc_mma_bf16_ta(tO, tp + 32 + 8 * j, dv + j * 128, id2, 1u);
+              if (tree) tc_mma_bf16_ta(tO, tp + 8 * j, dvl + j * 128, id2, 1u);
             }
             tc_commit(bar_pe + 8 * (u & 1));
             if (!tree) tc_commit(bar_kve + 8 * (u % NS));
@@ -641,23 +636,16 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
     const unsigned long long vis_tree =
         mrow & (a.tree_upto >= 64 ? ~0ull : ((1ull << max(a.tree_upto, 0)) - 1ull));
     float m_run = -INFINITY, l_run = 0.f;
-    const uint32_t tO = tmem + lane_base + 128;
+    const uint32_t tO = tmem + lane_base + UA_T_O;
     for (int t = 0; t < T; ++t) {
       const bool tree = t == np;
       ok = ok && mbar_wait_sleepy(bar_sf + 8 * (t & 1), (t >> 1) & 1, a.err, abort_flag, wlim);
       tc_fence_after();
+      const uint32_t ts = tmem + lane_base + (t & 1) * 64;
       float s[ATT_CHUNK];
-      if (ok) {
-        const uint32_t ta = tmem + lane_base + (t & 1) * 64;
-        tmem_ld16(ta, s);
-        tmem_ld16(ta + 16, s + 16);
-        tmem_ld16(ta + 32, s + 32);
-        tmem_ld16(ta + 48, s + 48);
-        tmem_wait_ld();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_se + 8 * (t & 1));
+      tmem_ld32(ts, s);
+      tmem_ld32(ts + 32, s + 32);
+      tmem_wait_ld();
       // visible keys of the tile as a bit mask: prefix rows [lo, 64) (a shifted partial tile
       // starts late), tree rows that exist and are ancestors of (or are) the vector's row
       const unsigned long long vis =
@@ -676,39 +664,37 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
         for (int r = 8; r < ATT_CHUNK; ++r) m8[r & 7] = fmaxf(m8[r & 7], s[r]);
         mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
-      float f = 1.f, m_use = m_run;
+      float f = 1.f;
       bool resc = false;
       if (mt != -INFINITY) {
         if (m_run == -INFINITY) {
-          m_use = mt;
+          m_run = mt;
         } else if (mt > m_run + UA_RESCALE) {
-          m_use = mt;
           f = fast_exp2(m_run - mt);
+          m_run = mt;
           resc = true;
         }
       }
-      fac[(t & 1) * 128 + v] = f;
-      if (named_bar_or(1, 128, resc)) {
-        // some vector's max rose: scale its O^T column once every earlier P V^T is done
-        ok = ok && mbar_wait(bar_od, (t - 1) & 1, a.err, abort_flag, wlim);
+      if (__any_sync(0xffffffffu, resc)) {
+        // this warp's rows whose max rose: scale them in O once every earlier P V is done
+        ok = ok && mbar_wait_sleepy(bar_od, (t - 1) & 1, a.err, abort_flag, wlim);
         tc_fence_after();
-        if (ok) {
-          for (int c0 = 0; c0 < qvp; c0 += 16) {
-            float x[16];
-            tmem_ld16(tO + c0, x);
-            tmem_wait_ld();
+#pragma unroll 1
+        for (int c0 = 0; c0 < UA_HD; c0 += 32) {
+          float x[32];
+          tmem_ld32(tO + c0, x);
+          tmem_wait_ld();
+          uint32_t y[32];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] *= fac[(t & 1) * 128 + c0 + e];
-            tmem_st16(tO + c0, x);
-          }
-          tmem_wait_st();
+          for (int e = 0; e < 32; ++e) y[e] = __float_as_uint(x[e] * f);
+          tmem_st32(tO + c0, y);
         }
+        tmem_wait_st();
       }
-      m_run = m_use;
       l_run *= f;
       // probabilities 2^(s - m) (a masked key gives 2^-inf = 0); rows without a key so far
-      // (and padding rows) write zeros
-      float ps = 0.f;
+      // (and padding rows) give zeros.  P (hi, lo) is written over this tile's S.
+      uint32_t ph[ATT_CHUNK / 2], pl[ATT_CHUNK / 2];
       if (work && m_run != -INFINITY) {
         float p8[8];
 #pragma unroll
@@ -718,40 +704,35 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
           s[r] = fast_exp2(s[r] - m_run);
           p8[r & 7] += s[r];
         }
-        ps = ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
+        l_run += ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
+#pragma unroll
+        for (int e = 0; e < ATT_CHUNK / 2; ++e) split2_packed(s[2 * e], s[2 * e + 1], ph[e], pl[e]);
       } else {
 #pragma unroll
-        for (int r = 0; r < ATT_CHUNK; ++r) s[r] = 0.f;
+        for (int e = 0; e < ATT_CHUNK / 2; ++e) ph[e] = pl[e] = 0u;
       }
-      l_run += ps;
-      // P row v (hi, lo) into buffer t & 1 once the product of tile t - 2 released it
-      ok = ok && mbar_wait_sleepy(bar_pe + 8 * (t & 1), ((t >> 1) & 1) ^ 1, a.err, abort_flag, wlim);
-      if (ok && v < qvp) {
-        const uint32_t phi = p_u + (t & 1) * 2 * pbytes, plo = phi + pbytes;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 hi, lo4;
-          ua_split8(s + 8 * c, hi, lo4);
-          st_shared_v4(phi + ua_sw(v, c), hi);
-          st_shared_v4(plo + ua_sw(v, c), lo4);
-        }
-      }
-      fence_proxy_async_smem();
+      tmem_st32(ts, ph);
+      tmem_st32(ts + 32, pl);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pf + 8 * (t & 1));
     }
-    // the CTA's state: O^T column v -> st[v][.] (thread = head dimension lane), m and l
+    // the CTA's state: row v of O -> st[v][.], its m and l
     ok = mbar_wait_sleepy(bar_fin, 0, a.err, abort_flag, wlim) && ok;
     tc_fence_after();
-    if (ok && T > 0) {
-      for (int c0 = 0; c0 < qvp; c0 += 16) {
-        float x[16];
-        tmem_ld16(tO + c0, x);
+    if (T > 0) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < UA_HD; c0 += 32) {
+        float x[32];
+        tmem_ld32(tO + c0, x);
         tmem_wait_ld();
+        if (live) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (c0 + e < qv) st[static_cast<size_t>(c0 + e) * UA_HD + v] = x[e];
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(st + static_cast<size_t>(v) * UA_ST_LD + c0 + e) =
+                make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+        }
       }
     }
     mcta[v] = (live && T > 0 && ok) ? m_run : -INFINITY;
@@ -774,7 +755,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
       if (r < cs) {
         mr[r] = cluster.map_shared_rank(mcta, r)[v];
         lr[r] = cluster.map_shared_rank(lcta, r)[v];
-        xr[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(st, r) + static_cast<size_t>(v) * UA_HD + 4 * d4);
+        xr[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(st, r) + static_cast<size_t>(v) * UA_ST_LD + 4 * d4);
       }
     }
     float M = -INFINITY;
@@ -809,7 +790,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
     }
   }
   cluster.sync();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, UA_TMEM_COLS);
 }
 
 static int rows_per_cta(const AttnArgs& a) {
@@ -884,12 +865,12 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
                 static_cast<long long>(G - 1) * a.rows_per_group >= a.rows_per_req))
     return cudaErrorInvalidValue;   // groups only on the tensor-core path, each with >= 1 row
   const int qv = rows_per_cta(a) * (a.Hq / a.Hkv);
-  // tensor-core kernel: queries padded to the MMA's N granule; as many ring slots as fit
-  const int qvp = std::max(16, (qv + 15) / 16 * 16);
+  // tensor-core kernel: as many key / value ring slots as fit
   int stages = UA_MAX_STAGES;
-  while (stages > 2 && ua_smem_bytes(qvp, stages) > g_ua_smem_cap) --stages;
-  if (tc && ua_smem_bytes(qvp, stages) > g_ua_smem_cap) return cudaErrorInvalidConfiguration;
-  const size_t smem = tc ? ua_smem_bytes(qvp, stages) : attn_smem_bytes(qv, a.hd);
+  while (stages > 2 && ua_smem_bytes(stages) > g_ua_smem_cap) --stages;
+  // (at least three: the final per-vector state, qv x 132 floats, is parked in the ring)
+  if (tc && (stages < 3 || ua_smem_bytes(stages) > g_ua_smem_cap)) return cudaErrorInvalidConfiguration;
+  const size_t smem = tc ? ua_smem_bytes(stages) : attn_smem_bytes(qv, a.hd);
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
@@ -938,7 +919,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
     const long long tokens = static_cast<long long>(a.B) * a.max_prefix;
     if (tokens > 0 && (!make_kv_map(&tmk, a.k_cache, tokens, a.Hkv) || !make_kv_map(&tmv, a.v_cache, tokens, a.Hkv)))
       return cudaErrorInvalidValue;
-return cudaLaunchKernelEx(&cfg, tree_attention_tc_kernel, tmk, tmv, a, qvp, stages);
+return cudaLaunchKernelEx(&cfg, tree_attention_tc_kernel, tmk, tmv, a, stages);
   }
   return cudaLaunchKernelEx(&cfg, tree_attention_kernel, a);
 }
