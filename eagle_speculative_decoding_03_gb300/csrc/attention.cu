@@ -919,7 +919,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
     const long long tokens = static_cast<long long>(a.B) * a.max_prefix;
     if (tokens > 0 && (!make_kv_map(&tmk, a.k_cache, tokens, a.Hkv) || !make_kv_map(&tmv, a.v_cache, tokens, a.Hkv)))
       return cudaErrorInvalidValue;
-return cudaLaunchKernelEx(&cfg, tree_attention_tc_kernel, tmk, tmv, a, stages);
+    return cudaLaunchKernelEx(&cfg, tree_attention_tc_kernel, tmk, tmv, a, stages);
   }
   return cudaLaunchKernelEx(&cfg, tree_attention_kernel, a);
 }
