@@ -865,11 +865,12 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
                 static_cast<long long>(G - 1) * a.rows_per_group >= a.rows_per_req))
     return cudaErrorInvalidValue;   // groups only on the tensor-core path, each with >= 1 row
   const int qv = rows_per_cta(a) * (a.Hq / a.Hkv);
-  // tensor-core kernel: as many key / value ring slots as fit
+  // tensor-core kernel: as many key / value ring slots as fit, but no more than a CTA's tiles
+  // need (a smaller footprint lets the next kernel's CTAs start beside it)
   int stages = UA_MAX_STAGES;
   while (stages > 2 && ua_smem_bytes(stages) > g_ua_smem_cap) --stages;
-  // (at least three: the final per-vector state, qv x 132 floats, is parked in the ring)
-  if (tc && (stages < 3 || ua_smem_bytes(stages) > g_ua_smem_cap)) return cudaErrorInvalidConfiguration;
+  // (at least four: the final per-vector state, qv x 132 floats, is parked in the ring)
+  if (tc && (stages < 4 || ua_smem_bytes(stages) > g_ua_smem_cap)) return cudaErrorInvalidConfiguration;
   const size_t smem = tc ? ua_smem_bytes(stages) : attn_smem_bytes(qv, a.hd);
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -906,6 +907,12 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
     if (cs >= 1 && cs <= cmax && cs <= a.max_splits && active_clusters(tc, cs, smem) > 0) best_cs = cs;
   }
   if (!best_cs) return cudaErrorInvalidConfiguration;
+  if (tc) {
+    const int per_cta = (a.max_splits + best_cs - 1) / best_cs;   // tiles, the tree tile's two slots included
+    // (at least four: two CTAs of this kernel never share an SM, whose TMEM holds one)
+    stages = std::max(4, std::min(stages, per_cta + 1));
+    cfg.dynamicSmemBytes = ua_smem_bytes(stages);
+  }
   attr[1].val.clusterDim.x = best_cs;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;

@@ -46,6 +46,12 @@ static eagle_status_t fail(eagle_status_t st, const char* fmt, ...) {
                   __FILE__, __LINE__);                                                    \
   } while (0)
 
+// LM-head launches of at least this many rows store the logits and select in a second
+// kernel; fewer rows keep the log-sum-exp and top-k in the GEMM's epilogue.  (The fused
+// epilogue's per-row work grows with the rows of a tile and, past a few dozen rows, outlasts
+// the tile's weight stream.)
+constexpr int LM_LOGITS_MIN_ROWS = 96;
+
 struct eagle_draft {
   eagle_draft_config_t cfg;
   eagle_draft_weights_t w;
@@ -53,6 +59,7 @@ struct eagle_draft {
   bool use_graph = true, use_pdl = true, gemm_occ2 = false;
   long long wait_limit = 0;   // bounded waits of the GEMMs, clock cycles (0: the default)
   int kv_keep = 0;            // the whole prefix cache stays in L2 between depths (evict-last hint)
+  int lm_logits_min_rows = LM_LOGITS_MIN_ROWS;
   int D = 0, R = 0, gen = 0, S = 0, n_max = 0, k_max = 0, f_max = 0, max_nodes = 0;
   int rows[EAGLE_MAX_DEPTH], kids[EAGLE_MAX_DEPTH];
   int row_base[EAGLE_MAX_DEPTH + 1], node_base[EAGLE_MAX_DEPTH + 1];
@@ -126,11 +133,6 @@ static bool fault_injected(const char* what) {
   return f && strcmp(f, what) == 0;
 }
 
-// LM-head launches of at least this many rows store the logits and select in a second
-// kernel; fewer rows keep the log-sum-exp and top-k in the GEMM's epilogue.  (The fused
-// epilogue's per-row work grows with the rows of a tile and, past a few dozen rows, outlasts
-// the tile's weight stream.)
-constexpr int LM_LOGITS_MIN_ROWS = 64;
 
 // --------------------------------------------------------------- validation
 static eagle_status_t validate(const eagle_draft_config_t& c, const eagle_draft_weights_t* w) {
@@ -211,7 +213,7 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   h->lm_val = cv.take<float>(lmn * KMAX);
   h->lm_id = cv.take<int>(lmn * KMAX);
   h->counters = cv.take<int>(16384);
-  h->logits = (h->tc && n >= LM_LOGITS_MIN_ROWS) ? cv.take<float>(static_cast<size_t>(n) * c.vocab) : nullptr;
+  h->logits = (h->tc && n >= h->lm_logits_min_rows) ? cv.take<float>(static_cast<size_t>(n) * c.vocab) : nullptr;
   const size_t nn = static_cast<size_t>(B) * h->max_nodes;
   h->node_tok = cv.take<int>(nn);
   h->node_parent = cv.take<int>(nn);
@@ -256,6 +258,9 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
   h->gemm_occ2 = (c.flags & EAGLE_FLAG_GEMM_TWO_CTA) != 0;
   // every depth reads the whole prefix cache again: when all of it fits in a third of L2
   // (the LM head streams past it with the evict-first hint) it is kept there
+  // tuning override: EAGLE_LM_LOGITS_MIN_ROWS = the row count from which the LM head stores
+  // logits for the select kernel (sweeps of the crossover); unset keeps the default
+  if (const char* ov = getenv("EAGLE_LM_LOGITS_MIN_ROWS")) h->lm_logits_min_rows = std::max(1, atoi(ov));
   h->kv_keep = static_cast<double>(c.max_batch) * c.max_prefix * c.n_kv_heads * c.head_dim * 4.0 <= 40e6 ? 1 : 0;
   h->D = c.depth;
   // tree geometry
@@ -372,7 +377,7 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
       // the LM head (+ a select per launch when it stores logits); up to 256 rows run as one
       // launch of CTA pairs
       const int launches = N <= 2 * MAX_ROWS_PER_BLOCK ? 1 : parts;
-      h->launches += launches - 1 + (N >= LM_LOGITS_MIN_ROWS ? launches : 0);
+      h->launches += launches - 1 + (N >= h->lm_logits_min_rows ? launches : 0);
     }
   *out = h;
   return EAGLE_OK;
@@ -482,7 +487,7 @@ static void set_sampling(EpiArgs& e, const SampleArgs& sa, int row0) {
 }
 
 static bool lm_via_logits(const eagle_draft* h, const uint16_t* a_hl, int N) {
-  return h->logits && a_hl && N >= LM_LOGITS_MIN_ROWS;
+  return h->logits && a_hl && N >= h->lm_logits_min_rows;
 }
 
 static eagle_status_t lm_head(eagle_draft* h, const float* a, const uint16_t* a_hl, int N, int topk,

@@ -215,8 +215,8 @@ EAGLE_DEV void merge_lm_row(const LmPartials& lm, int N, int kp, int n, int kout
 // to the lower token id.
 constexpr int SEL_THREADS = 512;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
-constexpr int SEL_PER = 32;                        // contiguous keys per thread in the passes
-constexpr int SEL_MAX_SPAN = SEL_THREADS * SEL_PER;   // 16384 keys per part (64 KB + padding)
+constexpr int SEL_PER = 16;                        // keys per thread (registers; contiguous in the fallback)
+constexpr int SEL_MAX_SPAN = SEL_THREADS * SEL_PER;   // 8192 keys per part (32 KB + padding)
 constexpr int SEL_CAP = 256;                       // candidates the threshold gather keeps
 
 // order-preserving image of a float: larger float -> larger integer; NaN -> 0 (below all)
@@ -304,7 +304,7 @@ EAGLE_DEV bool block_select_top(uint32_t kb, int k, SelectScratch& sc) {
 // so the threads of a warp read 32 different banks at every step
 EAGLE_DEV int sel_slot(int i) { return i + (i >> 5); }
 
-__global__ void __launch_bounds__(SEL_THREADS)
+__global__ void __launch_bounds__(SEL_THREADS, 2)
 lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, int k,
                  const unsigned long long* seeds, int sample_rows, int sample_depth, int row0,
                  float* out_max, float* out_sum, float* out_val, int* out_id) {
@@ -379,31 +379,36 @@ lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, i
   }
   if (tid == 0) s_cnt = 0;
   __syncthreads();
-  if (tid == 0) {
-    float M = -INFINITY, S = 0.f;
-    int tot = 0;
-    for (int w = 0; w < SEL_WARPS; ++w) {
-      const float mw = red_m[w], sw = red_s[w];
-      const float MM = fmaxf(M, mw);
-      S = (M == -INFINITY ? 0.f : S * expf(M - MM)) + (mw == -INFINITY ? 0.f : sw * expf(mw - MM));
+  if (warp == 0) {   // the part's state and threshold from the warps' (one lane each)
+    float M = lane < SEL_WARPS ? red_m[lane] : -INFINITY, S = lane < SEL_WARPS ? red_s[lane] : 0.f;
+    int tot = lane < SEL_WARPS ? wsum[lane] : 0;
+    const uint32_t xw = lane < SEL_WARPS ? wmax[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, M, o);
+      const float os = __shfl_xor_sync(0xffffffffu, S, o);
+      const float MM = fmaxf(M, om);
+      S = (M == -INFINITY ? 0.f : S * expf(M - MM)) + (om == -INFINITY ? 0.f : os * expf(om - MM));
       M = MM;
-      tot += wsum[w];
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
     }
-    out_max[static_cast<size_t>(n) * parts + part] = M;
-    out_sum[static_cast<size_t>(n) * parts + part] = S;
     const int ks = min(k, tot);   // keys to select (0 when every key is NaN)
-    s_krem = ks;
     // theta = the ks-th largest warp maximum (ties by warp) is at most the ks-th largest key
     // (ks warps hold a key >= theta), so every key of the top ks is >= theta
-    uint32_t th = 0u;
-    if (ks > 0) {
-      for (int w = 0; w < SEL_WARPS; ++w) {
-        int rk = 0;
-        for (int w2 = 0; w2 < SEL_WARPS; ++w2) rk += wmax[w2] > wmax[w] || (wmax[w2] == wmax[w] && w2 < w);
-        if (rk == ks - 1) th = wmax[w];
-      }
+    int rk = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < SEL_WARPS; ++w2) {
+      const uint32_t x2 = __shfl_sync(0xffffffffu, xw, w2);
+      rk += x2 > xw || (x2 == xw && w2 < lane);
     }
-    s_theta = th;
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < SEL_WARPS && ks > 0 && rk == ks - 1);
+    const uint32_t th = hit ? __shfl_sync(0xffffffffu, xw, __ffs(hit) - 1) : 0u;
+    if (lane == 0) {
+      out_max[static_cast<size_t>(n) * parts + part] = M;
+      out_sum[static_cast<size_t>(n) * parts + part] = S;
+      s_krem = ks;
+      s_theta = th;
+    }
   }
   __syncthreads();
   const int ksel = s_krem;
