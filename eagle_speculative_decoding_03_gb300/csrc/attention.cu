@@ -335,8 +335,10 @@ EAGLE_DEV void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
 // [token][kv head][dim] (a request's partial last tile is loaded shifted back to end on its
 // last key, so no copy reads past the request; rows before its first new key are masked).
 // S / P has two TMEM buffers, so one tile's QK^T overlaps the previous tile's softmax.
-// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2-3 tree-tile converters,
-// 4-7 softmax (thread = query vector = TMEM lane).  The running max is raised only when a
+// Warp roles: 0 TMA producer; 1 TMEM owner; 4 + q softmax for TMEM lane quadrant q (thread
+// = query vector = TMEM lane), for the quadrants that hold query vectors; the MMA issuer on
+// warp 3 (warp 1 when all four quadrants are in use); the other two of warps 1-3 convert
+// the tree tile.  The running max is raised only when a
 // tile exceeds it by more than 2^8 (the thread then rescales its row of O in TMEM), so
 // probabilities stay below 2^8.
 constexpr int UA_THREADS = 256;
@@ -411,6 +413,12 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
   const bool has_tree = npre % cs == rank;
   const int T = np + (has_tree ? 1 : 0);
   const long long wlim = a.wait_limit > 0 ? a.wait_limit : WAIT_LIMIT_CYCLES;
+  // Softmax warps: one per TMEM lane quadrant that holds query vectors (warp 4 + q reads
+  // quadrant q).  With three or fewer, the MMA issuer takes warp 3, whose SM sub-partition
+  // then runs no softmax warp: the issue loop keeps its sub-partition's instruction cache
+  // and issue slots to itself.
+  const int nq = min(4, max(1, (qv + 31) / 32));
+  const int mma_warp = nq <= 3 ? 3 : 1;
 
   if (tid == 0) {
     for (int s = 0; s < 8; ++s) {
@@ -419,7 +427,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_sf + 8 * i, 1);
-      mbar_init(bar_pf + 8 * i, 4);
+      mbar_init(bar_pf + 8 * i, nq);
       mbar_init(bar_pe + 8 * i, 1);
     }
     mbar_init(bar_od, 1);
@@ -477,7 +485,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
 
   // queries (scaled by log2(e) / sqrt(hd)) -> bf16 hi / lo parts in TMEM, one lane per
   // query vector (lanes past qv hold zeros)
-  if (warp >= 4) {
+  if (warp >= 4 && warp - 4 < nq) {
     const int v = tid - 128;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const float qs = 1.4426950408889634f / sqrtf(static_cast<float>(UA_HD));
@@ -527,7 +535,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == mma_warp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id1 = idesc_bf16_f32(128, 64);
@@ -593,8 +601,9 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
     }
   } else if (warp < 4) {
     // ------------------------------ tree tile: fp32 keys / values -> bf16 hi / lo tiles
+    // (the two of warps 1-3 that do not issue MMAs)
     if (has_tree) {
-      const int ct = tid - 64;
+      const int ct = (warp - 1 - (warp > mma_warp ? 1 : 0)) * 32 + lane;
       if (mbar_wait_sleepy(bar_tg, 0, a.err, abort_flag, wlim)) {
         const uint32_t ks = ring_u + tree_slot[0] * UA_SLOT, vs = ring_u + tree_slot[1] * UA_SLOT;
         for (int it = ct; it < ATT_CHUNK * 16; it += 64) {
@@ -626,7 +635,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_tf);
     }
-  } else {
+  } else if (warp - 4 < nq) {
     // ------------------------------------------------------------ softmax
     const int v = tid - 128;                       // query vector = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
