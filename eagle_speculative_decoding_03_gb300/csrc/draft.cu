@@ -47,10 +47,11 @@ static eagle_status_t fail(eagle_status_t st, const char* fmt, ...) {
   } while (0)
 
 // LM-head launches of at least this many rows store the logits and select in a second
-// kernel; fewer rows keep the log-sum-exp and top-k in the GEMM's epilogue.  (The fused
-// epilogue's per-row work grows with the rows of a tile and, past a few dozen rows, outlasts
-// the tile's weight stream.)
-constexpr int LM_LOGITS_MIN_ROWS = 96;
+// kernel; fewer rows (one 16-row chunk) keep the log-sum-exp and top-k in the GEMM's
+// epilogue.  (The fused epilogue's per-row work grows with the rows of a tile; from the
+// second chunk on, its tail after the last weight tile costs more than writing and
+// re-reading the logits.)
+constexpr int LM_LOGITS_MIN_ROWS = 17;
 
 struct eagle_draft {
   eagle_draft_config_t cfg;

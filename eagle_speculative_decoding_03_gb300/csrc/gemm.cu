@@ -1063,7 +1063,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
     if (g.e.nss) epi_rstd(g.e, g.N, es.rstd, tl);
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int rows_total = nrb * npad;
-    long long uc = 0;
+    const size_t pbytes = static_cast<size_t>(rows_total) * BM * sizeof(float);   // one partial tile
+    long long uc = 0, done = 0;
     bool ok = true;
     for (int sg = 0; ok; ++sg) {
       long long s0, s1;
@@ -1077,6 +1078,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
         if (!ok) break;
         tc_fence_after();
         const bool complete = kb0 == 0 && kb1 == KB;
+        const bool final_unit = (done += kb1 - kb0) == u1 - u0;   // this CTA's MMAs end with it
         const int slot = (mt == u0 / KB) ? 0 : 1;   // the CTA's first tile or its last
         float* mypart = g.part + (static_cast<size_t>(cta) * 2 + slot) * rows_total * BM;
         for (int rb = 0; rb < nrb; ++rb) {
@@ -1116,7 +1118,50 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ 
             *last_flag = (old == cl - cf);
           }
           named_bar(1, 128);
-          if (*last_flag) {
+          const int P = cl - cf + 1;
+          // After the CTA's last unit its stage ring is idle (every MMA has completed and no
+          // load is left): with more than one 16-row chunk the tile's partials come in by
+          // bulk copy, one transfer in place of a round trip per chunk (operand-by-TMA
+          // launches, whose source-row barriers are otherwise unused).  (With one chunk the
+          // direct loads are the shorter path.)
+          const bool staged = *last_flag && final_unit && g.b_tma && rows_total > 16 &&
+                              static_cast<size_t>(P) * pbytes <= static_cast<size_t>(g.stages) * L.stage_bytes;
+          if (staged) {
+            __threadfence();
+            if (tl == 0) {
+              g.counters[mt] = 0;
+              asm volatile("fence.proxy.async.global;" ::: "memory");   // the partials: generic writes
+              mbar_arrive_expect_tx(bar_bfull, static_cast<uint32_t>(P * pbytes));
+              for (int c = cf; c <= cl; ++c) {
+                const int sl = (sc.begin(c) / KB == mt) ? 0 : 1;
+                bulk_copy_g2s(sbase + static_cast<uint32_t>((c - cf) * pbytes),
+                              g.part + (static_cast<size_t>(c) * 2 + sl) * rows_total * BM,
+                              static_cast<uint32_t>(pbytes), bar_bfull);
+              }
+            }
+            ok = epi_all(mbar_wait(bar_bfull, 0, g.err, abort_flag, wlim));
+            if (!ok) {   // let the copies land before the CTA releases its shared memory
+              const long long t0 = clock64();
+              while (clock64() - t0 < 4000000) {
+              }
+            }
+            const float* sp = reinterpret_cast<const float*>(smem);
+            for (int rb = 0; rb < nrb && ok; ++rb) {
+              for (int c0 = 0; c0 < npad; c0 += 16) {
+                const int n0 = rb * npad + c0;
+                if (n0 >= g.N) break;
+                float v[16];
+  #pragma unroll
+                for (int r = 0; r < 16; ++r) v[r] = 0.f;
+                for (int pp = 0; pp < P; ++pp) {   // partials summed in CTA order
+                  const float* q0 = sp + (static_cast<size_t>(pp) * rows_total + n0) * BM + tl;
+  #pragma unroll
+                  for (int r = 0; r < 16; ++r) v[r] += q0[static_cast<size_t>(r) * BM];
+                }
+                epilogue_chunk(g, es, mt, n0, v, tl);
+              }
+            }
+          } else if (*last_flag) {
             __threadfence();
             if (tl == 0) g.counters[mt] = 0;
             for (int rb = 0; rb < nrb; ++rb) {

@@ -32,6 +32,18 @@ def test_tree_parity_small(lib, name):
     assert rep["ok"], rep["errors"]
 
 
+@pytest.mark.parametrize("name", ["small_max", "small_wide"])
+def test_tree_parity_fused_lm_epilogue_many_rows(lib, name, monkeypatch):
+    # depths of 24 to 96 rows normally store the logits for the select kernel; with the
+    # crossover raised the LM head keeps its multi-chunk log-sum-exp + top-k epilogue
+    monkeypatch.setenv("EAGLE_LM_LOGITS_MIN_ROWS", "100000")
+    cfg = configs.get(name)
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    d, out, tr = run_tree(cfg, W, I)
+    rep = parity.compare(synth.oracle_cfg(cfg), W, I, out, tr, d.info["slots"])
+    assert rep["ok"], rep["errors"]
+
+
 @pytest.mark.parametrize("name", ["small_dyn", "small_static", "small_fused"])
 def test_graph_replay_matches_direct_launch(lib, name):
     cfg = configs.get(name)
