@@ -323,7 +323,8 @@ EAGLE_DEV void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
 
 // ============================================================ tensor-core path
 // bf16 prefix cache, head size 128, at most 128 query vectors (rows x query heads of the KV
-// group) per CTA.  Same cluster decomposition and merge as the SIMT kernel; per 64-key tile
+// group) per CTA.  The cluster decomposition and merge of the SIMT kernel over 128-key
+// tiles (the tree rows: one tile, zero-padded past 64 rows); per tile
 // the two products run on the 5th-generation tensor cores (tcgen05.mma) with every operand
 // that the CTA produces itself held in tensor memory:
 //   S [query x key]  = Q K^T   A = queries (TMEM, bf16 hi and lo parts), B = key tile (smem)
@@ -335,6 +336,8 @@ EAGLE_DEV void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
 // [token][kv head][dim] (a request's partial last tile is loaded shifted back to end on its
 // last key, so no copy reads past the request; rows before its first new key are masked).
 // S / P has two TMEM buffers, so one tile's QK^T overlaps the previous tile's softmax.
+// (128 keys per tile: one QK^T instruction covers 128 keys, so a tile costs half the
+// instructions per key of a 64-key tile and half the barrier round trips.)
 // Warp roles: 0 TMA producer; 1 TMEM owner; 4 + q softmax for TMEM lane quadrant q (thread
 // = query vector = TMEM lane), for the quadrants that hold query vectors; the MMA issuer on
 // warp 3 (warp 1 when all four quadrants are in use); the other two of warps 1-3 convert
@@ -343,18 +346,19 @@ EAGLE_DEV void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
 // probabilities stay below 2^8.
 constexpr int UA_THREADS = 256;
 constexpr int UA_HD = 128;
-constexpr uint32_t UA_KBLK = 8192;       // 64 keys x 64 dims bf16, 128-byte swizzle
-constexpr uint32_t UA_SLOT = 4 * UA_KBLK;   // ring slot: K (dims 0-63, 64-127) | V (same)
 constexpr uint32_t UA_MISC = 1280;       // barriers, flags, merge m / l
 constexpr float UA_RESCALE = 8.0f;       // log2 units
-constexpr int UA_MAX_STAGES = 6;
-constexpr int UA_PREFETCH = 4;           // tiles requested into L2 beyond the ring
 constexpr int UA_ST_LD = UA_HD + 4;      // row stride (floats) of the CTA's final state in shared memory
-// TMEM columns: S / P buffers [0, 64), [64, 128); O [128, 256); Q hi [256, 320), Q lo [320, 384)
-constexpr uint32_t UA_T_O = 128, UA_T_QHI = 256, UA_T_QLO = 320, UA_TMEM_COLS = 512;
-
-__host__ __device__ inline size_t ua_smem_bytes(int stages) {
-  return static_cast<size_t>(stages) * UA_SLOT + UA_MISC + 1024;
+constexpr uint32_t UA_TMEM_COLS = 512;
+// Per tile size CH (64 or 128 keys): a 64-dim half of a key or value tile is CH rows of
+// 128 bytes (128-byte swizzle); a ring slot holds K (dims 0-63, 64-127) | V (same).
+// TMEM columns: S / P buffers [0, CH), [CH, 2 CH); O [2 CH, 2 CH + 128); Q hi, Q lo: 64
+// columns each after O (CH = 128 fills all 512).
+__host__ __device__ constexpr uint32_t ua_kblk(int ch) { return static_cast<uint32_t>(ch) * 128u; }
+__host__ __device__ constexpr uint32_t ua_slot(int ch) { return 4u * ua_kblk(ch); }
+__host__ __device__ constexpr int ua_max_stages(int ch) { return ch == 64 ? 6 : 3; }
+__host__ __device__ inline size_t ua_smem_bytes(int ch, int stages) {
+  return static_cast<size_t>(stages) * ua_slot(ch) + UA_MISC + 1024;
 }
 
 // byte offset of 16-byte chunk c (0-7) of row r in a 128-byte-swizzled block of 128-byte rows
@@ -374,9 +378,13 @@ EAGLE_DEV void st_shared_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+template <int CH>
 __global__ void __launch_bounds__(UA_THREADS, 1)
 tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const AttnArgs a, const int NS) {
+  constexpr uint32_t UA_KBLK = ua_kblk(CH), UA_SLOT = ua_slot(CH);
+  constexpr uint32_t UA_T_O = 2 * CH, UA_T_QHI = UA_T_O + 128, UA_T_QLO = UA_T_O + 192;
+  constexpr int UA_PREFETCH = 256 / CH;   // tiles requested into L2 beyond the ring
   extern __shared__ uint8_t ua_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ua_raw) + 1023) & ~uintptr_t(1023));
   cg::cluster_group cluster = cg::this_cluster();
@@ -408,7 +416,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
   // this CTA's keys: prefix tiles rank, rank + cs, ... and (one CTA) the tree tile
   const int tok0 = __ldg(a.cu_seqlens + b);
   const int nb = min(max(__ldg(a.cu_seqlens + b + 1) - tok0, 0), a.max_prefix);
-  const int npre = (nb + ATT_CHUNK - 1) / ATT_CHUNK;
+  const int npre = (nb + CH - 1) / CH;
   const int np = rank < npre ? (npre - 1 - rank) / cs + 1 : 0;
   const bool has_tree = npre % cs == rank;
   const int T = np + (has_tree ? 1 : 0);
@@ -449,16 +457,20 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
   // first token of tile t (a partial tile is shifted back to end on the request's last key)
   auto tile_t0 = [&](int t) {
     const int c = rank + t * cs;
-    return tok0 + c * ATT_CHUNK - (ATT_CHUNK - min(ATT_CHUNK, nb - c * ATT_CHUNK));
+    return tok0 + c * CH - (CH - min(CH, nb - c * CH));
   };
   // tiles beyond the ring are also requested into L2, so a slot's refill comes from L2
+  // (the maps' boxes are 64 tokens: two per 64-dim half)
   auto prefetch = [&](int t) {
     if (t >= np) return;
     const int t0 = tile_t0(t);
-    tma_prefetch_l2_3d(&tmk, 0, kvh, t0);
-    tma_prefetch_l2_3d(&tmk, 64, kvh, t0);
-    tma_prefetch_l2_3d(&tmv, 0, kvh, t0);
-    tma_prefetch_l2_3d(&tmv, 64, kvh, t0);
+#pragma unroll
+    for (int h = 0; h < CH; h += 64) {
+      tma_prefetch_l2_3d(&tmk, 0, kvh, t0 + h);
+      tma_prefetch_l2_3d(&tmk, 64, kvh, t0 + h);
+      tma_prefetch_l2_3d(&tmv, 0, kvh, t0 + h);
+      tma_prefetch_l2_3d(&tmv, 64, kvh, t0 + h);
+    }
   };
   const uint64_t pol = a.kv_keep ? policy_evict_last() : policy_evict_first();
   auto issue = [&](int t) {
@@ -466,10 +478,16 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
     const int t0 = tile_t0(t);
     const uint32_t dst = ring_u + slot * UA_SLOT, bar = bar_kvf + 8 * slot;
     mbar_arrive_expect_tx(bar, UA_SLOT);
-    tma_load_3d(dst, &tmk, 0, kvh, t0, bar, pol);
-    tma_load_3d(dst + UA_KBLK, &tmk, 64, kvh, t0, bar, pol);
-    tma_load_3d(dst + 2 * UA_KBLK, &tmv, 0, kvh, t0, bar, pol);
-    tma_load_3d(dst + 3 * UA_KBLK, &tmv, 64, kvh, t0, bar, pol);
+    // 64 tokens of 128-byte rows per box: the second box continues the first's 8-row
+    // swizzle groups, so each 64-dim half is one 128-row K-major block
+#pragma unroll
+    for (int h = 0; h < CH; h += 64) {
+      const uint32_t o = static_cast<uint32_t>(h) * 128u;
+      tma_load_3d(dst + o, &tmk, 0, kvh, t0 + h, bar, pol);
+      tma_load_3d(dst + UA_KBLK + o, &tmk, 64, kvh, t0 + h, bar, pol);
+      tma_load_3d(dst + 2 * UA_KBLK + o, &tmv, 0, kvh, t0 + h, bar, pol);
+      tma_load_3d(dst + 3 * UA_KBLK + o, &tmv, 64, kvh, t0 + h, bar, pol);
+    }
   };
   // The prefix cache is an input of the draft step that none of its kernels write: the
   // first ring slots are filled before the wait on the previous kernel.
@@ -538,7 +556,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
   } else if (warp == mma_warp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id1 = idesc_bf16_f32(128, 64);
+      const uint32_t id1 = idesc_bf16_f32(128, CH);
       const uint32_t id2 = idesc_bf16_f32(128, UA_HD) | (1u << 16);   // B (values) MN-major
       const uint32_t tO = tmem + UA_T_O;
       // Step t issues QK^T of tile t (into S buffer t & 1) and P V of tile t - 1; the tree
@@ -558,7 +576,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
             // (the tree tile's slots are known once the converters signalled)
             const uint32_t kb = tree_step ? ring_u + tree_slot[0] * UA_SLOT : ring_u + (t % NS) * UA_SLOT;
             tc_fence_after();
-            const uint32_t d = tmem + (t & 1) * 64;
+            const uint32_t d = tmem + (t & 1) * CH;
             // descriptors move only in their start-address field (16-byte units, no carry)
             const uint64_t dk = smem_desc_sw128(kb), dkl = dk + ((2 * UA_KBLK) >> 4);
 #pragma unroll
@@ -579,12 +597,14 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
             tc_fence_after();
             const uint32_t vb = tree ? ring_u + tree_slot[1] * UA_SLOT : ring_u + (u % NS) * UA_SLOT + 2 * UA_KBLK;
             const uint64_t dv = smem_desc_sw128_mn(vb, UA_KBLK, 1024), dvl = dv + ((2 * UA_KBLK) >> 4);
-            const uint32_t tp = tmem + (u & 1) * 64;
+            const uint32_t tp = tmem + (u & 1) * CH;
 #pragma unroll
-            for (int j = 0; j < ATT_CHUNK / 16; ++j) {   // 16 keys: 8 packed P columns, two 8-key V groups
-              tc_mma_bf16_ta(tO, tp + 8 * j, dv + j * 128, id2, (u > 0 || j > 0) ? 1u : 0u);
-              tc_mma_bf16_ta(tO, tp + 32 + 8 * j, dv + j * 128, id2, 1u);
-              if (tree) tc_mma_bf16_ta(tO, tp + 8 * j, dvl + j * 128, id2, 1u);
+            for (int j = 0; j < CH / 16; ++j) {   // 16 keys: 8 packed P columns, two 8-key V groups
+              // P of keys [32 c, 32 c + 32) sits at columns 32 c (hi, 16) and 32 c + 16 (lo, 16)
+              const uint32_t pa = tp + 32 * (j >> 1) + 8 * (j & 1);
+              tc_mma_bf16_ta(tO, pa, dv + j * 128, id2, (u > 0 || j > 0) ? 1u : 0u);
+              tc_mma_bf16_ta(tO, pa + 16, dv + j * 128, id2, 1u);
+              if (tree) tc_mma_bf16_ta(tO, pa, dvl + j * 128, id2, 1u);
             }
             tc_commit(bar_pe + 8 * (u & 1));
             if (!tree) tc_commit(bar_kve + 8 * (u % NS));
@@ -606,7 +626,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
       const int ct = (warp - 1 - (warp > mma_warp ? 1 : 0)) * 32 + lane;
       if (mbar_wait_sleepy(bar_tg, 0, a.err, abort_flag, wlim)) {
         const uint32_t ks = ring_u + tree_slot[0] * UA_SLOT, vs = ring_u + tree_slot[1] * UA_SLOT;
-        for (int it = ct; it < ATT_CHUNK * 16; it += 64) {
+        for (int it = ct; it < CH * 16; it += 64) {   // rows past the tree rows: zeros
           const int j = it >> 4, c16 = it & 15;
           float k8[8], v8[8];
           if (j < a.tree_upto) {
@@ -650,19 +670,28 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
       const bool tree = t == np;
       ok = ok && mbar_wait_sleepy(bar_sf + 8 * (t & 1), (t >> 1) & 1, a.err, abort_flag, wlim);
       tc_fence_after();
-      const uint32_t ts = tmem + lane_base + (t & 1) * 64;
-      float s[ATT_CHUNK];
-      tmem_ld32(ts, s);
-      tmem_ld32(ts + 32, s + 32);
-      tmem_wait_ld();
-      // visible keys of the tile as a bit mask: prefix rows [lo, 64) (a shifted partial tile
-      // starts late), tree rows that exist and are ancestors of (or are) the vector's row
-      const unsigned long long vis =
-          tree ? vis_tree : (~0ull << (ATT_CHUNK - min(ATT_CHUNK, nb - (rank + t * cs) * ATT_CHUNK)));
-      const bool work = live && ok;
-      if (work && vis != ~0ull) {
+      const uint32_t ts = tmem + lane_base + (t & 1) * CH;
+      float s[CH];
 #pragma unroll
-        for (int r = 0; r < ATT_CHUNK; ++r) s[r] = ((vis >> r) & 1ull) ? s[r] : -INFINITY;
+      for (int c = 0; c < CH; c += 32) tmem_ld32(ts + c, s + c);
+      tmem_wait_ld();
+      // visible keys of the tile as 64-bit masks (two for 128 keys): prefix rows [lead, CH)
+      // (a shifted partial tile starts late); the tree tile: rows that exist and are
+      // ancestors of (or are) the vector's row, all in the first 64
+      unsigned long long vis0 = vis_tree, vis1 = CH > 64 ? 0ull : ~0ull;
+      if (!tree) {
+        const int lead = CH - min(CH, nb - (rank + t * cs) * CH);
+        vis0 = lead >= 64 ? 0ull : (~0ull << lead);
+        vis1 = (CH == 64 || lead <= 64) ? ~0ull : (~0ull << (lead - 64));
+      }
+      const bool work = live && ok;
+      if (work && (vis0 & vis1) != ~0ull) {
+#pragma unroll
+        for (int r = 0; r < 64; ++r) s[r] = ((vis0 >> r) & 1ull) ? s[r] : -INFINITY;
+        if constexpr (CH > 64) {
+#pragma unroll
+          for (int r = 0; r < 64; ++r) s[64 + r] = ((vis1 >> r) & 1ull) ? s[64 + r] : -INFINITY;
+        }
       }
       float mt = -INFINITY;
       if (work) {
@@ -670,7 +699,7 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
 #pragma unroll
         for (int e = 0; e < 8; ++e) m8[e] = s[e];
 #pragma unroll
-        for (int r = 8; r < ATT_CHUNK; ++r) m8[r & 7] = fmaxf(m8[r & 7], s[r]);
+        for (int r = 8; r < CH; ++r) m8[r & 7] = fmaxf(m8[r & 7], s[r]);
         mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
       float f = 1.f;
@@ -702,26 +731,30 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
       }
       l_run *= f;
       // probabilities 2^(s - m) (a masked key gives 2^-inf = 0); rows without a key so far
-      // (and padding rows) give zeros.  P (hi, lo) is written over this tile's S.
-      uint32_t ph[ATT_CHUNK / 2], pl[ATT_CHUNK / 2];
-      if (work && m_run != -INFINITY) {
-        float p8[8];
+      // (and padding rows) give zeros.  P (hi, lo) is written over this tile's S: keys
+      // [32 c, 32 c + 32) as 16 packed hi columns at 32 c and 16 lo columns at 32 c + 16
+      // (each group's S is in registers before its columns are overwritten).
+      const bool pw = work && m_run != -INFINITY;
+      float p8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) p8[e] = 0.f;
+      for (int e = 0; e < 8; ++e) p8[e] = 0.f;
 #pragma unroll
-        for (int r = 0; r < ATT_CHUNK; ++r) {
-          s[r] = fast_exp2(s[r] - m_run);
-          p8[r & 7] += s[r];
+      for (int c = 0; c < CH; c += 32) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float x0 = 0.f, x1 = 0.f;
+          if (pw) {
+            x0 = fast_exp2(s[c + 2 * e] - m_run);
+            x1 = fast_exp2(s[c + 2 * e + 1] - m_run);
+            p8[(2 * e) & 7] += x0;
+            p8[(2 * e + 1) & 7] += x1;
+          }
+          split2_packed(x0, x1, pk[e], pk[16 + e]);
         }
-        l_run += ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
-#pragma unroll
-        for (int e = 0; e < ATT_CHUNK / 2; ++e) split2_packed(s[2 * e], s[2 * e + 1], ph[e], pl[e]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < ATT_CHUNK / 2; ++e) ph[e] = pl[e] = 0u;
+        tmem_st32(ts + c, pk);
       }
-      tmem_st32(ts, ph);
-      tmem_st32(ts + 32, pl);
+      l_run += ((p8[0] + p8[1]) + (p8[2] + p8[3])) + ((p8[4] + p8[5]) + (p8[6] + p8[7]));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -819,14 +852,18 @@ static size_t g_ua_smem_cap = 0;
 cudaError_t attn_setup_attributes() {
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(tree_attention_kernel));
   if (e != cudaSuccess) return e;
-  e = allow_max_smem(reinterpret_cast<const void*>(tree_attention_tc_kernel), &g_ua_smem_cap);
+  e = allow_max_smem(reinterpret_cast<const void*>(tree_attention_tc_kernel<64>), &g_ua_smem_cap);
+  if (e != cudaSuccess) return e;
+  e = allow_max_smem(reinterpret_cast<const void*>(tree_attention_tc_kernel<128>));
   if (e != cudaSuccess) return e;
   if (!g_att_cluster) {
     // 16-CTA clusters when the device schedules them, else the portable 8
     g_att_cluster = 8;
     if (cudaFuncSetAttribute(tree_attention_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
             cudaSuccess &&
-        cudaFuncSetAttribute(tree_attention_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaFuncSetAttribute(tree_attention_tc_kernel<64>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(tree_attention_tc_kernel<128>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
             cudaSuccess)
       g_att_cluster = ATT_MAX_CLUSTER;
     cudaGetLastError();
@@ -834,8 +871,9 @@ cudaError_t attn_setup_attributes() {
   return cudaSuccess;
 }
 
-// clusters of `cs` CTAs the device holds at once (cached per kernel, size and smem)
-static int active_clusters(bool tc, int cs, size_t smem) {
+// clusters of `cs` CTAs the device holds at once (cached per kernel, size and smem);
+// tc = 0: the SIMT kernel, else the tensor-core kernel of tc-key tiles
+static int active_clusters(int tc, int cs, size_t smem) {
   struct Entry { int dev, tc, cs; size_t smem; int n; };
   static Entry cache[128];
   static int used = 0;
@@ -857,13 +895,14 @@ static int active_clusters(bool tc, int cs, size_t smem) {
   cfg.gridDim = dim3(cs, 1, 1);
   cfg.dynamicSmemBytes = smem;
   int n = 0;
-  const cudaError_t e = tc ? cudaOccupancyMaxActiveClusters(&n, tree_attention_tc_kernel, &cfg)
-                           : cudaOccupancyMaxActiveClusters(&n, tree_attention_kernel, &cfg);
+  const cudaError_t e = tc == 128  ? cudaOccupancyMaxActiveClusters(&n, tree_attention_tc_kernel<128>, &cfg)
+                       : tc == 64 ? cudaOccupancyMaxActiveClusters(&n, tree_attention_tc_kernel<64>, &cfg)
+                                  : cudaOccupancyMaxActiveClusters(&n, tree_attention_kernel, &cfg);
   if (e != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
-  if (used < 128) cache[used++] = Entry{dev, tc ? 1 : 0, cs, smem, n};
+  if (used < 128) cache[used++] = Entry{dev, tc, cs, smem, n};
   return n;
 }
 
@@ -874,13 +913,32 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
                 static_cast<long long>(G - 1) * a.rows_per_group >= a.rows_per_req))
     return cudaErrorInvalidValue;   // groups only on the tensor-core path, each with >= 1 row
   const int qv = rows_per_cta(a) * (a.Hq / a.Hkv);
-  // tensor-core kernel: as many key / value ring slots as fit, but no more than a CTA's tiles
-  // need (a smaller footprint lets the next kernel's CTAs start beside it)
-  int stages = UA_MAX_STAGES;
-  while (stages > 2 && ua_smem_bytes(stages) > g_ua_smem_cap) --stages;
-  // (at least four: the final per-vector state, qv x 132 floats, is parked in the ring)
-  if (tc && (stages < 4 || ua_smem_bytes(stages) > g_ua_smem_cap)) return cudaErrorInvalidConfiguration;
-  const size_t smem = tc ? ua_smem_bytes(stages) : attn_smem_bytes(qv, a.hd);
+  // Cluster size: each CTA of a cluster of cs takes ceil(tiles / cs) tiles, and the
+  // (request, kv head) clusters run in waves of as many as the device holds at once.
+  // Estimated time ~ waves x (tiles per CTA + fixed cost of a CTA, ~4 tiles).  max_splits
+  // counts 64-key tiles, the tree tile included.
+  auto plan = [&](int kind, int tiles, size_t smem, long long& cost) {
+    const int total = a.Hkv * a.B * G;
+    const int cmax = g_att_cluster ? g_att_cluster : 8;
+    int best = 0;
+    for (int cs = 1; cs <= cmax && cs <= tiles; ++cs) {
+      const int nca = active_clusters(kind, cs, smem);
+      if (nca <= 0) continue;
+      const long long waves = (total + nca - 1) / nca;
+      const long long c = waves * ((tiles + cs - 1) / cs + 4);
+      if (!best || c < cost || (c == cost && cs > best)) {
+        best = cs;
+        cost = c;
+      }
+    }
+    // tuning override: EAGLE_ATTN_CLUSTER = a cluster size to use when the device holds such
+    // clusters (sweeps of the launch shape); unset or 0 keeps the cost model's choice
+    if (const char* ov = getenv("EAGLE_ATTN_CLUSTER")) {
+      const int cs = atoi(ov);
+      if (cs >= 1 && cs <= cmax && cs <= tiles && active_clusters(kind, cs, smem) > 0) best = cs;
+    }
+    return best;
+  };
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
@@ -890,37 +948,37 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
   cfg.numAttrs = 2;
   cfg.stream = st;
   cfg.blockDim = dim3(ATT_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  // Cluster size: each CTA of a cluster of cs takes ceil(chunks / cs) chunks, and the
-  // (request, kv head) clusters run in waves of as many as the device holds at once.
-  // Estimated time ~ waves x (chunks per CTA + fixed cost of a CTA, ~4 chunks).
-  const int total = a.Hkv * a.B * G;
-  const int cmax = g_att_cluster ? g_att_cluster : 8;
-  int best_cs = 0;
-  long long best_cost = 0;
-  for (int cs = 1; cs <= cmax; ++cs) {
-    if (cs > a.max_splits) break;
-    const int nca = active_clusters(tc, cs, smem);
-    if (nca <= 0) continue;
-    const long long waves = (total + nca - 1) / nca;
-    const long long cost = waves * ((a.max_splits + cs - 1) / cs + 4);
-    if (!best_cs || cost < best_cost || (cost == best_cost && cs > best_cs)) {
-      best_cs = cs;
-      best_cost = cost;
-    }
-  }
-  // tuning override: EAGLE_ATTN_CLUSTER = a cluster size to use when the device holds such
-  // clusters (sweeps of the launch shape); unset or 0 keeps the cost model's choice
-  if (const char* ov = getenv("EAGLE_ATTN_CLUSTER")) {
-    const int cs = atoi(ov);
-    if (cs >= 1 && cs <= cmax && cs <= a.max_splits && active_clusters(tc, cs, smem) > 0) best_cs = cs;
-  }
-  if (!best_cs) return cudaErrorInvalidConfiguration;
+  int best_cs = 0, ch = 0, stages = 0;
+  long long cost = 0;
   if (tc) {
+    // Tensor-core kernel over 64-key tiles, as many ring slots as fit but no more than a
+    // CTA's tiles need (at least four: the final per-vector state, qv x 132 floats, is
+    // parked in the ring); with 8 or more tiles per CTA, 128-key tiles instead (half the
+    // instructions and barrier round trips per key; three 64 KB slots).
+    int st64 = ua_max_stages(64);
+    while (st64 > 4 && ua_smem_bytes(64, st64) > g_ua_smem_cap) --st64;
+    if (ua_smem_bytes(64, st64) > g_ua_smem_cap) return cudaErrorInvalidConfiguration;
+    best_cs = plan(64, a.max_splits, ua_smem_bytes(64, st64), cost);
+    if (!best_cs) return cudaErrorInvalidConfiguration;
     const int per_cta = (a.max_splits + best_cs - 1) / best_cs;   // tiles, the tree tile's two slots included
-    // (at least four: two CTAs of this kernel never share an SM, whose TMEM holds one)
-    stages = std::max(4, std::min(stages, per_cta + 1));
-    cfg.dynamicSmemBytes = ua_smem_bytes(stages);
+    ch = 64;
+    stages = std::max(4, std::min(st64, per_cta + 1));
+    const int st128 = ua_max_stages(128);
+    if (per_cta >= 8 && ua_smem_bytes(128, st128) <= g_ua_smem_cap) {
+      long long c128 = 0;
+      const int cs128 = plan(128, a.max_splits / 2 + 1, ua_smem_bytes(128, st128), c128);
+      if (cs128) {
+        best_cs = cs128;
+        ch = 128;
+        stages = st128;
+      }
+    }
+    cfg.dynamicSmemBytes = ua_smem_bytes(ch, stages);
+  } else {
+    const size_t smem = attn_smem_bytes(qv, a.hd);
+    best_cs = plan(0, a.max_splits, smem, cost);
+    if (!best_cs) return cudaErrorInvalidConfiguration;
+    cfg.dynamicSmemBytes = smem;
   }
   attr[1].val.clusterDim.x = best_cs;
   attr[1].val.clusterDim.y = 1;
@@ -935,7 +993,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
     const long long tokens = static_cast<long long>(a.B) * a.max_prefix;
     if (tokens > 0 && (!make_kv_map(&tmk, a.k_cache, tokens, a.Hkv) || !make_kv_map(&tmv, a.v_cache, tokens, a.Hkv)))
       return cudaErrorInvalidValue;
-    return cudaLaunchKernelEx(&cfg, tree_attention_tc_kernel, tmk, tmv, a, stages);
+    if (ch == 128) return cudaLaunchKernelEx(&cfg, tree_attention_tc_kernel<128>, tmk, tmv, a, stages);
+    return cudaLaunchKernelEx(&cfg, tree_attention_tc_kernel<64>, tmk, tmv, a, stages);
   }
   return cudaLaunchKernelEx(&cfg, tree_attention_kernel, a);
 }
