@@ -964,7 +964,13 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl) {
     ch = 64;
     stages = std::max(4, std::min(st64, per_cta + 1));
     const int st128 = ua_max_stages(128);
-    if (per_cta >= 8 && ua_smem_bytes(128, st128) <= g_ua_smem_cap) {
+    // tuning / test override: EAGLE_ATTN_TILE = 64 or 128 keys per tile; unset keeps the rule
+    int want = per_cta >= 8 ? 128 : 64;
+    if (const char* ov = getenv("EAGLE_ATTN_TILE")) {
+      const int v = atoi(ov);
+      if (v == 64 || v == 128) want = v;
+    }
+    if (want == 128 && ua_smem_bytes(128, st128) <= g_ua_smem_cap) {
       long long c128 = 0;
       const int cs128 = plan(128, a.max_splits / 2 + 1, ua_smem_bytes(128, st128), c128);
       if (cs128) {

@@ -44,6 +44,30 @@ def test_tree_parity_fused_lm_epilogue_many_rows(lib, name, monkeypatch):
     assert rep["ok"], rep["errors"]
 
 
+@pytest.mark.parametrize("name", ["small_dyn", "small_static", "small_fused", "small_max", "small_wide"])
+def test_tree_parity_attention_128_key_tiles(lib, name, monkeypatch):
+    # launches whose CTAs walk few tiles keep 64-key tiles; force the 128-key instance over
+    # the small cases' ragged prefixes (3 to 200 keys: partial, shifted and single tiles)
+    monkeypatch.setenv("EAGLE_ATTN_TILE", "128")
+    cfg = configs.get(name)
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    d, out, tr = run_tree(cfg, W, I)
+    rep = parity.compare(synth.oracle_cfg(cfg), W, I, out, tr, d.info["slots"])
+    assert rep["ok"], rep["errors"]
+
+
+def test_partial_batch_and_empty_prefix_128_key_tiles(lib, monkeypatch):
+    monkeypatch.setenv("EAGLE_ATTN_TILE", "128")
+    cfg = configs.get("small_dyn")
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg, B=2, seed_offset=5)
+    n1 = int(I["cu_seqlens"][2] - I["cu_seqlens"][1])
+    I["k_cache"], I["v_cache"] = I["k_cache"][-n1:], I["v_cache"][-n1:]
+    I["cu_seqlens"] = np.array([0, 0, n1], np.int32)
+    d, out, tr = run_tree(cfg, W, I, max_batch=3)
+    rep = parity.compare(synth.oracle_cfg(cfg), W, I, out, tr, d.info["slots"])
+    assert rep["ok"], rep["errors"]
+
+
 @pytest.mark.parametrize("name", ["small_dyn", "small_static", "small_fused"])
 def test_graph_replay_matches_direct_launch(lib, name):
     cfg = configs.get(name)
