@@ -390,18 +390,38 @@ tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_c
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
-  // blockIdx.z = request * row groups + group (see the SIMT kernel)
+  // blockIdx.z = (request order) * row groups + group (see the SIMT kernel)
   const int G = a.row_groups > 1 ? a.row_groups : 1;
-  const int kvh = blockIdx.y, b = blockIdx.z / G, grp = blockIdx.z - (blockIdx.z / G) * G;
+  const int kvh = blockIdx.y, grp = blockIdx.z - (blockIdx.z / G) * G;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t ring_u = smem_u32(sm);
+  uint8_t* misc = sm + static_cast<uint32_t>(NS) * UA_SLOT;
+  // With several requests the CTAs take them longest prefix first (then by index), so that
+  // when the grid runs in waves the long requests start in the first and the short ones fill
+  // the gaps: the o-th request in that order, ranked from the (input) prefix lengths.
+  int b = blockIdx.z / G;
+  if (a.B > 1) {
+    int* s_req = reinterpret_cast<int*>(misc + 224);
+    const int o = b;
+    auto len = [&](int r) { return min(max(__ldg(a.cu_seqlens + r + 1) - __ldg(a.cu_seqlens + r), 0), a.max_prefix); };
+    for (int r = tid; r < a.B; r += UA_THREADS) {
+      const int lr = len(r);
+      int rk = 0;
+      for (int q = 0; q < a.B; ++q) {
+        const int lq = len(q);
+        rk += (lq > lr || (lq == lr && q < r)) ? 1 : 0;
+      }
+      if (rk == o) *s_req = r;
+    }
+    __syncthreads();
+    b = *s_req;
+  }
   const int rpg = G > 1 ? a.rows_per_group : a.rows_per_req;
   const int rfirst = grp * rpg;
   const int gq = a.Hq / a.Hkv;
   const int qv = max(0, min(rpg, a.rows_per_req - rfirst)) * gq;
   const int row0 = b * a.rows_per_req + rfirst;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const uint32_t ring_u = smem_u32(sm);
-  uint8_t* misc = sm + static_cast<uint32_t>(NS) * UA_SLOT;
   const uint32_t misc_u = smem_u32(misc);
   const uint32_t bar_kvf = misc_u, bar_kve = misc_u + 64, bar_sf = misc_u + 128, bar_pf = misc_u + 144,
                  bar_pe = misc_u + 160, bar_od = misc_u + 176, bar_tg = misc_u + 184, bar_tf = misc_u + 192,
