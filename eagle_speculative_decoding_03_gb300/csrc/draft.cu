@@ -242,6 +242,13 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   *total = cv.off + 256;
 }
 
+// EAGLE-3's fused-feature GEMM takes its operand by TMA when fc's operand buffer
+// ([2 n_max][2d]) holds the B rows' copy ([2B][3d]).
+static bool fc3_by_tma(const eagle_draft* h, int B) {
+  return 2 * static_cast<long long>(h->n_max) * 2 * h->cfg.d >= 2 * static_cast<long long>(B) * 3 * h->cfg.d &&
+         h->cfg.d % 8 == 0;
+}
+
 // ------------------------------------------------------------------- create
 extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, const eagle_draft_weights_t* weights,
                                              eagle_draft_t** out) {
@@ -371,6 +378,7 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
     return fail(EAGLE_ERR_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
   }
   h->launches = 1 + (c.feat_kind == EAGLE_FEAT_FUSED ? 1 : 0) + (h->tc ? 9 : 8) * c.depth + 1;
+  if (h->tc && c.feat_kind == EAGLE_FEAT_FUSED && fc3_by_tma(h, c.max_batch)) h->launches += 1;   // fc3's operand copy
   if (h->tc)   // LM heads over more than 128 rows run as several launches (at max_batch), and
                // those over many rows add one select launch each
     for (int s = 0; s < h->D; ++s) {
@@ -640,7 +648,17 @@ static eagle_status_t enqueue_tree(eagle_draft* h, const eagle_draft_inputs_t* i
   if (c.feat_kind == EAGLE_FEAT_FUSED) {
     // EAGLE-3: g = FC([l; m; h]) for the verified position of every request
     GemmPlan p = base_plan(h, h->tm_fc3, nullptr, h->w.w_fc3, nullptr, d, 3 * d, d);
-    if (h->tc) {
+    if (h->tc && fc3_by_tma(h, B)) {
+      // the rows' operand copy (bf16: hi = the value, lo = 0) in fc's operand buffer (fc's
+      // own copy overwrites it after this GEMM), then a TMA operand like every other GEMM
+      p.args.b.mode = B_BF16;
+      p.args.b.xb = static_cast<const uint16_t*>(in->root_feat);
+      {
+        ProfScope ps(h, EAGLE_K_FC_OPERAND, st);
+        CU(launch_bf16_operand(static_cast<const uint16_t*>(in->root_feat), B, 3 * d, 3 * d, h->fc_hl, st, pdl));
+      }
+      tma_operand(p, h->fc_hl, h->gemm_occ2);
+    } else if (h->tc) {
       p.args.b.mode = B_BF16;
       p.args.b.xb = static_cast<const uint16_t*>(in->root_feat);
     } else {

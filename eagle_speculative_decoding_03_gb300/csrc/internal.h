@@ -198,6 +198,9 @@ struct FcOperandArgs {
   uint16_t* out;              // [2N][2d]
 };
 cudaError_t launch_fc_operand(const FcOperandArgs& a, cudaStream_t st, bool pdl);
+// The operand copy of N bf16 rows x [N][K] (stride ldx; K, ldx multiples of 8): out [2N][K],
+// row 2n = row n of x, row 2n + 1 = zeros (a bf16 value has no low-order part).
+cudaError_t launch_bf16_operand(const uint16_t* x, int N, int K, int ldx, uint16_t* out, cudaStream_t st, bool pdl);
 cudaError_t launch_expand(const TreeArgs& t, int s, const LmPartials& lm, const RowMeta& cur,
                           const RowMeta& next, const ExpandTrace& tr, cudaStream_t st, bool pdl);
 cudaError_t launch_rerank(const TreeArgs& t, const OutArgs& o, cudaStream_t st, bool pdl);

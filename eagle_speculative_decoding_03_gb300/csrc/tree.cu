@@ -93,6 +93,22 @@ __global__ void __launch_bounds__(256) fc_operand_kernel(const FcOperandArgs a) 
   }
 }
 
+// Operand copy of bf16 rows (EAGLE-3's fused root features): row n of x [N][K] (stride ldx)
+// -> rows 2n (the values) and 2n + 1 (zeros) of out [2N][K]; one item = 8 columns.
+__global__ void __launch_bounds__(256) bf16_operand_kernel(const uint16_t* x, int N, int K, int ldx, uint16_t* out) {
+  pdl_trigger();
+  pdl_wait();
+  const int chunks = K / 8;
+  const long long total = static_cast<long long>(N) * chunks;
+  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
+       it += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(it / chunks), c = static_cast<int>(it - static_cast<long long>(n) * chunks);
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(n) * ldx) + c);
+    reinterpret_cast<uint4*>(out + 2 * static_cast<size_t>(n) * K)[c] = v;
+    reinterpret_cast<uint4*>(out + (2 * static_cast<size_t>(n) + 1) * K)[c] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // ---------------------------------------------- merge of LM-head partials
 constexpr int MERGE_MAX_G = 256;   // CTAs (lists) one warp can merge: 8 lists per lane
 
@@ -992,6 +1008,16 @@ cudaError_t launch_rerank(const TreeArgs& t, const OutArgs& o, cudaStream_t st, 
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(t.B), dim3(RR_THREADS), 0, st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, rerank_kernel, t, o);
+}
+
+cudaError_t launch_bf16_operand(const uint16_t* x, int N, int K, int ldx, uint16_t* out, cudaStream_t st, bool pdl) {
+  if (N < 1 || K % 8 != 0 || ldx % 8 != 0) return cudaErrorInvalidValue;
+  const long long items = static_cast<long long>(N) * (K / 8);
+  long long blocks = (items + 255) / 256;
+  if (blocks > 1216) blocks = 1216;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, bf16_operand_kernel, x, N, K, ldx, out);
 }
 
 cudaError_t launch_fc_operand(const FcOperandArgs& a, cudaStream_t st, bool pdl) {
