@@ -229,10 +229,13 @@ EAGLE_DEV void merge_lm_row(const LmPartials& lm, int N, int kp, int n, int kout
 // parts).  Keys are the logits, or (sampled drafting) the logits plus the row's Gumbel
 // noise.  Exact top-k by radix select on order-preserving 32-bit images of the keys, ties
 // to the lower token id.
-constexpr int SEL_THREADS = 512;
+constexpr int SEL_THREADS = 256;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
+constexpr int SEL_GROUPS = 16;                     // lane groups whose maxima give the threshold (k <= 16)
+constexpr int SEL_GROUP_LANES = SEL_THREADS / SEL_GROUPS;
 constexpr int SEL_PER = 16;                        // keys per thread (registers; contiguous in the fallback)
-constexpr int SEL_MAX_SPAN = SEL_THREADS * SEL_PER;   // 8192 keys per part (32 KB + padding)
+constexpr int SEL_MAX_SPAN = SEL_THREADS * SEL_PER;   // 4096 keys per part (16 KB + padding)
+static_assert(SEL_GROUP_LANES <= 32 && 32 % SEL_GROUP_LANES == 0 && SEL_GROUPS >= KMAX, "threshold groups");
 constexpr int SEL_CAP = 256;                       // candidates the threshold gather keeps
 
 // order-preserving image of a float: larger float -> larger integer; NaN -> 0 (below all)
@@ -320,7 +323,7 @@ EAGLE_DEV bool block_select_top(uint32_t kb, int k, SelectScratch& sc) {
 // so the threads of a warp read 32 different banks at every step
 EAGLE_DEV int sel_slot(int i) { return i + (i >> 5); }
 
-__global__ void __launch_bounds__(SEL_THREADS, 2)
+__global__ void __launch_bounds__(SEL_THREADS, 4)
 lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, int k,
                  const unsigned long long* seeds, int sample_rows, int sample_depth, int row0,
                  float* out_max, float* out_sum, float* out_val, int* out_id) {
@@ -328,7 +331,7 @@ lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, i
   __shared__ int hist[256];
   __shared__ float red_m[SEL_WARPS], red_s[SEL_WARPS];
   __shared__ int wsum[SEL_WARPS];
-  __shared__ uint32_t wmax[SEL_WARPS];
+  __shared__ uint32_t wmax[SEL_GROUPS];
   __shared__ int s_bin, s_krem, s_cnt;
   __shared__ uint32_t s_key[KMAX];
   __shared__ int s_id[KMAX];
@@ -383,22 +386,21 @@ lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, i
     m = M;
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-    nvalid += __shfl_xor_sync(0xffffffffu, nvalid, o);
-  }
+  for (int o = SEL_GROUP_LANES / 2; o > 0; o >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) nvalid += __shfl_xor_sync(0xffffffffu, nvalid, o);
+  if (lane % SEL_GROUP_LANES == 0) wmax[tid / SEL_GROUP_LANES] = tmax;   // one maximum per lane group
   if (lane == 0) {
     red_m[warp] = m;
     red_s[warp] = sm;
-    wmax[warp] = tmax;
     wsum[warp] = nvalid;
   }
   if (tid == 0) s_cnt = 0;
   __syncthreads();
-  if (warp == 0) {   // the part's state and threshold from the warps' (one lane each)
+  if (warp == 0) {   // the part's state from the warps' and the threshold from the groups' maxima
     float M = lane < SEL_WARPS ? red_m[lane] : -INFINITY, S = lane < SEL_WARPS ? red_s[lane] : 0.f;
     int tot = lane < SEL_WARPS ? wsum[lane] : 0;
-    const uint32_t xw = lane < SEL_WARPS ? wmax[lane] : 0u;
+    const uint32_t xw = lane < SEL_GROUPS ? wmax[lane] : 0u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float om = __shfl_xor_sync(0xffffffffu, M, o);
@@ -409,15 +411,15 @@ lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, i
       tot += __shfl_xor_sync(0xffffffffu, tot, o);
     }
     const int ks = min(k, tot);   // keys to select (0 when every key is NaN)
-    // theta = the ks-th largest warp maximum (ties by warp) is at most the ks-th largest key
-    // (ks warps hold a key >= theta), so every key of the top ks is >= theta
+    // theta = the ks-th largest group maximum (ties by group) is at most the ks-th largest
+    // key (ks groups hold a key >= theta), so every key of the top ks is >= theta
     int rk = 0;
 #pragma unroll
-    for (int w2 = 0; w2 < SEL_WARPS; ++w2) {
+    for (int w2 = 0; w2 < SEL_GROUPS; ++w2) {
       const uint32_t x2 = __shfl_sync(0xffffffffu, xw, w2);
       rk += x2 > xw || (x2 == xw && w2 < lane);
     }
-    const unsigned hit = __ballot_sync(0xffffffffu, lane < SEL_WARPS && ks > 0 && rk == ks - 1);
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < SEL_GROUPS && ks > 0 && rk == ks - 1);
     const uint32_t th = hit ? __shfl_sync(0xffffffffu, xw, __ffs(hit) - 1) : 0u;
     if (lane == 0) {
       out_max[static_cast<size_t>(n) * parts + part] = M;
