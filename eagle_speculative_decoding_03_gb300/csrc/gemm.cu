@@ -1532,14 +1532,16 @@ bool plan_gemm(GemmPlan& p, int N) {
   if (g.e.kind != EPI_LMHEAD && g.e.kind != EPI_LOGITS && !p.stream_k) {
     int S = std::min(std::min(8, g.KB), sms / g.MT);
     while (S >= 2 && gemm_active_clusters(S) < g.MT) --S;
-    // Long K (fc's 2d, the FFN's d_ff) with one row block stays on stream-K: its CTAs start
-    // on each SM as the previous kernel's CTAs retire, while a cluster waits for S free SMs
-    // at once, and the on-chip reduction saves little against so long a weight stream.  With
-    // two or more row blocks the stream-K partial tiles double and the accumulator loses its
-    // second buffer, so the clusters win there.  (With more than one 16-row chunk the
-    // reduction tail, spread over the ranks, matters more than covering every SM with the
-    // weight stream.)
-    if (S >= 2 && (g.K < 8192 || g.nrb > 1) && (5 * g.MT * S >= 4 * sms || (N > 16 && 2 * g.MT * S >= sms))) {
+    // Long K (fc's 2d, the FFN's d_ff) takes the clusters too when the launch has one 16-row
+    // chunk: the on-chip reduction's shorter tail outweighs the clusters' later start (each
+    // waits for S free SMs where stream-K CTAs start SM by SM as the previous kernel
+    // retires); with more rows the long-K stream-K launches measured faster.  With two or
+    // more row blocks the stream-K partial tiles double and the accumulator loses its second
+    // buffer, so the clusters win there.  (With more than one 16-row chunk the reduction
+    // tail, spread over the ranks, matters more than covering every SM with the weight
+    // stream.)
+    if (S >= 2 && (g.K < 8192 || g.nrb > 1 || N <= 16) &&
+        (5 * g.MT * S >= 4 * sms || (N > 16 && 2 * g.MT * S >= sms))) {
       g.csplit = S;
       p.occ = 1;
     } else if (S < 2 && 4 * g.MT >= 3 * sms && g.MT <= sms * (g.b_tma ? 2 : 1)) {
