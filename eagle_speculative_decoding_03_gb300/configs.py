@@ -126,7 +126,7 @@ SMALL = {
         rms_eps=1e-6, rope_theta=1e4, dtype="bf16", tree="dynamic", depth=4, k=16, m=63,
         B=2, prefix=(1, 90), seed=2005, gamma_jitter=0.1),
     # 24 requests x 4 rows = 96 rows per depth: the LM head stores logits and a select kernel
-    # takes the top-k, over a vocabulary of five select parts (the last one ragged)
+    # takes the top-k, over a vocabulary of 33 select parts of 1024 keys (the last one ragged)
     "small_wide": DraftConfig(
         name="small_wide", d=256, n_heads=2, n_kv_heads=1, head_dim=128, d_ff=640, vocab=33152,
         rms_eps=1e-6, rope_theta=1e4, dtype="bf16", tree="dynamic", depth=3, k=4, m=10,

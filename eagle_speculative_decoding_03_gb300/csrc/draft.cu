@@ -214,7 +214,9 @@ static void carve(eagle_draft* h, char* base, size_t* total) {
   h->lm_val = cv.take<float>(lmn * KMAX);
   h->lm_id = cv.take<int>(lmn * KMAX);
   h->counters = cv.take<int>(16384);
-  h->logits = (h->tc && n >= h->lm_logits_min_rows) ? cv.take<float>(static_cast<size_t>(n) * c.vocab) : nullptr;
+  h->logits = (h->tc && n >= h->lm_logits_min_rows && lm_select_parts(c.vocab) > 0)
+                  ? cv.take<float>(static_cast<size_t>(n) * c.vocab)
+                  : nullptr;
   const size_t nn = static_cast<size_t>(B) * h->max_nodes;
   h->node_tok = cv.take<int>(nn);
   h->node_parent = cv.take<int>(nn);
@@ -318,7 +320,9 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
     return fail(EAGLE_ERR_UNSUPPORTED, "too many query vectors per KV group (%d)", h->qv_max);
   }
   if (h->tc && h->n_max > 256) { delete h; return fail(EAGLE_ERR_UNSUPPORTED, "more than 256 rows per depth"); }
-  h->lm_G = h->tc ? num_sms() : ceil_div(c.vocab, BM);
+  // partial lists per row: the fused epilogue's one per CTA, or the select kernel's one per
+  // vocabulary part
+  h->lm_G = h->tc ? std::max(num_sms(), lm_select_parts(c.vocab)) : ceil_div(c.vocab, BM);
   if (h->lm_G > 256) { delete h; return fail(EAGLE_ERR_UNSUPPORTED, "more than 256 LM-head partial lists (SMs or vocabulary tiles)"); }
 
   cudaError_t e = cudaSuccess;
@@ -386,7 +390,7 @@ extern "C" eagle_status_t eagle_draft_create(const eagle_draft_config_t* cfg, co
       // the LM head (+ a select per launch when it stores logits); up to 256 rows run as one
       // launch of CTA pairs
       const int launches = N <= 2 * MAX_ROWS_PER_BLOCK ? 1 : parts;
-      h->launches += launches - 1 + (N >= h->lm_logits_min_rows ? launches : 0);
+      h->launches += launches - 1 + (N >= h->lm_logits_min_rows && lm_select_parts(c.vocab) > 0 ? launches : 0);
     }
   *out = h;
   return EAGLE_OK;

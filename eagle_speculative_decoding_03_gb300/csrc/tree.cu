@@ -227,16 +227,15 @@ EAGLE_DEV void merge_lm_row(const LmPartials& lm, int N, int kp, int n, int kout
 // then takes, per (row, vocabulary part), the part's log-sum-exp state and its top-k keys,
 // in the per-CTA-list / per-tile-state layout the expansion merges (lists = parts, tiles =
 // parts).  Keys are the logits, or (sampled drafting) the logits plus the row's Gumbel
-// noise.  Exact top-k by radix select on order-preserving 32-bit images of the keys, ties
-// to the lower token id.
-constexpr int SEL_THREADS = 256;
-constexpr int SEL_WARPS = SEL_THREADS / 32;
-constexpr int SEL_GROUPS = 16;                     // lane groups whose maxima give the threshold (k <= 16)
-constexpr int SEL_GROUP_LANES = SEL_THREADS / SEL_GROUPS;
-constexpr int SEL_PER = 16;                        // keys per thread (registers; contiguous in the fallback)
-constexpr int SEL_MAX_SPAN = SEL_THREADS * SEL_PER;   // 4096 keys per part (16 KB + padding)
-static_assert(SEL_GROUP_LANES <= 32 && 32 % SEL_GROUP_LANES == 0 && SEL_GROUPS >= KMAX, "threshold groups");
-constexpr int SEL_CAP = 256;                       // candidates the threshold gather keeps
+// noise.  Exact top-k on order-preserving 32-bit images of the keys, ties to the lower
+// token id.  One warp per part of 1024 keys (32 in each lane's registers): every reduction
+// is a shuffle and nothing waits on a block barrier.
+constexpr int SEL_WARPS = 8;                       // parts per CTA
+constexpr int SEL_PER = 32;                        // keys per lane: key i of a part in lane i % 32
+constexpr int SEL_SPAN = 32 * SEL_PER;             // 1024 keys per part
+constexpr int SEL_MAX_PARTS = 256;                 // lists the expansion merges per row
+constexpr int SEL_CAP = 64;                        // candidates the threshold gather keeps per warp
+static_assert(KMAX <= 32, "the threshold takes the k-th largest of the 32 lane maxima");
 
 // order-preserving image of a float: larger float -> larger integer; NaN -> 0 (below all)
 EAGLE_DEV uint32_t key_bits(float x) {
@@ -319,251 +318,214 @@ EAGLE_DEV bool block_select_top(uint32_t kb, int k, SelectScratch& sc) {
   return keep;
 }
 
-// element i of the part lives at i + i / 32: thread t's contiguous 32 keys start at 33 t,
-// so the threads of a warp read 32 different banks at every step
-EAGLE_DEV int sel_slot(int i) { return i + (i >> 5); }
+// Per-warp scratch: the gathered candidates, and the radix histogram of the fallback.
+struct WarpSelect {
+  uint32_t key[SEL_CAP];
+  int id[SEL_CAP];
+  int hist[256];
+};
 
-__global__ void __launch_bounds__(SEL_THREADS, 4)
-lm_select_kernel(const float* __restrict__ logits, int V, int span, int parts, int k,
+// Descending bitonic sort of one float per lane across the warp (NaN-free inputs).
+EAGLE_DEV float warp_sort_desc(float x, int lane) {
+#pragma unroll
+  for (int k2 = 2; k2 <= 32; k2 <<= 1)
+#pragma unroll
+    for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+      const float y = __shfl_xor_sync(0xffffffffu, x, j2);
+      x = (((lane & j2) == 0) == ((lane & k2) == 0)) ? fmaxf(x, y) : fminf(x, y);
+    }
+  return x;
+}
+
+// Selection values s (the logits, or with SAMPLED the logits plus the row's Gumbel noise) of
+// one 1024-key part, key i = lane + 32 j in s[j] of each lane; past the part: -inf.  The
+// fast path compares floats: theta, the ks-th largest of the 32 lane maxima, is at most the
+// ks-th largest key (ks lanes hold a value >= theta), so the top ks are among the values
+// >= theta (usually a few more than ks); those are ranked exactly on order-preserving keys.
+// A part with NaN, theta = -inf or more than SEL_CAP such values takes the radix select.
+template <bool SAMPLED>
+__global__ void __launch_bounds__(SEL_WARPS * 32, SAMPLED ? 2 : 4)
+lm_select_kernel(const float* __restrict__ logits, int V, int parts, int items, int k,
                  const unsigned long long* seeds, int sample_rows, int sample_depth, int row0,
                  float* out_max, float* out_sum, float* out_val, int* out_id) {
-  extern __shared__ uint32_t su[];                 // [span + span / 32] keys (fallback only)
-  __shared__ int hist[256];
-  __shared__ float red_m[SEL_WARPS], red_s[SEL_WARPS];
-  __shared__ int wsum[SEL_WARPS];
-  __shared__ uint32_t wmax[SEL_GROUPS];
-  __shared__ int s_bin, s_krem, s_cnt;
-  __shared__ uint32_t s_key[KMAX];
-  __shared__ int s_id[KMAX];
-  __shared__ uint32_t s_ckey[SEL_CAP];
-  __shared__ int s_cid[SEL_CAP];
-  __shared__ uint32_t s_theta;
+  __shared__ WarpSelect ws_all[SEL_WARPS];
   pdl_wait();
   pdl_trigger();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = blockIdx.x / parts, part = blockIdx.x - n * parts;   // n: row of this launch
-  const int base = part * span;
-  const int len = max(0, min(span, V - base));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int item = blockIdx.x * SEL_WARPS + warp;
+  if (item >= items) return;   // whole warps only: nothing below waits on the block
+  WarpSelect& ws = ws_all[warp];
+  const unsigned lt = (1u << lane) - 1u;
+  const int n = item / parts, part = item - n * parts;   // n: row of this launch
+  const int base = part * SEL_SPAN;
+  const int len = max(0, min(SEL_SPAN, V - base));
   const float* x = logits + static_cast<size_t>(n) * V + base;
-  int sb = 0, si = 0;
-  unsigned long long sd = 0;
-  if (seeds) {
-    const int gr = row0 + n;
-    sb = gr / sample_rows;
-    si = gr - sb * sample_rows;
-    sd = __ldg(seeds + sb);
-  }
-  // this thread's keys i = tid + 512 j (coalesced), in registers; 0 = no key (past the part,
-  // or NaN)
-  float v[SEL_PER];
-  uint32_t kr[SEL_PER];
+  float s[SEL_PER];
 #pragma unroll
   for (int j = 0; j < SEL_PER; ++j) {
-    const int i = tid + SEL_THREADS * j;
-    v[j] = i < len ? __ldcg(x + i) : -INFINITY;
+    const int i = lane + 32 * j;
+    s[j] = i < len ? __ldcg(x + i) : -INFINITY;
   }
-  float m = -INFINITY;
+  // the part's log-sum-exp state: its maximum m, and the sum of exp(logit - m) (NaN when a
+  // logit is NaN: the maximum skips NaN, the sum does not)
+  float lmax = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < SEL_PER; ++j) m = fmaxf(m, v[j]);
-  float sm = 0.f;
-  uint32_t tmax = 0u;
-  int nvalid = 0;
+  for (int j = 0; j < SEL_PER; ++j) lmax = fmaxf(lmax, s[j]);
+  float m = lmax;
 #pragma unroll
-  for (int j = 0; j < SEL_PER; ++j) {
-    sm += v[j] == -INFINITY ? 0.f : __expf(v[j] - m);   // (a NaN logit makes the sum NaN)
-    const int i = tid + SEL_THREADS * j;
-    kr[j] = i < len ? key_bits(seeds ? v[j] + token_gumbel(base + i, si, sample_depth, sd) : v[j]) : 0u;
-    tmax = max(tmax, kr[j]);
-    nvalid += kr[j] != 0u;
-  }
-  // the part's log-sum-exp state
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float om = __shfl_xor_sync(0xffffffffu, m, o);
-    const float os = __shfl_xor_sync(0xffffffffu, sm, o);
-    const float M = fmaxf(m, om);
-    sm = (m == -INFINITY ? 0.f : sm * expf(m - M)) + (om == -INFINITY ? 0.f : os * expf(om - M));
-    m = M;
-  }
-#pragma unroll
-  for (int o = SEL_GROUP_LANES / 2; o > 0; o >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) nvalid += __shfl_xor_sync(0xffffffffu, nvalid, o);
-  if (lane % SEL_GROUP_LANES == 0) wmax[tid / SEL_GROUP_LANES] = tmax;   // one maximum per lane group
-  if (lane == 0) {
-    red_m[warp] = m;
-    red_s[warp] = sm;
-    wsum[warp] = nvalid;
-  }
-  if (tid == 0) s_cnt = 0;
-  __syncthreads();
-  if (warp == 0) {   // the part's state from the warps' and the threshold from the groups' maxima
-    float M = lane < SEL_WARPS ? red_m[lane] : -INFINITY, S = lane < SEL_WARPS ? red_s[lane] : 0.f;
-    int tot = lane < SEL_WARPS ? wsum[lane] : 0;
-    const uint32_t xw = lane < SEL_GROUPS ? wmax[lane] : 0u;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float om = __shfl_xor_sync(0xffffffffu, M, o);
-      const float os = __shfl_xor_sync(0xffffffffu, S, o);
-      const float MM = fmaxf(M, om);
-      S = (M == -INFINITY ? 0.f : S * expf(M - MM)) + (om == -INFINITY ? 0.f : os * expf(om - MM));
-      M = MM;
-      tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    }
-    const int ks = min(k, tot);   // keys to select (0 when every key is NaN)
-    // theta = the ks-th largest group maximum (ties by group) is at most the ks-th largest
-    // key (ks groups hold a key >= theta), so every key of the top ks is >= theta
-    int rk = 0;
-#pragma unroll
-    for (int w2 = 0; w2 < SEL_GROUPS; ++w2) {
-      const uint32_t x2 = __shfl_sync(0xffffffffu, xw, w2);
-      rk += x2 > xw || (x2 == xw && w2 < lane);
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, lane < SEL_GROUPS && ks > 0 && rk == ks - 1);
-    const uint32_t th = hit ? __shfl_sync(0xffffffffu, xw, __ffs(hit) - 1) : 0u;
-    if (lane == 0) {
-      out_max[static_cast<size_t>(n) * parts + part] = M;
-      out_sum[static_cast<size_t>(n) * parts + part] = S;
-      s_krem = ks;
-      s_theta = th;
-    }
-  }
-  __syncthreads();
-  const int ksel = s_krem;
-  const uint32_t theta = s_theta;
-  // fast path: the keys >= theta (usually a few more than ksel), ranked exactly (larger key,
-  // then lower id); more than SEL_CAP of them: the radix select below
-  if (ksel > 0 && theta != 0u) {
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float ms = m == -INFINITY ? 0.f : m;
+  int ks = min(k, len);   // keys to select when no logit is NaN
+  float sm = 0.f, theta;
+  int cnt = 0;
+  if (!SAMPLED) {
+    theta = __shfl_sync(0xffffffffu, warp_sort_desc(lmax, lane), ks - 1);
 #pragma unroll
     for (int j = 0; j < SEL_PER; ++j) {
-      if (kr[j] >= theta) {
-        const int slot = atomicAdd(&s_cnt, 1);
-        if (slot < SEL_CAP) {
-          s_ckey[slot] = kr[j];
-          s_cid[slot] = base + tid + SEL_THREADS * j;
-        }
+      sm += __expf(s[j] - ms);
+      cnt += s[j] >= theta;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < SEL_PER; ++j) sm += __expf(s[j] - ms);
+    // Gumbel noise of token t = base + lane + 32 j: word j % 4 of the Philox block of
+    // counter (32 (t / 128) + t % 32, row, depth, 0), shared by j = 4q .. 4q + 3
+    const int gr = row0 + n, sb = gr / sample_rows;
+    const unsigned long long sd = __ldg(seeds + sb);
+    lmax = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < SEL_PER / 4; ++q) {
+      const uint4 w = philox4x32_10(make_uint4(32u * static_cast<uint32_t>((base >> 7) + q) + lane,
+                                               static_cast<uint32_t>(gr - sb * sample_rows),
+                                               static_cast<uint32_t>(sample_depth), 0u),
+                                    static_cast<uint32_t>(sd), static_cast<uint32_t>(sd >> 32));
+      const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * q + e;
+        if (lane + 32 * j < len) s[j] += gumbel_of_word(wd[e]);
+        lmax = fmaxf(lmax, s[j]);
       }
     }
+    theta = __shfl_sync(0xffffffffu, warp_sort_desc(lmax, lane), ks - 1);
+#pragma unroll
+    for (int j = 0; j < SEL_PER; ++j) cnt += s[j] >= theta;
   }
-  __syncthreads();
-  const int nc = s_cnt;
-  if (ksel == 0 || (theta != 0u && nc <= SEL_CAP)) {
-    const size_t o = (static_cast<size_t>(n) * parts + part) * k;
-    if (ksel > 0 && tid < nc) {
-      const uint32_t kk = s_ckey[tid];
-      const int id = s_cid[tid];
-      int rank = 0;
-      for (int j = 0; j < nc; ++j) rank += s_ckey[j] > kk || (s_ckey[j] == kk && s_cid[j] < id);
-      if (rank < ksel) {
-        out_val[o + rank] = key_float(kk);
-        out_id[o + rank] = id;
-      }
-    }
-    if (tid >= ksel && tid < k) {
-      out_val[o + tid] = -INFINITY;
-      out_id[o + tid] = -1;
-    }
-    return;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+  int incl = cnt;   // inclusive prefix of the counts over lanes
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
   }
-  // fallback (many keys tie around the k-th): stage the keys, contiguous ranges per thread
-#pragma unroll
-  for (int j = 0; j < SEL_PER; ++j) {
-    const int i = tid + SEL_THREADS * j;
-    if (i < span) su[sel_slot(i)] = kr[j];
+  int nc = __shfl_sync(0xffffffffu, incl, 31);
+  if (lane == 0) {
+    out_max[static_cast<size_t>(n) * parts + part] = m;
+    out_sum[static_cast<size_t>(n) * parts + part] = sm;
   }
-  __syncthreads();
-  const int i0 = tid * SEL_PER, i1 = min(span, i0 + SEL_PER);
-  uint32_t prefix = 0u, pmask = 0u;
-  for (int shift = 24; shift >= 0 && ksel > 0; shift -= 8) {
-    if (tid < 256) hist[tid] = 0;
-    __syncthreads();
-    for (int i = i0; i < i1; ++i) {
-      const uint32_t kb = su[sel_slot(i)];
-      if (kb != 0u && (kb & pmask) == prefix) atomicAdd(hist + ((kb >> shift) & 255u), 1);
+  if (sm == sm && theta > -INFINITY && nc <= SEL_CAP) {
+    int pos = incl - cnt;
+#pragma unroll
+    for (int j = 0; j < SEL_PER; ++j)
+      if (s[j] >= theta) {
+        ws.key[pos] = key_bits(s[j]);
+        ws.id[pos] = base + lane + 32 * j;
+        ++pos;
+      }
+  } else {
+    // radix select on 8-bit digits of the keys (0 = past the part or NaN) from the top, then
+    // the keys equal to the k-th in id order; the keys replace the values in s (their bits)
+    int nv = 0;
+#pragma unroll
+    for (int j = 0; j < SEL_PER; ++j) {
+      const uint32_t kb = lane + 32 * j < len ? key_bits(s[j]) : 0u;
+      nv += kb != 0u;
+      s[j] = __uint_as_float(kb);
     }
-    __syncthreads();
-    if (warp == 0) {   // the bin holding the krem-th largest, scanning down from bin 255
-      int c[8], tot = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = hist[255 - (lane * 8 + j)];
-        tot += c[j];
-      }
-      int incl = tot;   // inclusive prefix over lanes (bins 255 .. down)
+    for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
+    ks = min(k, nv);
+    uint32_t prefix = 0u, pmask = 0u;
+    int krem = ks;
+    for (int shift = 24; shift >= 0 && ks > 0; shift -= 8) {
+      for (int b = lane; b < 256; b += 32) ws.hist[b] = 0;
+      __syncwarp();
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int excl = incl - tot;
-      const int krem = s_krem;
-      if (excl < krem && incl >= krem) {
-        int run = excl;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (run < krem && run + c[j] >= krem) {
-            s_bin = 255 - (lane * 8 + j);
-            s_cnt = run;   // keys in higher bins
-          }
-          run += c[j];
-        }
+      for (int j = 0; j < SEL_PER; ++j) {
+        const uint32_t kb = __float_as_uint(s[j]);
+        if (kb != 0u && (kb & pmask) == prefix) atomicAdd(ws.hist + ((kb >> shift) & 255u), 1);
       }
       __syncwarp();
-      if (lane == 0) s_krem = krem - s_cnt;
-    }
-    __syncthreads();
-    prefix |= static_cast<uint32_t>(s_bin) << shift;
-    pmask |= 255u << shift;
-  }
-  // keys above the k-th: all of them; keys equal to it: the lowest ids, in id order
-  const uint32_t kth = prefix;
-  const int need_eq = ksel > 0 ? s_krem : 0;   // equal keys still needed after the higher ones
-  int n_eq = 0;
-  for (int i = i0; i < i1; ++i) n_eq += ksel > 0 && su[sel_slot(i)] == kth;
-  int incl = n_eq;   // block-exclusive prefix of the equal keys, in thread (= id) order
+      int c[8], tot = 0;   // bins 255 - (8 lane + jj), scanned from the top
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  if (tid == 0) s_cnt = 0;
-  __syncthreads();
-  int before = incl - n_eq;
-  for (int w = 0; w < warp; ++w) before += wsum[w];
-  if (ksel > 0) {
-    for (int i = i0; i < i1; ++i) {
-      const uint32_t kb = su[sel_slot(i)];
-      bool take = kb > kth && kb != 0u;
-      if (kb == kth) {
-        take = before < need_eq;
-        ++before;
+      for (int jj = 0; jj < 8; ++jj) {
+        c[jj] = ws.hist[255 - (lane * 8 + jj)];
+        tot += c[jj];
       }
-      if (take) {
-        const int slot = atomicAdd(&s_cnt, 1);
-        if (slot < KMAX) {
-          s_key[slot] = kb;
-          s_id[slot] = base + i;
+      int hi = tot;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, hi, d);
+        if (lane >= d) hi += y;
+      }
+      const int excl = hi - tot;
+      int bin = 0, above = 0;
+      if (excl < krem && hi >= krem) {
+        int run = excl;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (run < krem && run + c[jj] >= krem) {
+            bin = 255 - (lane * 8 + jj);
+            above = run;
+          }
+          run += c[jj];
         }
       }
+      const unsigned who = __ballot_sync(0xffffffffu, excl < krem && hi >= krem);
+      const int src = __ffs(who) - 1;
+      bin = __shfl_sync(0xffffffffu, bin, src);
+      above = __shfl_sync(0xffffffffu, above, src);
+      prefix |= static_cast<uint32_t>(bin) << shift;
+      pmask |= 255u << shift;
+      krem -= above;
+      __syncwarp();   // every lane has read the histogram before the next pass clears it
+    }
+    // keys above the k-th: all; keys equal to it: the krem of lowest id (id order: j, then lane)
+    int eq_seen = 0, taken = 0;
+#pragma unroll
+    for (int j = 0; j < SEL_PER; ++j) {
+      const uint32_t kb = __float_as_uint(s[j]);
+      const bool eq = ks > 0 && kb == prefix;
+      const unsigned em = __ballot_sync(0xffffffffu, eq);
+      const bool take = ks > 0 && (kb > prefix || (eq && eq_seen + __popc(em & lt) < krem));
+      eq_seen += __popc(em);
+      const unsigned tm = __ballot_sync(0xffffffffu, take);
+      if (take) {
+        const int pos = taken + __popc(tm & lt);
+        ws.key[pos] = kb;
+        ws.id[pos] = base + lane + 32 * j;
+      }
+      taken += __popc(tm);
+    }
+    nc = taken;   // == ks
+  }
+  __syncwarp();
+  // the ks best candidates, best first (larger key, then lower id); empty places: -inf / -1
+  const size_t o = (static_cast<size_t>(n) * parts + part) * k;
+  for (int c = lane; c < nc; c += 32) {
+    const uint32_t kk = ws.key[c];
+    const int id = ws.id[c];
+    int rank = 0;
+    for (int c2 = 0; c2 < nc; ++c2) rank += ws.key[c2] > kk || (ws.key[c2] == kk && ws.id[c2] < id);
+    if (rank < ks) {
+      out_val[o + rank] = key_float(kk);
+      out_id[o + rank] = id;
     }
   }
-  __syncthreads();
-  // the selected keys, best first (larger key, then lower id); empty places: -inf / -1
-  if (tid < k) {
-    const size_t o = (static_cast<size_t>(n) * parts + part) * k;
-    if (tid < ksel) {
-      const uint32_t kb = s_key[tid];
-      const int id = s_id[tid];
-      int rank = 0;
-      for (int j = 0; j < ksel; ++j)
-        rank += s_key[j] > kb || (s_key[j] == kb && s_id[j] < id);
-      out_val[o + rank] = key_float(kb);
-      out_id[o + rank] = id;
-    } else {
-      out_val[o + tid] = -INFINITY;
-      out_id[o + tid] = -1;
-    }
+  if (lane >= ks && lane < k) {
+    out_val[o + lane] = -INFINITY;
+    out_id[o + lane] = -1;
   }
 }
 
@@ -981,9 +943,6 @@ cudaError_t tree_setup_attributes() {
   cudaError_t e = cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sizeof(float2) * EXR_CAND));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(lm_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sizeof(uint32_t) * (SEL_MAX_SPAN + SEL_MAX_SPAN / 32)));
-  if (e != cudaSuccess) return e;
   return allow_max_smem(reinterpret_cast<const void*>(lm_merge_kernel));
 }
 
@@ -1043,21 +1002,26 @@ cudaError_t launch_lm_merge(const LmPartials& lm, int N, int k, int* ids, float*
 
 namespace eagle {
 
-int lm_select_parts(int vocab) { return (vocab + SEL_MAX_SPAN - 1) / SEL_MAX_SPAN; }
+int lm_select_parts(int vocab) {
+  const int parts = (vocab + SEL_SPAN - 1) / SEL_SPAN;
+  return vocab > 0 && parts <= SEL_MAX_PARTS ? parts : 0;
+}
 
 cudaError_t launch_lm_select(const float* logits, int N, int vocab, int k, const unsigned long long* seeds,
                              int sample_rows, int sample_depth, int row0, const LmPartials& lm, cudaStream_t st,
                              bool pdl) {
   const int parts = lm_select_parts(vocab);
-  int span = (vocab + parts - 1) / parts;
-  span = (span + 31) & ~31;
-  if (span > SEL_MAX_SPAN || k < 1 || k > KMAX || lm.G != parts || lm.T != parts) return cudaErrorInvalidValue;
+  if (parts == 0 || N < 1 || k < 1 || k > KMAX || lm.G != parts || lm.T != parts) return cudaErrorInvalidValue;
+  if (seeds && sample_rows < 1) return cudaErrorInvalidValue;
+  const long long items = static_cast<long long>(N) * parts;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(N * parts), dim3(SEL_THREADS),
-                                    sizeof(uint32_t) * (span + span / 32), st, pdl, attr);
-  return cudaLaunchKernelEx(&cfg, lm_select_kernel, logits, vocab, span, parts, k, seeds, sample_rows, sample_depth,
-                            row0, lm.max + static_cast<size_t>(row0) * parts, lm.sum + static_cast<size_t>(row0) * parts,
-                            lm.val + static_cast<size_t>(row0) * parts * k, lm.id + static_cast<size_t>(row0) * parts * k);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(static_cast<unsigned>((items + SEL_WARPS - 1) / SEL_WARPS)),
+                                    dim3(SEL_WARPS * 32), 0, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, seeds ? lm_select_kernel<true> : lm_select_kernel<false>, logits, vocab, parts,
+                            static_cast<int>(items), k, seeds, sample_rows, sample_depth, row0,
+                            lm.max + static_cast<size_t>(row0) * parts,
+                            lm.sum + static_cast<size_t>(row0) * parts, lm.val + static_cast<size_t>(row0) * parts * k,
+                            lm.id + static_cast<size_t>(row0) * parts * k);
 }
 
 }  // namespace eagle

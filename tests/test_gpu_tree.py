@@ -107,6 +107,26 @@ def test_zero_lm_head_ties(lib):
     assert out["tokens"][0][1:cfg.k + 1].tolist() == list(range(cfg.k))
 
 
+@pytest.mark.parametrize("name", ["small_wide", "small_pairs"])
+def test_select_kernel_ties(lib, name):
+    # depths of 96 / 192 rows store the logits for the select kernel; an LM head of zeros but
+    # one row makes every part a run of equal keys (the radix fallback: the lowest ids win),
+    # with token 5 above or below the ties depending on the row
+    cfg = configs.get(name)
+    W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
+    w = np.zeros_like(W["w_lm"])
+    w[5] = W["w_lm"][5]
+    W["w_lm"] = w
+    d, out, tr = run_tree(cfg, W, I)
+    rep = parity.compare(synth.oracle_cfg(cfg), W, I, out, tr, d.info["slots"])
+    assert rep["ok"], rep["errors"]
+    # the select decisions are exact (equal keys: lowest ids); the frontier and the rerank may
+    # meet path values equal in float64 but not in float32, forced within the margin
+    assert [f for f in rep["forced"] if f[0] == "children"] == []
+    kids = out["tokens"][:, 1:cfg.k + 1]
+    assert all(set(r.tolist()) <= {0, 1, 2, 3, 4, 5} for r in kids)
+
+
 def test_prefix_longer_than_max_prefix_is_reported(lib):
     cfg = configs.get("small_dyn")
     W, I = synth.make_weights(cfg), synth.make_inputs(cfg)
