@@ -209,8 +209,6 @@ cudaError_t launch_lm_merge(const LmPartials& lm, int N, int k, int* ids, float*
 // LM head over many rows, second half: the rows' stored logits [N][vocab] -> per (row, part)
 // log-sum-exp state and top-k keys (logit, or logit + Gumbel noise with seeds), written at
 // rows row0.. of `lm` (G = T = lm_select_parts(vocab)).  N rows of this launch.
-// lm_select_parts: the vocabulary parts of 1024 keys, or 0 past 256 parts (no select kernel:
-// the LM head keeps its fused top-k epilogue).
 int lm_select_parts(int vocab);
 cudaError_t launch_lm_select(const float* logits, int N, int vocab, int k, const unsigned long long* seeds,
                              int sample_rows, int sample_depth, int row0, const LmPartials& lm, cudaStream_t st,

@@ -1002,6 +1002,8 @@ cudaError_t launch_lm_merge(const LmPartials& lm, int N, int k, int* ids, float*
 
 namespace eagle {
 
+// the vocabulary parts of 1024 keys, or 0 past 256 parts (no select kernel: the LM head then
+// keeps its fused top-k epilogue)
 int lm_select_parts(int vocab) {
   const int parts = (vocab + SEL_SPAN - 1) / SEL_SPAN;
   return vocab > 0 && parts <= SEL_MAX_PARTS ? parts : 0;
