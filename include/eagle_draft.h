@@ -207,7 +207,9 @@ EAGLE_API eagle_status_t eagle_draft_tree(eagle_draft_t* handle,
  * cross-CTA merge, on the handle's weights and workspace.
  * a: f32 [N, d] device; N <= n_max; k <= 16.
  * Outputs (device): ids int32 [N, k] sorted by descending logit, logp f32 [N, k],
- * lse f32 [N].  This is the same kernel the tree step launches at every depth. */
+ * lse f32 [N].  This is the kernel the tree step launches at depths of up to 16 rows;
+ * from 17 rows the step's LM head stores the rows' logits and a select kernel takes the
+ * log-sum-exp and top-k per 1024-token part instead. */
 EAGLE_API eagle_status_t eagle_draft_lm_head_topk(eagle_draft_t* handle, const float* a, int32_t N,
                                         int32_t k, int32_t* ids, float* logp, float* lse,
                                         void* stream);
